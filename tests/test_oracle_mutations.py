@@ -1,0 +1,63 @@
+"""Planted mistakes: each mutant copy of the oracle's C source must fail at
+least one pin in test_oracle_pins.py.
+
+This checks that the pins are sharp enough to catch the plausible slips a
+hand-written attention oracle can make (wrong GQA head, swapped K/V, dropped
+scale or max, wrong row order, off-by-one mask, broken merge weight, wrong
+append slot).  Mutants are compiled on the CPU into a temporary directory;
+the real oracle is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import tests.test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "shkv_oracle.c")
+
+MUTANTS = {
+    "gqa_head_modulo": ("const int g = h / G;", "const int g = h % j->Hkv;"),
+    "keys_as_values": ("token_ptr(j, j->v_pages, b, g, t0 + i)", "token_ptr(j, j->k_pages, b, g, t0 + i)"),
+    "no_scale": ("s[i] = j->scale * acc;", "s[i] = acc;"),
+    "max_not_subtracted_in_numerator": ("double p = exp(s[i] - smax) / denom;", "double p = exp(s[i]) / denom;"),
+    "head_major_rows": ("const long r = (long)m * j->Hq + h;", "const long r = (long)h * j->N + m;"),
+    "mask_off_by_one": ("int t1 = j->t_end < L ? j->t_end : L;", "int t1 = j->t_end < L + 1 ? j->t_end : L + 1;"),
+    "lse_without_log": ("*lse = smax + log(denom);", "*lse = smax + denom;"),
+    "merge_weight_sign": ("double w = exp(l - M);", "double w = exp(M - l);"),
+    "append_slot_shift": ("long dst = (((long)page * Hkv + g) * P + pos % P) * (long)D;",
+                          "long dst = (((long)page * Hkv + g) * P + (pos + 1) % P) * (long)D;"),
+    "token_slot_shift": ("return pool + (((long)page * j->Hkv + g) * j->P + t % j->P) * (long)j->D;",
+                         "return pool + (((long)page * j->Hkv + g) * j->P + (t + 1) % j->P) * (long)j->D;"),
+}
+
+PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, mutant_dir, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
+    path_c = os.path.join(mutant_dir, f"{name}.c")
+    path_so = os.path.join(mutant_dir, f"lib{name}.so")
+    with open(path_c, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           "-o", path_so, path_c, "-lm"])
+    monkeypatch.setattr(oracle, "_lib", None)
+    monkeypatch.setattr(oracle, "build", lambda force=False: path_so)
+    failed = []
+    for t in PIN_TESTS:
+        try:
+            t()
+        except (AssertionError, RuntimeError):
+            failed.append(t.__name__)
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert failed, f"no pin caught the planted mistake {name!r}"

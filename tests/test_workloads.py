@@ -1,0 +1,62 @@
+"""Seeded synthetic inputs: determinism, shapes and the length mixes."""
+import math
+
+import numpy as np
+import pytest
+
+from cross_model_shared_gb300 import workloads as W
+
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, -2.5, 1.0 + 2**-9], np.float32)
+    back = W.f32_from_bf16_bits(W.bf16_bits_from_f32(x))
+    # 1+2^-8 is a tie between 1 and 1+2^-7 -> even (1.0); 1+3*2^-8 -> 1+2^-6
+    np.testing.assert_array_equal(back, np.array([1.0, 1.0, 1.0 + 2**-6, -2.5, 1.0], np.float32))
+
+
+@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+def test_configs_are_deterministic_and_consistent(name):
+    a, b = W.make_workload(name), W.make_workload(name)
+    np.testing.assert_array_equal(a.lens_prefill, b.lens_prefill)
+    np.testing.assert_array_equal(a.block_table, b.block_table)
+    P = a.P
+    pages = a.pages_per_request()
+    assert int(pages.sum()) == a.num_pages
+    used = np.concatenate([a.block_table[i, :pages[i]] for i in range(a.B)])
+    assert sorted(used.tolist()) == list(range(a.num_pages))      # a permutation, no sharing
+    assert (a.block_table[np.arange(a.max_pages_per_seq)[None, :] >= pages[:, None]] == -1).all()
+    assert a.Hq % a.Hkv == 0 and (a.lens_final >= 1).all()
+    assert (a.lens_final <= a.max_pages_per_seq * P).all()
+
+
+def test_length_mixes_follow_the_stated_readings():
+    c = W.make_workload("llama8b")
+    assert c.lens_final.min() >= 1024 and c.lens_final.max() <= 8192
+    q8 = W.make_workload("qwen8b")
+    assert q8.lens_final.min() >= 512 and q8.lens_final.max() <= 32768
+    q14 = W.make_workload("qwen14b")
+    assert q14.lens_final.min() >= 1024 and q14.lens_final.max() <= 65536
+    lg = W.make_workload("long")
+    assert (lg.lens_prefill == 131072).all() and (lg.lens_final == 131584).all()
+    assert W.make_workload("tiny").lens_final.tolist() == [256]
+
+
+def test_truncated_lognormal_calibration():
+    """mu is chosen so the truncated mean is 27648 (PrFaaS: mean ~27K)."""
+    mu = W.trunc_lognormal_mu(27648, 1.0, 1024, 65536)
+    rng = np.random.default_rng(0)
+    x = rng.lognormal(mu, 1.0, size=2_000_000)
+    x = x[(x >= 1024) & (x <= 65536)]
+    assert abs(x.mean() / 27648 - 1) < 0.01
+    assert 10.3 < mu < 10.6
+
+
+def test_generators_are_seeded():
+    wl = W.make_workload("tiny")
+    np.testing.assert_array_equal(W.gen_q(wl), W.gen_q(wl))
+    k1, v1 = W.gen_pool(wl)
+    k2, v2 = W.gen_pool(wl)
+    np.testing.assert_array_equal(k1, k2)
+    assert not np.array_equal(k1, v1)
+    f = W.f32_from_bf16_bits(k1)
+    assert abs(f.mean()) < 0.05 and abs(f.std() - 1) < 0.05
