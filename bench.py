@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark: shared-KV multi-decoder paged decode attention on GB300.
+
+One step = one shkv_decode_attention call (one layer of one decode step for
+the whole batch: every decoder's stacked queries against the shared paged
+cache).  The headline value is KV GB/s: the algorithmic bytes of a step
+(unique KV pages + Q + O, each read or written once) divided by the step
+time, summed over ranks.  Also reported: decode steps/s, fraction of the
+measured HBM peak, the same kernel run once per decoder without sharing,
+an end-to-end figure through the C ABI with host buffers, and the fp64
+oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl shkv|reference]
+
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (the path shards by request with no exchange step): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from cross_model_shared_gb300 import workloads as W  # noqa: E402
+
+METRIC = "shared-KV decode attention: KV GB/s (% of HBM peak) and decode steps/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ["cross_model_shared_gb300/csrc/decode_attn.cu", "cross_model_shared_gb300/csrc/shkv_device.cuh"]
+
+
+# ---------------------------------------------------------------------------
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="llama8b", choices=W.CONFIG_ORDER)
+    ap.add_argument("--impl", default="shkv", choices=["shkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_attn_{config}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.lstrip().startswith("#"):
+                    k, _, v = line.partition(":")
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") != kernel_sha():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def step_bytes(wl: W.Workload) -> int:
+    """Algorithmic bytes of one step: unique KV pages + Q read + O written."""
+    qo = 2 * wl.B * wl.rows * wl.D * 2
+    return W.unique_kv_bytes(wl) + qo
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, float("inf"))
+        rows = [s for t, s in self.samples if t0 <= t <= t1 + 0.06] or [s for _, s in self.samples]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float):
+    """Time the fp64 oracle on whole requests (all rows, full context) until
+    the budget is spent.  Returns (KV GB/s over the sampled requests, cores,
+    description)."""
+    import oracle
+    order = np.argsort(wl.lens_final, kind="stable")
+    picks = [int(order[len(order) // 2])]
+    kv_bytes, elapsed, done = 0, 0.0, []
+    i = 0
+    while elapsed < budget_s and i < wl.B:
+        b = picks[0] if i == 0 else int(order[(len(order) // 2 + i) % len(order)])
+        kb, vb, npg = fetch_pages(b)
+        bt = np.arange(npg, dtype=np.int32)[None, :]
+        t0 = time.perf_counter()
+        oracle.decode_attention(q_bits[b:b + 1], kb, vb, bt, np.array([wl.lens_final[b]], np.int32),
+                                n_models=wl.N, hq=wl.Hq, scale=wl.scale)
+        elapsed += time.perf_counter() - t0
+        kv_bytes += npg * wl.P * wl.Hkv * wl.D * 4
+        done.append(b)
+        i += 1
+    desc = (f"{len(done)} whole requests of {wl.name} (all {wl.rows} stacked rows, full context, "
+            f"{sum(int(wl.lens_final[b]) for b in done)} tokens), fp64, {oracle.num_threads()} threads")
+    return kv_bytes / elapsed / 1e9, oracle.num_threads(), desc, elapsed
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = W.make_workload(args.config)
+    q = W.gen_q(wl)
+    rng = np.random.default_rng(wl.seed + 77)
+    R = wl.R
+    units = [(b, g) for b in np.argsort(wl.lens_final) for g in range(wl.Hkv)]
+    # Each step is one (request, KV head) with all R stacked rows over a token
+    # window sized so the whole run stays within a few minutes.
+    total_steps = args.steps + args.warmup
+    budget_per_step = min(2.0, 150.0 / max(1, total_steps))
+    probe_L = int(min(wl.lens_final))
+    kb = W.bf16_bits_from_f32(rng.standard_normal((1, 1, probe_L, wl.D), dtype=np.float32))
+    t0 = time.perf_counter()
+    oracle.decode_attention(q[:1, :R], kb, kb, np.zeros((1, 1), np.int32), np.array([probe_L], np.int32),
+                            n_models=wl.N, hq=wl.G, scale=wl.scale)
+    per_token = (time.perf_counter() - t0) / probe_L
+    window = int(max(wl.P, min(max(wl.lens_final), budget_per_step / max(per_token, 1e-9))))
+    kv_bytes, elapsed = 0, 0.0
+    for s in range(total_steps):
+        b, g = units[s % len(units)]
+        L = int(min(window, wl.lens_final[b]))
+        kp = W.bf16_bits_from_f32(rng.standard_normal((1, 1, L, wl.D), dtype=np.float32))
+        vp = W.bf16_bits_from_f32(rng.standard_normal((1, 1, L, wl.D), dtype=np.float32))
+        qs = np.ascontiguousarray(np.stack([q[b, m * wl.Hq + g * wl.G: m * wl.Hq + (g + 1) * wl.G]
+                                            for m in range(wl.N)]).reshape(1, R, wl.D))
+        t0 = time.perf_counter()
+        oracle.decode_attention(qs, kp, vp, np.zeros((1, 1), np.int32), np.array([L], np.int32),
+                                n_models=wl.N, hq=wl.G, scale=wl.scale)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            elapsed += dt
+            kv_bytes += L * wl.D * 4
+    value = kv_bytes / elapsed / 1e9
+    desc = (f"per step one (request, KV head) of {wl.name} with all {R} stacked rows over up to {window} "
+            f"cached tokens, fp64 oracle, {oracle.num_threads()} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from cross_model_shared_gb300 import SharedKVPool
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl = W.make_workload(args.config)
+    q_bits = W.gen_q(wl)
+    k_dev, v_dev = W.gen_pool_device(wl, device=dev)
+    pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
+                        device=dev, k_pages=k_dev, v_pages=v_dev, initial_seq_lens=wl.lens_prefill)
+    pool.block_table.copy_(torch.from_numpy(wl.block_table).to(dev))
+    append_ms = None
+    if wl.n_append:
+        g = torch.Generator(device=dev).manual_seed(404)
+        shape = (wl.B, wl.n_append, wl.Hkv, wl.D)
+        kn = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pool.append_kv(kn, vn)
+        e1.record()
+        torch.cuda.synchronize()
+        append_ms = e0.elapsed_time(e1)
+        del kn, vn
+    q = torch.from_numpy(q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws_t = pool.workspace(wl.B, wl.N, wl.Hq)
+    torch.cuda.synchronize()
+
+    def step():
+        pool.decode_attention(q, wl.N, scale=wl.scale, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    flags = pool.check_errors()
+    if flags:
+        raise RuntimeError(f"device error bits 0x{flags:x} during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flags = pool.check_errors()
+    if flags:
+        raise RuntimeError(f"device error bits 0x{flags:x} in the timed region")
+
+    ms_per_step = ms / args.steps
+    nbytes = step_bytes(wl)
+    value = ws * nbytes * args.steps / (ms * 1e-3) / 1e9
+    per_gpu = nbytes / (ms_per_step * 1e-3) / 1e9
+
+    # --- the same kernel once per decoder, without sharing (N launches/step)
+    q_models = [q[:, m * wl.Hq:(m + 1) * wl.Hq].contiguous() for m in range(wl.N)]
+    out_m = [torch.empty_like(x) for x in q_models]
+    u_steps = max(10, min(args.steps, 500))
+    for m in range(wl.N):
+        pool.decode_attention(q_models[m], 1, scale=wl.scale, out=out_m[m])
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(u_steps):
+        for m in range(wl.N):
+            pool.decode_attention(q_models[m], 1, scale=wl.scale, out=out_m[m])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    unshared_ms = ev0.elapsed_time(ev1) / u_steps
+
+    # --- end to end through the C ABI: pinned host q in, host out back, per step
+    q_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_host.copy_(q.cpu())
+    out_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_e2e = torch.empty_like(q)
+    e_steps = max(10, min(args.steps, 1000))
+
+    def e2e_step():
+        q_e2e.copy_(q_host, non_blocking=True)
+        pool.decode_attention(q_e2e, wl.N, scale=wl.scale, out=out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = ws * nbytes * e_steps / e2e_s / 1e9
+    qbytes = q.numel() * 2
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        def fetch(b):
+            npg = int((wl.lens_final[b] + wl.P - 1) // wl.P)
+            ids = torch.from_numpy(wl.block_table[b, :npg].astype(np.int64)).to(dev)
+            kb = k_dev.index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16)
+            vb = v_dev.index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16)
+            return kb, vb, npg
+        v_cpu, cores, desc, secs = cpu_oracle_sample(wl, q_bits, fetch, args.cpu_budget_s)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": round(secs, 2)}
+
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic(wl.name)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": wl.name, "batch": wl.B, "decoders": wl.N, "hq_per_decoder": wl.Hq, "hkv": wl.Hkv,
+                "head_dim": wl.D, "page_size": wl.P, "rows_per_kv_head": wl.R,
+                "mean_context": float(wl.lens_final.mean()), "kv_bytes_per_step": W.unique_kv_bytes(wl),
+                "step_bytes": nbytes, "l2": "inputs larger than L2" if W.unique_kv_bytes(wl) > 2 * 129e6
+                else "L2-resident working set (warm)", "parallelism": f"replicas x{ws}",
+            },
+            "steps_per_s": 1e3 / ms_per_step,
+            "decoder_tokens_per_s": wl.B * wl.N * 1e3 / ms_per_step,
+            "pct_of_hbm_peak": {"measured_copy": 100 * per_gpu / peak, "nominal_8tbs": 100 * per_gpu / NOMINAL_HBM_GBS},
+            "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
+                         "frac": per_gpu / peak, "peak_kind": peak_kind, "traffic": traffic},
+            "unshared": {"ms_per_step": unshared_ms, "launches_per_step": wl.N,
+                         "speedup_of_sharing": unshared_ms / ms_per_step},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": qbytes, "d2h_bytes_per_step": qbytes,
+                    "steps": e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        if append_ms is not None:
+            line["append"] = {"ms": append_ms, "bytes": 4 * wl.B * wl.n_append * wl.Hkv * wl.D * 2}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+"""ctypes binding of libshkv (include/shkv.h).
+
+Argument marshalling only: every function here forwards to the C entry
+point of the same name.  The library is built in-tree by
+``cross_model_shared_gb300.build``; if it is missing, loading fails loudly
+(there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libshkv.so")
+
+SHKV_OK = 0
+SHKV_ERR_INVALID_ARG = 1
+SHKV_ERR_CAPACITY = 2
+SHKV_ERR_UNSUPPORTED = 3
+SHKV_ERR_CUDA = 4
+SHKV_ERR_DEVICE = 5
+
+SHKV_ERRF_PAGE_OOB = 0x1
+SHKV_ERRF_SEQ_LEN = 0x2
+SHKV_ERRF_TIMEOUT = 0x4
+
+SHKV_MAX_BATCH = 1024
+
+# Every symbol include/shkv.h declares.
+EXPORTS = [
+    "shkv_pool_create", "shkv_pool_destroy", "shkv_pool_set_seq_lens", "shkv_pool_get_seq_lens",
+    "shkv_append_kv", "shkv_decode_workspace_size", "shkv_decode_attention", "shkv_splitkv_merge",
+    "shkv_check_errors", "shkv_plan_decode", "shkv_status_string",
+]
+
+
+class shkv_pool_config(ctypes.Structure):
+    _fields_ = [
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("max_batch", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("k_pages", ctypes.c_void_p),
+        ("v_pages", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("seq_lens", ctypes.c_void_p),
+        ("error_word", ctypes.c_void_p),
+        ("initial_seq_lens", ctypes.c_void_p),
+    ]
+
+
+class ShkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libshkv.so (built in-tree).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libshkv.so not found at {LIB_PATH}: build it with "
+                          "`python -m cross_model_shared_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, u32p, i32p = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p
+    sig = {
+        "shkv_pool_create": [ctypes.POINTER(shkv_pool_config), ctypes.POINTER(vp)],
+        "shkv_pool_destroy": [vp],
+        "shkv_pool_set_seq_lens": [vp, i32, i32p, vp],
+        "shkv_pool_get_seq_lens": [vp, i32, i32p],
+        "shkv_append_kv": [vp, i32, i32, vp, vp, vp],
+        "shkv_decode_workspace_size": [vp, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
+        "shkv_decode_attention": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
+        "shkv_splitkv_merge": [i32, i32, i32, i32, vp, vp, vp, vp, vp],
+        "shkv_check_errors": [vp, vp, u32p],
+        "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.shkv_status_string.argtypes = [ctypes.c_int]
+    lib.shkv_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().shkv_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> int:
+    if status != SHKV_OK:
+        raise ShkvError(status, what)
+    return status
+
+
+# --- thin wrappers, one per C entry point (pointers are ints) -------------
+def shkv_pool_create(cfg: shkv_pool_config) -> int:
+    h = ctypes.c_void_p()
+    _check(load().shkv_pool_create(ctypes.byref(cfg), ctypes.byref(h)), "shkv_pool_create")
+    return h.value
+
+
+def shkv_pool_destroy(pool: int) -> None:
+    _check(load().shkv_pool_destroy(pool), "shkv_pool_destroy")
+
+
+def shkv_pool_set_seq_lens(pool: int, batch: int, lens_ptr: int, stream: int) -> None:
+    _check(load().shkv_pool_set_seq_lens(pool, batch, lens_ptr, stream), "shkv_pool_set_seq_lens")
+
+
+def shkv_pool_get_seq_lens(pool: int, batch: int, lens_ptr: int) -> None:
+    _check(load().shkv_pool_get_seq_lens(pool, batch, lens_ptr), "shkv_pool_get_seq_lens")
+
+
+def shkv_append_kv(pool: int, batch: int, n_new: int, k_new: int, v_new: int, stream: int) -> None:
+    _check(load().shkv_append_kv(pool, batch, n_new, k_new, v_new, stream), "shkv_append_kv")
+
+
+def shkv_decode_workspace_size(pool: int, batch: int, n_models: int, hq: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().shkv_decode_workspace_size(pool, batch, n_models, hq, ctypes.byref(n)),
+           "shkv_decode_workspace_size")
+    return n.value
+
+
+def shkv_decode_attention(pool: int, batch: int, n_models: int, hq: int, q: int, scale: float, out: int,
+                          lse_out: int, workspace: int, workspace_bytes: int, stream: int) -> None:
+    _check(load().shkv_decode_attention(pool, batch, n_models, hq, q, scale, out, lse_out, workspace,
+                                        workspace_bytes, stream), "shkv_decode_attention")
+
+
+def shkv_splitkv_merge(n_splits: int, batch: int, rows: int, head_dim: int, o_part: int, lse_part: int,
+                       out: int, lse_out: int, stream: int) -> None:
+    _check(load().shkv_splitkv_merge(n_splits, batch, rows, head_dim, o_part, lse_part, out, lse_out, stream),
+           "shkv_splitkv_merge")
+
+
+def shkv_check_errors(pool: int, stream: int) -> int:
+    """Returns the device error bits (0 if none); raises only on CUDA errors."""
+    flags = ctypes.c_uint32()
+    st = load().shkv_check_errors(pool, stream, ctypes.byref(flags))
+    if st not in (SHKV_OK, SHKV_ERR_DEVICE):
+        raise ShkvError(st, "shkv_check_errors")
+    return flags.value
+
+
+def shkv_plan_decode(lens, page_size: int, num_kv_heads: int, max_ctas: int):
+    """Host-only split plan: (cta_begin list, num_ctas, num_splits)."""
+    import numpy as np
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    begin = np.zeros(max_ctas + 1, dtype=np.int64)
+    nc, ns = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().shkv_plan_decode(len(lens), lens.ctypes.data, page_size, num_kv_heads, max_ctas,
+                                   begin.ctypes.data, ctypes.byref(nc), ctypes.byref(ns)), "shkv_plan_decode")
+    return begin[: nc.value + 1].copy(), nc.value, ns.value

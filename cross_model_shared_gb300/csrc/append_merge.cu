@@ -1,0 +1,123 @@
+// append_merge.cu -- partial-prefill append and the split-KV merge (sm_103a).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "shkv_device.cuh"
+
+namespace shkv {
+
+// Partial-prefill append (PrefillShare Sec. 3.3 / Sec. 7): token t of request
+// b lands at logical position L_b + t of the shared paged cache.  One
+// (request, token, head) row of D bf16 values is moved per group of D/8
+// threads, 16 bytes each, so a warp writes 2 (D=128) or 4 (D=64) whole rows
+// with full-sector coalescing on both sides.  The old lengths come from the
+// pool's host copy; block 0 then publishes L_b + T (no thread of this kernel
+// reads seq_lens after that store).
+__global__ void __launch_bounds__(256) shkv_append_kernel(const __grid_constant__ AppendParams p)
+{
+    const int hv = p.head_vecs;                      // 16-byte vectors per head row
+    const int64_t rows = (int64_t)p.batch * p.n_new * p.hkv;
+    const int64_t total = rows * hv;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / hv;
+        const int v = (int)(i - row * hv);
+        const int g = (int)(row % p.hkv);
+        const int64_t bt_ = row / p.hkv;
+        const int t = (int)(bt_ % p.n_new);
+        const int b = (int)(bt_ / p.n_new);
+        const int pos = p.old_len[b] + t;
+        const int page = __ldg(p.block_table + (int64_t)b * p.max_pages + pos / p.page_size);
+        if (page < 0 || page >= p.num_pages) {
+            if (v == 0)
+                atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
+            continue;
+        }
+        const int64_t dst = (((int64_t)page * p.hkv + g) * p.page_size + pos % p.page_size) * hv + v;
+        p.k_pages[dst] = __ldg(p.k_new + i);
+        p.v_pages[dst] = __ldg(p.v_new + i);
+    }
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+            if (p.seq_lens[b] != p.old_len[b])
+                atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
+            p.seq_lens[b] = p.old_len[b] + p.n_new;
+        }
+    }
+}
+
+cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)p.batch * p.n_new * p.hkv * p.head_vecs;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8)
+        blocks = (int64_t)num_sms * 8;
+    if (blocks < 1)
+        blocks = 1;
+    shkv_append_kernel<<<(int)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Log-sum-exp merge of split-KV partials.  One warp per (request, row); the
+// lanes read the S log-sum-exps, agree on the max, then each lane reduces
+// float4 slices of the S partial outputs with weights exp(lse_s - max).
+__global__ void __launch_bounds__(256)
+    shkv_merge_kernel(int n_splits, int batch, int rows, int head_dim, const float *__restrict__ o_part,
+                      const float *__restrict__ lse_part, __nv_bfloat16 *__restrict__ out,
+                      float *__restrict__ lse_out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nrow = (int64_t)batch * rows;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= nrow)
+        return;
+    float M = -INFINITY;
+    for (int s = lane; s < n_splits; s += 32)
+        M = fmaxf(M, lse_part[(int64_t)s * nrow + row]);
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float wsum = 0.f;
+    if (M != -INFINITY)
+        for (int s = lane; s < n_splits; s += 32)
+            wsum += ex2_approx((lse_part[(int64_t)s * nrow + row] - M) * 1.4426950408889634f);
+    for (int o = 16; o > 0; o >>= 1)
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int dq = head_dim / 4;
+    for (int d4 = lane; d4 < dq; d4 += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            for (int s = 0; s < n_splits; ++s) {
+                const float w = ex2_approx((lse_part[(int64_t)s * nrow + row] - M) * 1.4426950408889634f);
+                const float4 v = reinterpret_cast<const float4 *>(o_part + ((int64_t)s * nrow + row) * head_dim)[d4];
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(out + row * head_dim)[d4] = packed;
+    }
+    if (lane == 0 && lse_out)
+        lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
+                         const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream)
+{
+    const int64_t nrow = (int64_t)batch * rows;
+    const int64_t blocks = (nrow + 7) / 8;
+    if (blocks > 0)
+        shkv_merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n_splits, batch, rows, head_dim, o_part,
+                                                                lse_part, out, lse_out);
+    return cudaGetLastError();
+}
+
+}  // namespace shkv

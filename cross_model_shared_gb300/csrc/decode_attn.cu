@@ -1,0 +1,681 @@
+// decode_attn.cu -- shared-KV multi-decoder paged decode attention (sm_103a).
+//
+// The method (ICaRus, key design 3; PrefillShare Sec. 3.3): N decoders that
+// share one frozen encoder also share one paged KV cache, and their queries
+// are stacked along the head axis so that all of them attend the cache
+// together.  For KV head g the stacked rows are the R = N * (Hq / Hkv) query
+// heads of every decoder that map to g; each K/V page of head g is therefore
+// fetched from HBM once per step and applied to all R rows while it sits in
+// shared memory.  Decode is memory-bound (PrefillShare Sec. 4, two-phase
+// execution), so the R-fold reuse is what hides the extra decoders' compute.
+//
+// Work decomposition (flash-decoding with a balanced static split):
+//   The (request b, KV head g, page p) chunks, ordered request-major, are cut
+//   into num_ctas equal contiguous ranges; one persistent CTA per SM walks its
+//   range as a sequence of segments (one segment per (b, g) it touches).  A
+//   (b, g) that straddles a cut is split: each piece writes a normalised
+//   partial and its log-sum-exp, and the last piece to finish (an atomic
+//   arrival counter, no waiting) merges them.  No CTA ever waits for another.
+//
+// Inside a CTA:
+//   * one producer warp issues TMA tensor loads (128-byte swizzle, L2
+//     evict-first) of whole (page, head) K and V chunks into an mbarrier ring
+//     of kStageTokens-token slots, plus a bulk copy of the segment's R query
+//     rows; block-table entries are prefetched 32 at a time;
+//   * consumer warps take slots round-robin.  Each warp owns 8 or 16 stacked
+//     rows (a row group); larger R uses several row groups that read the same
+//     slot.  Per slot a warp computes S^T = K Q^T with tokens as the MMA M
+//     dimension (16 tokens x 8 rows per mma.sync m16n8k16), so R = 8 rows fill
+//     an MMA exactly; an online softmax in base 2 follows; P^T is transposed in
+//     registers (movmatrix) and O^T += V^T P^T accumulates in fp32;
+//   * at the end of a segment the warps of a row group merge their
+//     (max, sum, O) states through shared memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "shkv_device.cuh"
+
+namespace shkv {
+
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Segment {
+    int b, g, pages_b, p0, p1;
+    int64_t unit_begin, unit_end, seg_begin, seg_end;
+};
+
+// Chunk index -> (request, head, page) and the segment it starts, clipped to
+// the CTA's range end.
+__device__ __forceinline__ Segment locate(const DecodeParams &p, int64_t idx, int64_t cta_end)
+{
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if ((int64_t)p.hkv * p.page_prefix[mid] <= idx)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    Segment s;
+    s.b = lo;
+    s.pages_b = p.page_prefix[lo + 1] - p.page_prefix[lo];
+    const int64_t base = (int64_t)p.hkv * p.page_prefix[lo];
+    const int64_t rem = idx - base;
+    s.g = (int)(rem / s.pages_b);
+    s.p0 = (int)(rem - (int64_t)s.g * s.pages_b);
+    s.unit_begin = base + (int64_t)s.g * s.pages_b;
+    s.unit_end = s.unit_begin + s.pages_b;
+    s.seg_begin = idx;
+    s.seg_end = s.unit_end < cta_end ? s.unit_end : cta_end;
+    s.p1 = s.p0 + (int)(s.seg_end - idx);
+    return s;
+}
+
+__device__ __forceinline__ int64_t cta_start(const DecodeParams &p, int c)
+{
+    return (int64_t)c * p.total_chunks / p.num_ctas;
+}
+
+// CTA whose range holds chunk idx.
+__device__ __forceinline__ int cta_of(const DecodeParams &p, int64_t idx)
+{
+    return (int)(((idx + 1) * p.num_ctas - 1) / p.total_chunks);
+}
+
+// Partial slot written by CTA c for its piece of the unit starting at
+// unit_begin: slot 0 if the piece opens the CTA's range, else slot 1.
+__device__ __forceinline__ int piece_slot(const DecodeParams &p, int c, int64_t unit_begin)
+{
+    const int64_t st = cta_start(p, c);
+    return 2 * c + (unit_begin <= st ? 0 : 1);
+}
+
+__device__ __forceinline__ int q_row(const DecodeParams &p, int g, int r)
+{
+    const int m = r / p.group, j = r - (r / p.group) * p.group;
+    return m * p.hq + g * p.group + j;
+}
+
+struct Ctx {
+    uint8_t *smem;
+    DecodeSmem lay;
+    uint32_t base;          // shared-space address of smem
+    volatile uint32_t *abort_flag;
+    uint32_t *bcast;
+    int64_t cta_begin, cta_end;
+};
+
+__device__ __forceinline__ uint32_t full_bar(const Ctx &c, int s) { return c.base + c.lay.bars + 8u * s; }
+__device__ __forceinline__ uint32_t empty_bar(const Ctx &c, int s, int stages)
+{
+    return c.base + c.lay.bars + 8u * (stages + s);
+}
+__device__ __forceinline__ uint32_t qfull_bar(const Ctx &c, int i, int stages)
+{
+    return c.base + c.lay.bars + 8u * (2 * stages + i);
+}
+__device__ __forceinline__ uint32_t qempty_bar(const Ctx &c, int i, int stages)
+{
+    return c.base + c.lay.bars + 8u * (2 * stages + 2 + i);
+}
+
+// ---------------------------------------------------------------------------
+// producer warp
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,
+                         const Ctx &c)
+{
+    constexpr int NBOX = D / 64;
+    const int lane = threadIdx.x & 31;
+    const int stages = p.stages;
+    const int SP = p.pages_per_stage;
+    const int P = p.page_size;
+    const uint32_t box_bytes = (uint32_t)P * 128u;
+    const uint32_t page_bytes_kv = 2u * (uint32_t)P * D * 2u;
+    const uint64_t pol = l2_evict_first_policy();
+    if (lane == 0) {
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
+    }
+
+    bool alive = true;
+    int64_t idx = c.cta_begin;
+    int kbase = 0, seg = 0;
+    int last_issued_stage = -1;     // highest stage index with copies issued
+    int q_issued[2] = {-1, -1};     // segment whose Q was last issued per buffer
+    while (idx < c.cta_end) {
+        const Segment s = locate(p, idx, c.cta_end);
+        // --- query rows of this (b, g): N bulk copies of G contiguous rows
+        const int qb = seg & 1;
+        if (alive) {
+            bool ok = mbar_wait_bounded(qempty_bar(c, qb, stages), ((seg >> 1) & 1) ^ 1, c.abort_flag, p.err);
+            alive = __all_sync(0xffffffffu, ok);
+        }
+        if (alive && lane == 0) {
+            const uint32_t rows_bytes = (uint32_t)p.group * D * 2u;
+            mbar_arrive_expect_tx(qfull_bar(c, qb, stages), rows_bytes * p.n_models);
+            const __nv_bfloat16 *qsrc = p.q + ((int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group) * D;
+            const uint32_t qdst = c.base + c.lay.qbuf + qb * c.lay.qbuf_bytes;
+            for (int m = 0; m < p.n_models; ++m)
+                bulk_load(qdst + m * rows_bytes, qsrc + (int64_t)m * p.hq * D, rows_bytes,
+                          qfull_bar(c, qb, stages));
+            q_issued[qb] = seg;
+        }
+        // --- K/V pages of the segment
+        const int nst = (s.p1 - s.p0 + SP - 1) / SP;
+        const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
+        int w0 = s.p0;
+        int cur = (w0 + lane < s.p1) ? __ldg(btrow + w0 + lane) : -1;
+        int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+        for (int j = 0; j < nst; ++j) {
+            const int k = kbase + j;
+            const int slot = k % stages;
+            const int pg0 = s.p0 + j * SP;
+            if (pg0 >= w0 + 32) {
+                w0 += 32;
+                cur = nxt;
+                nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+            }
+            const int id0 = __shfl_sync(0xffffffffu, cur, (pg0 - w0) & 31);
+            const int id1 = __shfl_sync(0xffffffffu, cur, (pg0 - w0 + 1) & 31);
+            if (alive) {
+                bool ok = mbar_wait_bounded(empty_bar(c, slot, stages), ((k / stages) & 1) ^ 1, c.abort_flag, p.err);
+                alive = __all_sync(0xffffffffu, ok);
+            }
+            if (alive && lane == 0) {
+                uint32_t mask = 0, bytes = 0;
+                for (int i = 0; i < SP; ++i) {
+                    const int id = i == 0 ? id0 : id1;
+                    if (pg0 + i >= s.p1)
+                        continue;
+                    if (id >= 0 && id < p.num_pages) {
+                        mask |= 1u << i;
+                        bytes += page_bytes_kv;
+                    } else {
+                        atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
+                    }
+                }
+                volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
+                meta[slot] = mask;
+                const uint32_t kdst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+                const uint32_t vdst = kdst + (uint32_t)(kStageTokens * D * 2);
+                mbar_arrive_expect_tx(full_bar(c, slot), bytes);
+                for (int i = 0; i < SP; ++i) {
+                    if (!(mask & (1u << i)))
+                        continue;
+                    const int y = ((i == 0 ? id0 : id1) * p.hkv + s.g) * P;
+#pragma unroll
+                    for (int x = 0; x < NBOX; ++x) {
+                        const uint32_t off = (uint32_t)x * (kStageTokens * 128u) + (uint32_t)i * box_bytes;
+                        tma_load_2d(kdst + off, tmK, x * 64, y, full_bar(c, slot), pol);
+                        tma_load_2d(vdst + off, tmV, x * 64, y, full_bar(c, slot), pol);
+                    }
+                }
+                last_issued_stage = k;
+            }
+            __syncwarp();
+        }
+        kbase += nst;
+        idx = s.seg_end;
+        ++seg;
+    }
+    // After an abort, wait (bounded) for every copy this CTA still has in
+    // flight so no TMA write lands after the CTA exits.
+    if (!alive && lane == 0) {
+        for (int k = last_issued_stage - stages + 1; k <= last_issued_stage; ++k)
+            if (k >= 0)
+                mbar_drain_bounded(full_bar(c, k % stages), (uint32_t)((k / stages) & 1));
+        for (int i = 0; i < 2; ++i)
+            if (q_issued[i] >= 0)
+                mbar_drain_bounded(qfull_bar(c, i, stages), (uint32_t)((q_issued[i] >> 1) & 1));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps
+// ---------------------------------------------------------------------------
+template <int D, int NT>
+__device__ void consumer(const DecodeParams &p, const Ctx &c)
+{
+    constexpr int KSTEPS = D / 16;
+    constexpr int ROWS_W = 8 * NT;
+    constexpr int NREG = KSTEPS * NT * 4;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ncw = p.nrg * p.wt;
+    const int rg = warp / p.wt;
+    const int wtid = warp - rg * p.wt;
+    const int row0 = rg * ROWS_W;
+    const int stages = p.stages;
+    const int SP = p.pages_per_stage;
+    const int P = p.page_size;
+    const float sl2 = p.scale_log2;
+
+    float *comb_o = reinterpret_cast<float *>(c.smem + c.lay.comb_o);
+    float *comb_m = reinterpret_cast<float *>(c.smem + c.lay.comb_m);
+    float *comb_l = reinterpret_cast<float *>(c.smem + c.lay.comb_l);
+    const volatile uint32_t *meta = reinterpret_cast<const volatile uint32_t *>(c.smem + c.lay.meta);
+
+    // per-lane constant parts of the ldmatrix addresses
+    const int k_tok = (lane & 7) + ((lane >> 3) & 1) * 8;   // K: token within a 16-token tile
+    const int k_col = (lane >> 4) * 8;                        // K: column offset within 16
+    const int v_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // V: token within a 16-token tile
+    const int v_col = ((lane >> 3) & 1) * 8;                  // V: column offset within 16
+
+    bool alive = true;
+    int64_t idx = c.cta_begin;
+    int kbase = 0, seg = 0;
+    while (idx < c.cta_end) {
+        const Segment s = locate(p, idx, c.cta_end);
+        const int nst = (s.p1 - s.p0 + SP - 1) / SP;
+        const int qb = seg & 1;
+
+        // --- query fragments (B operand of S^T = K Q^T): rows row0.., all D
+        uint32_t qf[KSTEPS][NT][2];
+        {
+            bool ok = true;
+            if (alive) {
+                ok = mbar_wait_bounded(qfull_bar(c, qb, stages), (seg >> 1) & 1, c.abort_flag, p.err);
+                alive = __all_sync(0xffffffffu, ok);
+            }
+            const uint32_t qbase = c.base + c.lay.qbuf + qb * c.lay.qbuf_bytes;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ks += 2) {
+                    const uint32_t addr = qbase + (uint32_t)((row0 + nt * 8 + (lane & 7)) * D * 2) +
+                                          (uint32_t)((ks * 16 + (lane >> 3) * 8) * 2);
+                    if (alive)
+                        ldsm_x4(addr, qf[ks][nt][0], qf[ks][nt][1], qf[ks + 1][nt][0], qf[ks + 1][nt][1]);
+                    else
+                        qf[ks][nt][0] = qf[ks][nt][1] = qf[ks + 1][nt][0] = qf[ks + 1][nt][1] = 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qempty_bar(c, qb, stages));
+        }
+
+        // --- cached length; the plan was built from the host copy
+        int L = __ldg(p.seq_lens + s.b);
+        if ((L + P - 1) / P != s.pages_b) {
+            if (lane == 0 && wtid == 0 && rg == 0)
+                atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
+            L = L < 0 ? 0 : (L > s.pages_b * P ? s.pages_b * P : L);
+        }
+
+        float o[KSTEPS][NT][4];
+        float mrow[NT][2], lrow[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mrow[nt][0] = mrow[nt][1] = -INFINITY;
+            lrow[nt][0] = lrow[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt)
+                o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+        }
+
+        for (int j = (wtid - kbase % p.wt + p.wt) % p.wt; j < nst; j += p.wt) {
+            const int k = kbase + j;
+            const int slot = k % stages;
+            bool ok = false;
+            if (alive) {
+                ok = mbar_wait_bounded(full_bar(c, slot), (k / stages) & 1, c.abort_flag, p.err);
+                ok = __all_sync(0xffffffffu, ok);
+                alive = ok;
+            }
+            if (ok) {
+                const uint32_t kst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+                const uint32_t vst = kst + (uint32_t)(kStageTokens * D * 2);
+                const uint32_t mask = meta[slot];
+                const int pg0 = s.p0 + j * SP;
+                const int tok_base = pg0 * P;   // logical token of slot row 0
+                const uint32_t full_mask = (1u << SP) - 1u;
+                const bool all_valid = (pg0 + SP <= s.p1) && (mask == full_mask) && (tok_base + kStageTokens <= L);
+                auto tok_valid = [&](int t) -> bool {
+                    const int i = t / P;
+                    return ((mask >> i) & 1u) && (pg0 + i < s.p1) && (tok_base + t < L);
+                };
+                if (!all_valid) {
+                    // Rows that are masked may hold stale or non-finite bits:
+                    // zero their V so 0 * V stays 0 in the PV product.
+                    for (int e = lane; e < kStageTokens * (D / 8); e += 32) {
+                        const int t = e / (D / 8);
+                        const int cchunk = e - t * (D / 8);
+                        if (!tok_valid(t))
+                            st_shared_zero16(vst + (uint32_t)((cchunk >> 3) * (kStageTokens * 128) + t * 128 + (cchunk & 7) * 16));
+                    }
+                    __syncwarp();
+                }
+
+                // S^T[tok, row] = K[tok, :] . Q[row, :]
+                float sc[2][NT][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        const int tok = mt * 16 + k_tok;
+                        const int col = ks * 16 + k_col;
+                        const uint32_t addr = kst + (uint32_t)((col >> 6) * (kStageTokens * 128) + tok * 128 +
+                                                               ((((col & 63) >> 3) ^ (tok & 7)) << 4));
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_bf16(sc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+                    }
+                }
+
+                // online softmax in base 2: x = s * scale * log2(e)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float x = sc[mt][nt][e] * sl2;
+                            if (!all_valid && !tok_valid(mt * 16 + (lane >> 2) + (e >> 1) * 8))
+                                x = -INFINITY;
+                            sc[mt][nt][e] = x;
+                        }
+                uint32_t pb[2][NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float mx[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        float v = fmaxf(fmaxf(sc[0][nt][i], sc[0][nt][i + 2]), fmaxf(sc[1][nt][i], sc[1][nt][i + 2]));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                        mx[i] = v;
+                    }
+                    float alpha[2], muse[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float mnew = fmaxf(mrow[nt][i], mx[i]);
+                        muse[i] = (mnew == -INFINITY) ? 0.f : mnew;
+                        alpha[i] = ex2_approx(mrow[nt][i] - muse[i]);
+                        mrow[nt][i] = mnew;
+                    }
+                    float rs[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float pv = ex2_approx(sc[mt][nt][e] - muse[e & 1]);
+                            sc[mt][nt][e] = pv;
+                            rs[e & 1] += pv;
+                        }
+                    lrow[nt][0] = lrow[nt][0] * alpha[0] + rs[0];
+                    lrow[nt][1] = lrow[nt][1] * alpha[1] + rs[1];
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        o[mt][nt][0] *= alpha[0];
+                        o[mt][nt][1] *= alpha[1];
+                        o[mt][nt][2] *= alpha[0];
+                        o[mt][nt][3] *= alpha[1];
+                    }
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        pb[kt][nt][0] = movmatrix_trans(pack_bf16x2(sc[kt][nt][0], sc[kt][nt][1]));
+                        pb[kt][nt][1] = movmatrix_trans(pack_bf16x2(sc[kt][nt][2], sc[kt][nt][3]));
+                    }
+                }
+
+                // O^T[d, row] += V^T[d, tok] . P^T[tok, row]
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        const int tok = kt * 16 + v_tok;
+                        const int col = mt * 16 + v_col;
+                        const uint32_t addr = vst + (uint32_t)((col >> 6) * (kStageTokens * 128) + tok * 128 +
+                                                               ((((col & 63) >> 3) ^ (tok & 7)) << 4));
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_t(addr, a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_bf16(o[mt][nt], a0, a1, a2, a3, pb[kt][nt][0], pb[kt][nt][1]);
+                    }
+                }
+                if (!all_valid)
+                    fence_proxy_async_smem();   // generic zero-writes before the next TMA into this slot
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty_bar(c, slot, stages));
+        }
+
+        // --- merge the row group's warps: publish (m, l, O) ...
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                float v = lrow[nt][i];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                lrow[nt][i] = v;
+            }
+        if (lane < 4) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    comb_m[warp * ROWS_W + nt * 8 + 2 * lane + i] = mrow[nt][i];
+                    comb_l[warp * ROWS_W + nt * 8 + 2 * lane + i] = lrow[nt][i];
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    comb_o[((size_t)warp * NREG + (mt * NT + nt) * 4 + e) * 32 + lane] = o[mt][nt][e];
+        named_barrier(1, (uint32_t)ncw * 32u);
+
+        // ... and combine them, each warp taking every wt-th register slot
+        const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
+        const int slot_id = whole ? 0 : 2 * (int)blockIdx.x + (s.seg_begin == c.cta_begin ? 0 : 1);
+        const int w_first = rg * p.wt;
+        for (int reg = wtid; reg < NREG; reg += p.wt) {
+            const int e = reg & 3;
+            const int nt = (reg >> 2) % NT;
+            const int mt = (reg >> 2) / NT;
+            const int rl = nt * 8 + 2 * (lane & 3) + (e & 1);
+            const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
+            float M = -INFINITY;
+            for (int w = 0; w < p.wt; ++w)
+                M = fmaxf(M, comb_m[(w_first + w) * ROWS_W + rl]);
+            float lsum = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+                for (int w = 0; w < p.wt; ++w) {
+                    const float f = ex2_approx(comb_m[(w_first + w) * ROWS_W + rl] - M);
+                    lsum += comb_l[(w_first + w) * ROWS_W + rl] * f;
+                    acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * f;
+                }
+            }
+            const int r = row0 + rl;
+            if (r >= p.rows)
+                continue;
+            const float val = lsum > 0.f ? acc / lsum : 0.f;
+            const bool lse_writer = (mt == 0) && (e < 2) && ((lane >> 2) == 0);
+            const float lse = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            if (whole) {
+                const int qr = q_row(p, s.g, r);
+                const int64_t orow = (int64_t)s.b * p.n_models * p.hq + qr;
+                p.out[orow * D + d] = __float2bfloat16_rn(val);
+                if (lse_writer && p.lse_out)
+                    p.lse_out[orow] = lse;
+            } else {
+                p.ws_part[((int64_t)slot_id * p.rows + r) * D + d] = val;
+                if (lse_writer)
+                    p.ws_lse[(int64_t)slot_id * p.rows + r] = lse;
+            }
+        }
+        if (!whole)
+            __threadfence();   // partials visible device-wide before the arrival count below
+        named_barrier(1, (uint32_t)ncw * 32u);
+
+        // --- split unit: the last piece to arrive merges all pieces
+        if (!whole) {
+            const int c0 = cta_of(p, s.unit_begin);
+            const int c1 = cta_of(p, s.unit_end - 1);
+            uint32_t *counter = p.ws_count + (int64_t)s.b * p.hkv + s.g;
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const uint32_t prev = atomicAdd(counter, 1u);
+                *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
+            }
+            named_barrier(1, (uint32_t)ncw * 32u);
+            if (*c.bcast) {
+                __threadfence();
+                const int dq = D / 4;
+                for (int it = threadIdx.x; it < p.rows * dq; it += ncw * 32) {
+                    const int r = it / dq;
+                    const int d4 = it - r * dq;
+                    float M = -INFINITY;
+                    for (int cc = c0; cc <= c1; ++cc) {
+                        const int sl = piece_slot(p, cc, s.unit_begin);
+                        M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)sl * p.rows + r));
+                    }
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float wsum = 0.f;
+                    if (M != -INFINITY) {
+                        for (int cc = c0; cc <= c1; ++cc) {
+                            const int sl = piece_slot(p, cc, s.unit_begin);
+                            const float l = __ldcg(p.ws_lse + (int64_t)sl * p.rows + r);
+                            const float w = ex2_approx((l - M) * 1.4426950408889634f);
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                p.ws_part + ((int64_t)sl * p.rows + r) * D) + d4);
+                            wsum += w;
+                            acc.x += w * v.x;
+                            acc.y += w * v.y;
+                            acc.z += w * v.z;
+                            acc.w += w * v.w;
+                        }
+                    }
+                    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                    const int qr = q_row(p, s.g, r);
+                    const int64_t orow = (int64_t)s.b * p.n_models * p.hq + qr;
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+                    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+                    uint2 packed;
+                    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+                    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(p.out + orow * D + d4 * 4) = packed;
+                    if (d4 == 0 && p.lse_out)
+                        p.lse_out[orow] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+                }
+                if (threadIdx.x == 0)
+                    *counter = 0u;
+            }
+            named_barrier(1, (uint32_t)ncw * 32u);
+        }
+
+        kbase += nst;
+        idx = s.seg_end;
+        ++seg;
+    }
+}
+
+}  // namespace
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    shkv_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Ctx c;
+    {
+        const uint32_t raw = smem_u32(smem_raw);
+        const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+        c.smem = smem_raw + pad;
+        c.base = raw + pad;
+    }
+    constexpr int KSTEPS = D / 16;
+    const int ncw = p.nrg * p.wt;
+    c.lay = decode_smem_layout(D, 8 * NT, KSTEPS * NT * 4, ncw, p.rpad, p.stages);
+    c.abort_flag = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.misc);
+    c.bcast = reinterpret_cast<uint32_t *>(c.smem + c.lay.misc + 4);
+    c.cta_begin = cta_start(p, blockIdx.x);
+    c.cta_end = cta_start(p, blockIdx.x + 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full_bar(c, s), 1);
+            mbar_init(empty_bar(c, s, p.stages), (uint32_t)p.nrg);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull_bar(c, i, p.stages), 1);
+            mbar_init(qempty_bar(c, i, p.stages), (uint32_t)ncw);
+        }
+        *c.abort_flag = 0u;
+        *c.bcast = 0u;
+        fence_barrier_init();
+    }
+    // rows [R, rpad) of both query buffers are padding: zero them once
+    {
+        const int pad_rows = p.rpad - p.rows;
+        const int n16 = pad_rows * D * 2 / 16;
+        for (int i = threadIdx.x; i < 2 * n16; i += blockDim.x) {
+            const int bufi = i / (n16 > 0 ? n16 : 1);
+            const int e = i - bufi * n16;
+            st_shared_zero16(c.base + c.lay.qbuf + bufi * c.lay.qbuf_bytes + p.rows * D * 2 + e * 16);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5;
+    if (warp == ncw)
+        producer<D>(&tmK, &tmV, p, c);
+    else if (warp < ncw)
+        consumer<D, NT>(p, c);
+}
+
+// ---------------------------------------------------------------------------
+// host-side launcher (internal to the library)
+// ---------------------------------------------------------------------------
+template <int D, int NT>
+static cudaError_t launch_decode_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+                                   uint32_t smem, cudaStream_t stream)
+{
+    auto kern = shkv_decode_kernel<D, NT>;
+    static uint32_t configured = 0;
+    if (smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        configured = smem;
+    }
+    const int threads = (p.nrg * p.wt + 1) * 32;
+    kern<<<p.num_ctas, threads, smem, stream>>>(tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const DecodeParams &p, uint32_t smem, cudaStream_t stream)
+{
+    if (D == 128)
+        return NT == 1 ? launch_decode_t<128, 1>(tmK, tmV, p, smem, stream)
+                       : launch_decode_t<128, 2>(tmK, tmV, p, smem, stream);
+    return NT == 1 ? launch_decode_t<64, 1>(tmK, tmV, p, smem, stream)
+                   : launch_decode_t<64, 2>(tmK, tmV, p, smem, stream);
+}
+
+}  // namespace shkv

@@ -1,0 +1,266 @@
+// shkv_device.cuh -- device-side building blocks for libshkv (sm_103a).
+//
+// Inline PTX wrappers for the Blackwell data-movement path (mbarrier, TMA
+// tensor and bulk copies with L2 hints), the warp-level tensor-core path
+// (ldmatrix, mma.sync m16n8k16 bf16, movmatrix) and bounded waits.  Every
+// spin-wait here gives up after kWaitLimitNs of wall time, records
+// SHKV_ERRF_TIMEOUT in the pool's error word and reports failure to the
+// caller, which then skips work and drains its own in-flight copies; no
+// kernel in this library can wait forever or trap.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "shkv.h"
+
+namespace shkv {
+
+// Tokens staged per pipeline slot: two 16-token pages or one 32-token page.
+constexpr int kStageTokens = 32;
+// Upper bound on pipeline slots per CTA.
+constexpr int kMaxStages = 8;
+// Largest block (consumer warps + one producer warp).
+constexpr int kMaxThreads = 320;
+// Wall-clock limit for any single wait on an mbarrier.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Dynamic shared memory a CTA may use on sm_100-family parts.
+constexpr int kSmemLimit = 232448;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;    // [B, N*Hq, D]
+    __nv_bfloat16 *out;        // [B, N*Hq, D]
+    float *lse_out;            // [B, N*Hq] or null
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    uint32_t *err;
+    uint32_t *ws_count;        // [B*Hkv] arrival counters, zero between calls
+    float *ws_lse;             // [2*C, R]
+    float *ws_part;            // [2*C, R, D]
+    int32_t batch, n_models, hq, hkv, group, rows;   // rows = R = N*G per KV head
+    int32_t nrg, wt, rpad, stages;                   // row groups, token warps per group
+    int32_t page_size, pages_per_stage, max_pages, num_pages;
+    int32_t num_ctas, pad0;
+    int64_t total_chunks;
+    float scale_log2;
+    float pad1;
+    int32_t page_prefix[SHKV_MAX_BATCH + 1];
+};
+
+struct AppendParams {
+    const uint4 *k_new, *v_new;    // [B, T, Hkv, D] bf16 as 16-byte vectors
+    uint4 *k_pages, *v_pages;
+    const int32_t *block_table;
+    int32_t *seq_lens;
+    uint32_t *err;
+    int32_t batch, n_new, hkv, head_vecs, page_size, max_pages, num_pages, pad;
+    int32_t old_len[SHKV_MAX_BATCH];
+};
+
+// ---------------------------------------------------------------------------
+// shared-memory layout of the decode kernel (host and device agree on it)
+// ---------------------------------------------------------------------------
+struct DecodeSmem {
+    uint32_t ring, stage_bytes, qbuf, qbuf_bytes, comb_o, comb_m, comb_l, bars, meta, misc, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// head_dim, rows per warp (8*NT), registers of O per lane, consumer warps, stages
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int rows_w, int nreg, int ncw,
+                                                         int rpad, int stages)
+{
+    DecodeSmem s;
+    s.stage_bytes = (uint32_t)(2 * kStageTokens * D * 2);
+    s.ring = 0;
+    s.qbuf = s.ring + (uint32_t)stages * s.stage_bytes;
+    s.qbuf_bytes = (uint32_t)(rpad * D * 2);
+    s.comb_o = align_up(s.qbuf + 2 * s.qbuf_bytes, 128);
+    s.comb_m = s.comb_o + (uint32_t)(ncw * nreg * 32 * 4);
+    s.comb_l = s.comb_m + (uint32_t)(ncw * rows_w * 4);
+    s.bars = align_up(s.comb_l + (uint32_t)(ncw * rows_w * 4), 8);
+    s.meta = s.bars + (uint32_t)((2 * stages + 4) * 8);
+    s.misc = s.meta + (uint32_t)(stages * 4);
+    s.total = s.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity.  Returns false if the CTA's abort
+// flag is raised or the wait runs over kWaitLimitNs (then the flag is raised
+// and SHKV_ERRF_TIMEOUT recorded).  Per-thread; callers combine per warp.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t *abort_flag, uint32_t *err)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if ((it & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1u;
+            atomicOr(err, SHKV_ERRF_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Same, ignoring the abort flag: used only to drain copies this CTA issued.
+__device__ __forceinline__ bool mbar_drain_bounded(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled TMA load global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 bf16 matrix held one 32-bit pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// 2^x, the hardware approximation (MUFU.EX2); ex2(-inf) = +0.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+}  // namespace shkv

@@ -1,0 +1,424 @@
+// shkv_host.cu -- the C ABI of libshkv: argument checks, work planning and
+// kernel launches.  Declarations and their contracts are in include/shkv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "shkv.h"
+#include "shkv_device.cuh"
+
+namespace shkv {
+cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const DecodeParams &p, uint32_t smem, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
+                         const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream);
+}  // namespace shkv
+
+using namespace shkv;
+
+struct shkv_pool {
+    shkv_pool_config cfg;
+    int device;
+    int num_sms;
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    std::vector<int32_t> lens;   // host copy of seq_lens
+};
+
+namespace {
+
+// Smallest number of chunks a CTA is given before the grid shrinks.
+constexpr int64_t kMinChunksPerCta = 8;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D view of a [num_pages, Hkv, P, D] bf16 pool: rows = num_pages*Hkv*P,
+// columns = D; a 64-column x P-row box with 128-byte swizzle is one page of
+// one head (split in two boxes when D = 128).
+bool make_pool_map(CUtensorMap *tm, void *base, const shkv_pool_config &c)
+{
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_pages * c.num_kv_heads * c.page_size};
+    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)c.page_size};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Page prefix over requests and the CTA count; shared by the plan query and
+// the decode launch so both describe the same split.
+shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv, int32_t max_ctas,
+                       int32_t *prefix, int64_t *total_chunks, int32_t *num_ctas)
+{
+    if (batch < 1 || batch > SHKV_MAX_BATCH || !lens || page_size <= 0 || hkv <= 0 || max_ctas <= 0)
+        return SHKV_ERR_INVALID_ARG;
+    prefix[0] = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (lens[b] < 1)
+            return SHKV_ERR_INVALID_ARG;
+        int64_t next = (int64_t)prefix[b] + ceil_div(lens[b], page_size);
+        if (next > INT32_MAX)
+            return SHKV_ERR_UNSUPPORTED;
+        prefix[b + 1] = (int32_t)next;
+    }
+    const int64_t W = (int64_t)hkv * prefix[batch];
+    int64_t C = ceil_div(W, kMinChunksPerCta);
+    if (C > max_ctas)
+        C = max_ctas;
+    if (C < 1)
+        C = 1;
+    *total_chunks = W;
+    *num_ctas = (int32_t)C;
+    return SHKV_OK;
+}
+
+size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms)
+{
+    const size_t count = align_up((uint32_t)(batch * hkv * 4), 256);
+    const size_t lse = align_up((uint32_t)(2 * num_sms * rows * 4), 256);
+    const size_t part = (size_t)2 * num_sms * rows * head_dim * 4;
+    return count + lse + part;
+}
+
+shkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SHKV_OK : SHKV_ERR_CUDA; }
+
+// Launch shape of the decode kernel for R stacked rows per KV head.
+struct DecodeShape {
+    int nt, nrg, wt, rpad;
+};
+
+DecodeShape decode_shape(int rows)
+{
+    DecodeShape s;
+    s.nt = rows <= 8 ? 1 : 2;
+    s.nrg = s.nt == 1 ? 1 : (rows + 15) / 16;
+    static const int wt_of_nrg[5] = {0, 8, 4, 3, 2};
+    s.wt = wt_of_nrg[s.nrg];
+    s.rpad = s.nrg * 8 * s.nt;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *shkv_status_string(shkv_status s)
+{
+    switch (s) {
+    case SHKV_OK:
+        return "ok";
+    case SHKV_ERR_INVALID_ARG:
+        return "invalid argument";
+    case SHKV_ERR_CAPACITY:
+        return "sequence exceeds the pool's per-request capacity";
+    case SHKV_ERR_UNSUPPORTED:
+        return "unsupported shape or configuration";
+    case SHKV_ERR_CUDA:
+        return "CUDA runtime error";
+    case SHKV_ERR_DEVICE:
+        return "device error bits set";
+    }
+    return "unknown status";
+}
+
+shkv_status shkv_pool_create(const shkv_pool_config *cfg, shkv_pool **out)
+{
+    if (!cfg || !out)
+        return SHKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    const shkv_pool_config &c = *cfg;
+    if (c.num_pages <= 0 || c.num_kv_heads <= 0 || c.max_batch <= 0 || c.max_pages_per_seq <= 0 ||
+        !c.k_pages || !c.v_pages || !c.block_table || !c.seq_lens || !c.error_word)
+        return SHKV_ERR_INVALID_ARG;
+    if (!aligned16(c.k_pages) || !aligned16(c.v_pages) || ((uintptr_t)c.block_table & 3u) ||
+        ((uintptr_t)c.seq_lens & 3u) || ((uintptr_t)c.error_word & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    if ((c.page_size != 16 && c.page_size != 32) || (c.head_dim != 64 && c.head_dim != 128))
+        return SHKV_ERR_UNSUPPORTED;
+    if ((int64_t)c.num_pages * c.num_kv_heads * c.page_size > INT32_MAX ||
+        (int64_t)c.max_pages_per_seq * c.page_size > INT32_MAX)
+        return SHKV_ERR_UNSUPPORTED;
+    if (c.initial_seq_lens)
+        for (int b = 0; b < c.max_batch; ++b)
+            if (c.initial_seq_lens[b] < 0 || (int64_t)c.initial_seq_lens[b] > (int64_t)c.max_pages_per_seq * c.page_size)
+                return SHKV_ERR_CAPACITY;
+
+    shkv_pool *pool = new (std::nothrow) shkv_pool();
+    if (!pool)
+        return SHKV_ERR_INVALID_ARG;
+    pool->cfg = c;
+    pool->cfg.initial_seq_lens = nullptr;
+    pool->lens.assign(c.max_batch, 0);
+    if (c.initial_seq_lens)
+        memcpy(pool->lens.data(), c.initial_seq_lens, sizeof(int32_t) * c.max_batch);
+    if (cudaGetDevice(&pool->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pool->num_sms, cudaDevAttrMultiProcessorCount, pool->device) != cudaSuccess) {
+        delete pool;
+        return SHKV_ERR_CUDA;
+    }
+    if (!make_pool_map(&pool->tm_k, c.k_pages, c) || !make_pool_map(&pool->tm_v, c.v_pages, c)) {
+        delete pool;
+        return SHKV_ERR_CUDA;
+    }
+    if (cudaMemcpy(c.seq_lens, pool->lens.data(), sizeof(int32_t) * c.max_batch, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemset(c.error_word, 0, sizeof(uint32_t)) != cudaSuccess) {
+        delete pool;
+        return SHKV_ERR_CUDA;
+    }
+    *out = pool;
+    return SHKV_OK;
+}
+
+shkv_status shkv_pool_destroy(shkv_pool *pool)
+{
+    if (!pool)
+        return SHKV_ERR_INVALID_ARG;
+    delete pool;
+    return SHKV_OK;
+}
+
+shkv_status shkv_pool_set_seq_lens(shkv_pool *pool, int32_t batch, const int32_t *lens, void *stream)
+{
+    if (!pool || !lens || batch < 0 || batch > pool->cfg.max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    const int64_t cap = (int64_t)pool->cfg.max_pages_per_seq * pool->cfg.page_size;
+    for (int b = 0; b < batch; ++b)
+        if (lens[b] < 0 || lens[b] > cap)
+            return SHKV_ERR_CAPACITY;
+    if (batch == 0)
+        return SHKV_OK;
+    memcpy(pool->lens.data(), lens, sizeof(int32_t) * batch);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(pool->cfg.seq_lens, pool->lens.data(), sizeof(int32_t) * batch,
+                                    cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
+
+shkv_status shkv_pool_get_seq_lens(const shkv_pool *pool, int32_t batch, int32_t *lens)
+{
+    if (!pool || !lens || batch < 0 || batch > pool->cfg.max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    memcpy(lens, pool->lens.data(), sizeof(int32_t) * batch);
+    return SHKV_OK;
+}
+
+shkv_status shkv_append_kv(shkv_pool *pool, int32_t batch, int32_t n_new_tokens, const void *k_new,
+                           const void *v_new, void *stream)
+{
+    if (!pool || batch < 0 || batch > pool->cfg.max_batch || batch > SHKV_MAX_BATCH || n_new_tokens < 0)
+        return SHKV_ERR_INVALID_ARG;
+    if (batch == 0 || n_new_tokens == 0)
+        return SHKV_OK;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return SHKV_ERR_INVALID_ARG;
+    const shkv_pool_config &c = pool->cfg;
+    const int64_t cap = (int64_t)c.max_pages_per_seq * c.page_size;
+    for (int b = 0; b < batch; ++b)
+        if ((int64_t)pool->lens[b] + n_new_tokens > cap)
+            return SHKV_ERR_CAPACITY;
+    AppendParams p;
+    memset(&p, 0, sizeof p);
+    p.k_new = reinterpret_cast<const uint4 *>(k_new);
+    p.v_new = reinterpret_cast<const uint4 *>(v_new);
+    p.k_pages = reinterpret_cast<uint4 *>(c.k_pages);
+    p.v_pages = reinterpret_cast<uint4 *>(c.v_pages);
+    p.block_table = c.block_table;
+    p.seq_lens = c.seq_lens;
+    p.err = c.error_word;
+    p.batch = batch;
+    p.n_new = n_new_tokens;
+    p.hkv = c.num_kv_heads;
+    p.head_vecs = c.head_dim / 8;
+    p.page_size = c.page_size;
+    p.max_pages = c.max_pages_per_seq;
+    p.num_pages = c.num_pages;
+    for (int b = 0; b < batch; ++b)
+        p.old_len[b] = pool->lens[b];
+    cudaError_t e = launch_append(p, pool->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    for (int b = 0; b < batch; ++b)
+        pool->lens[b] += n_new_tokens;
+    return SHKV_OK;
+}
+
+shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int32_t n_models,
+                                       int32_t hq_per_model, size_t *bytes)
+{
+    if (!pool || !bytes || batch < 1 || n_models < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    const int hkv = pool->cfg.num_kv_heads;
+    if (hq_per_model % hkv)
+        return SHKV_ERR_UNSUPPORTED;
+    const int rows = n_models * (hq_per_model / hkv);
+    *bytes = workspace_bytes_for(batch, hkv, rows, pool->cfg.head_dim, pool->num_sms);
+    return SHKV_OK;
+}
+
+shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model,
+                                  const void *q, float scale, void *out, float *lse_out, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    if (!pool || !q || !out || !workspace || batch < 1 || n_models < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || ((uintptr_t)lse_out & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    if (!isfinite(scale))
+        return SHKV_ERR_INVALID_ARG;
+    const shkv_pool_config &c = pool->cfg;
+    if (batch > c.max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    if (batch > SHKV_MAX_BATCH || hq_per_model % c.num_kv_heads)
+        return SHKV_ERR_UNSUPPORTED;
+    const int group = hq_per_model / c.num_kv_heads;
+    const int rows = n_models * group;
+    if (rows > 64)
+        return SHKV_ERR_UNSUPPORTED;
+    if (workspace_bytes < workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim, pool->num_sms))
+        return SHKV_ERR_INVALID_ARG;
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    shkv_status st = build_plan(batch, pool->lens.data(), c.page_size, c.num_kv_heads, pool->num_sms,
+                                p.page_prefix, &p.total_chunks, &p.num_ctas);
+    if (st != SHKV_OK)
+        return st;
+    const DecodeShape sh = decode_shape(rows);
+    const int ncw = sh.nrg * sh.wt;
+    const int nreg = (c.head_dim / 16) * sh.nt * 4;
+    const DecodeSmem probe = decode_smem_layout(c.head_dim, 8 * sh.nt, nreg, ncw, sh.rpad, 0);
+    int stages = (int)((kSmemLimit - (int64_t)probe.total - 64) / (probe.stage_bytes + 20));
+    if (stages > kMaxStages)
+        stages = kMaxStages;
+    if (stages < 2)
+        return SHKV_ERR_UNSUPPORTED;
+    const DecodeSmem lay = decode_smem_layout(c.head_dim, 8 * sh.nt, nreg, ncw, sh.rpad, stages);
+    if (lay.total > (uint32_t)kSmemLimit)
+        return SHKV_ERR_UNSUPPORTED;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t count_bytes = align_up((uint32_t)(batch * c.num_kv_heads * 4), 256);
+    const size_t lse_bytes = align_up((uint32_t)(2 * pool->num_sms * rows * 4), 256);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    p.block_table = c.block_table;
+    p.seq_lens = c.seq_lens;
+    p.err = c.error_word;
+    p.ws_count = reinterpret_cast<uint32_t *>(ws);
+    p.ws_lse = reinterpret_cast<float *>(ws + count_bytes);
+    p.ws_part = reinterpret_cast<float *>(ws + count_bytes + lse_bytes);
+    p.batch = batch;
+    p.n_models = n_models;
+    p.hq = hq_per_model;
+    p.hkv = c.num_kv_heads;
+    p.group = group;
+    p.rows = rows;
+    p.nrg = sh.nrg;
+    p.wt = sh.wt;
+    p.rpad = sh.rpad;
+    p.stages = stages;
+    p.page_size = c.page_size;
+    p.pages_per_stage = kStageTokens / c.page_size;
+    p.max_pages = c.max_pages_per_seq;
+    p.num_pages = c.num_pages;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    cudaError_t e = launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, lay.total, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, int32_t head_dim, const float *o_part,
+                               const float *lse_part, void *out, float *lse_out, void *stream)
+{
+    if (n_splits < 1 || batch < 0 || rows < 0 || head_dim <= 0 || head_dim % 4 || !o_part || !lse_part || !out)
+        return SHKV_ERR_INVALID_ARG;
+    if (!aligned16(o_part) || ((uintptr_t)lse_part & 3u) || ((uintptr_t)out & 7u) || ((uintptr_t)lse_out & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    cudaError_t e = launch_merge(n_splits, batch, rows, head_dim, o_part, lse_part,
+                                 static_cast<__nv_bfloat16 *>(out), lse_out, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags)
+{
+    if (!pool || !flags)
+        return SHKV_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    *flags = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, pool->cfg.error_word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    if (v && cudaMemset(pool->cfg.error_word, 0, sizeof v) != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    *flags = v;
+    return v ? SHKV_ERR_DEVICE : SHKV_OK;
+}
+
+shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t page_size, int32_t num_kv_heads,
+                             int32_t max_ctas, int64_t *cta_begin, int32_t *num_ctas, int32_t *num_splits)
+{
+    if (!num_ctas)
+        return SHKV_ERR_INVALID_ARG;
+    std::vector<int32_t> prefix((size_t)SHKV_MAX_BATCH + 1);
+    int64_t W = 0;
+    int32_t C = 0;
+    shkv_status st = build_plan(batch, seq_lens, page_size, num_kv_heads, max_ctas, prefix.data(), &W, &C);
+    if (st != SHKV_OK)
+        return st;
+    *num_ctas = C;
+    if (cta_begin)
+        for (int c = 0; c <= C; ++c)
+            cta_begin[c] = (int64_t)c * W / C;
+    if (num_splits) {
+        int32_t n = 0;
+        for (int b = 0; b < batch; ++b) {
+            const int64_t pages = prefix[b + 1] - prefix[b];
+            for (int g = 0; g < num_kv_heads; ++g) {
+                const int64_t u0 = (int64_t)num_kv_heads * prefix[b] + g * pages;
+                const int64_t u1 = u0 + pages - 1;
+                if (((u0 + 1) * C - 1) / W != ((u1 + 1) * C - 1) / W)
+                    ++n;
+            }
+        }
+        *num_splits = n;
+    }
+    return SHKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+"""PyTorch-facing helpers over the libshkv C ABI.
+
+PyTorch provides device memory and streams only; every step of the decode
+path runs in libshkv's CUDA kernels.  ``SharedKVPool`` owns the torch tensors
+the pool description points at (the paged K/V cache of PrefillShare
+Sec. 3.3, shared by all decoders as in ICaRus key design 2) and forwards to
+the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _require(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class SharedKVPool:
+    """One paged KV cache shared by N decoders.
+
+    k_pages / v_pages: bf16 [num_pages, num_kv_heads, page_size, head_dim]
+    block_table: int32 [max_batch, max_pages_per_seq] (fill it, then call
+    ``sync_block_table`` is not needed: the kernels read it in place)
+    seq_lens: int32 [max_batch], owned by the pool after creation.
+    """
+
+    def __init__(self, num_pages: int, page_size: int, num_kv_heads: int, head_dim: int,
+                 max_batch: int, max_pages_per_seq: int, device=None,
+                 k_pages: Optional[torch.Tensor] = None, v_pages: Optional[torch.Tensor] = None,
+                 initial_seq_lens=None):
+        N.load()
+        device = torch.device(device if device is not None else "cuda")
+        shape = (num_pages, num_kv_heads, page_size, head_dim)
+        self.k_pages = k_pages if k_pages is not None else torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.v_pages = v_pages if v_pages is not None else torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        for name, t in (("k_pages", self.k_pages), ("v_pages", self.v_pages)):
+            _require(t, torch.bfloat16, name)
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} shape {tuple(t.shape)} != {shape}")
+        self.block_table = torch.full((max_batch, max_pages_per_seq), -1, dtype=torch.int32, device=device)
+        self.seq_lens = torch.zeros(max_batch, dtype=torch.int32, device=device)
+        self.error_word = torch.zeros(1, dtype=torch.int32, device=device)
+        self.num_pages, self.page_size, self.num_kv_heads, self.head_dim = shape[0], page_size, num_kv_heads, head_dim
+        self.max_batch, self.max_pages_per_seq = max_batch, max_pages_per_seq
+        init = None
+        if initial_seq_lens is not None:
+            init = np.zeros(max_batch, dtype=np.int32)
+            init[: len(initial_seq_lens)] = np.asarray(initial_seq_lens, dtype=np.int32)
+        cfg = N.shkv_pool_config(
+            num_pages=num_pages, page_size=page_size, num_kv_heads=num_kv_heads, head_dim=head_dim,
+            max_batch=max_batch, max_pages_per_seq=max_pages_per_seq,
+            k_pages=self.k_pages.data_ptr(), v_pages=self.v_pages.data_ptr(),
+            block_table=self.block_table.data_ptr(), seq_lens=self.seq_lens.data_ptr(),
+            error_word=self.error_word.data_ptr(),
+            initial_seq_lens=init.ctypes.data if init is not None else None)
+        torch.cuda.synchronize(device)
+        self.handle = N.shkv_pool_create(cfg)
+        self._workspace: Optional[torch.Tensor] = None
+
+    # -- lifecycle ----------------------------------------------------------
+    def close(self):
+        if getattr(self, "handle", None):
+            N.shkv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- lengths --------------------------------------------------------------
+    def set_seq_lens(self, lens, stream=None):
+        arr = np.ascontiguousarray(lens, dtype=np.int32)
+        N.shkv_pool_set_seq_lens(self.handle, len(arr), arr.ctypes.data, _stream_ptr(stream))
+
+    def host_seq_lens(self, batch: Optional[int] = None) -> np.ndarray:
+        batch = self.max_batch if batch is None else batch
+        out = np.zeros(batch, dtype=np.int32)
+        N.shkv_pool_get_seq_lens(self.handle, batch, out.ctypes.data)
+        return out
+
+    # -- the path -------------------------------------------------------------
+    def append_kv(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """Partial-prefill append of [B, T, Hkv, D] bf16 K/V (PrefillShare Sec. 3.3)."""
+        _require(k_new, torch.bfloat16, "k_new")
+        _require(v_new, torch.bfloat16, "v_new")
+        B, T, H, D = k_new.shape
+        if tuple(v_new.shape) != (B, T, H, D) or H != self.num_kv_heads or D != self.head_dim:
+            raise ValueError("k_new/v_new must be [B, T, num_kv_heads, head_dim]")
+        N.shkv_append_kv(self.handle, B, T, k_new.data_ptr(), v_new.data_ptr(), _stream_ptr(stream))
+
+    def workspace(self, batch: int, n_models: int, hq: int) -> torch.Tensor:
+        need = N.shkv_decode_workspace_size(self.handle, batch, n_models, hq)
+        if self._workspace is None or self._workspace.numel() < need:
+            self._workspace = torch.zeros(need, dtype=torch.uint8, device=self.k_pages.device)
+        return self._workspace
+
+    def decode_attention(self, q: torch.Tensor, n_models: int, scale: Optional[float] = None,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         return_lse: bool = False, stream=None):
+        """Stacked decode attention (ICaRus key design 3).
+
+        q: bf16 [B, n_models * hq, head_dim], model-major.  Returns out (bf16,
+        same shape) and, if asked, lse (fp32 [B, n_models * hq]).
+        """
+        _require(q, torch.bfloat16, "q")
+        B, rows, D = q.shape
+        if rows % n_models or D != self.head_dim:
+            raise ValueError("q must be [B, n_models * hq, head_dim]")
+        hq = rows // n_models
+        if scale is None:
+            scale = 1.0 / float(np.sqrt(D))
+        if out is None:
+            out = torch.empty_like(q)
+        _require(out, torch.bfloat16, "out")
+        if return_lse and lse is None:
+            lse = torch.empty((B, rows), dtype=torch.float32, device=q.device)
+        ws = self.workspace(B, n_models, hq)
+        N.shkv_decode_attention(self.handle, B, n_models, hq, q.data_ptr(), float(scale), out.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, ws.data_ptr(), ws.numel(),
+                                _stream_ptr(stream))
+        return (out, lse) if (return_lse or lse is not None) else out
+
+    def check_errors(self, stream=None) -> int:
+        """Synchronize and return (then clear) the device error bits."""
+        return N.shkv_check_errors(self.handle, _stream_ptr(stream))
+
+
+def splitkv_merge(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,
+                  lse_out: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Log-sum-exp merge of split partials: o_part fp32 [S, B, rows, D],
+    lse_part fp32 [S, B, rows] -> (bf16 [B, rows, D], fp32 [B, rows])."""
+    _require(o_part, torch.float32, "o_part")
+    _require(lse_part, torch.float32, "lse_part")
+    S, B, rows, D = o_part.shape
+    if out is None:
+        out = torch.empty((B, rows, D), dtype=torch.bfloat16, device=o_part.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, rows), dtype=torch.float32, device=o_part.device)
+    N.shkv_splitkv_merge(S, B, rows, D, o_part.data_ptr(), lse_part.data_ptr(), out.data_ptr(),
+                         lse_out.data_ptr(), _stream_ptr(stream))
+    return out, lse_out

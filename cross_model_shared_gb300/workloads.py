@@ -271,3 +271,25 @@ def pages_required(lens, P: int, n_models: int, shared: bool) -> int:
 def unique_kv_bytes(wl: Workload) -> int:
     """Bytes of the distinct KV pages one decode step must read."""
     return int(wl.pages_per_request().sum()) * wl.P * wl.Hkv * wl.D * 2 * 2
+
+
+# ---------------------------------------------------------------------------
+# device-side value generator for pools too large to draw on the host
+# ---------------------------------------------------------------------------
+def gen_pool_device(wl: Workload, device="cuda", salt: int = 0, chunk: int = 1 << 28):
+    """K and V pages drawn N(0,1) on the GPU with a seeded torch generator and
+    rounded to bf16 (torch's fp32 -> bf16 cast rounds to nearest even).  Used
+    for multi-GB pools; tests read back the pages they check."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(wl.seed) * 1000003 + 202 + int(salt))
+    shape = (wl.num_pages, wl.Hkv, wl.P, wl.D)
+    out = []
+    for _ in range(2):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = t.view(-1)
+        for s in range(0, flat.numel(), chunk):
+            e = min(flat.numel(), s + chunk)
+            flat[s:e] = torch.randn(e - s, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        out.append(t)
+    return out[0], out[1]

@@ -1,0 +1,219 @@
+/*
+ * shkv.h -- C ABI of libshkv: shared-KV multi-decoder paged decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The problem, as the pages state it:
+ *   - PrefillShare (Sec. 3.3, Sec. 7; Eqs. 8-9): one frozen base prefill
+ *     module writes a single KV cache C_base, held in vLLM PagedAttention
+ *     blocks (pages); N task-specific decode modules all consume that one
+ *     cache; a returning session runs a partial prefill on its new tokens
+ *     only and hands the extended cache on.
+ *   - ICaRus (key designs 2 and 3): all decoders share one frozen logical
+ *     encoder, so their KV caches are bitwise identical and stored once; the
+ *     decoders' queries are concatenated along the head axis and attend the
+ *     same KV together, so each KV byte is read once per step instead of once
+ *     per model.
+ *
+ * Conventions for every call:
+ *   - All device buffers are caller-owned (the library allocates no device
+ *     memory).  Pointers are device pointers unless a parameter says "host".
+ *     Device pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; argument errors are
+ *     returned synchronously before anything is enqueued.
+ *   - bf16 means IEEE bfloat16 bit patterns (uint16_t storage).
+ *   - Calls on one pool are not thread-safe; use one host thread per pool.
+ *   - Device-side faults never trap: a bad page index, an inconsistent
+ *     sequence length or a pipeline wait that runs over its time limit sets a
+ *     bit in the pool's error word, the affected data is skipped (zero
+ *     contribution), and shkv_check_errors() reports it.
+ */
+#ifndef SHKV_H
+#define SHKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SHKV_OK = 0,
+    SHKV_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, shape mismatch */
+    SHKV_ERR_CAPACITY = 2,      /* a sequence would exceed max_pages_per_seq * page_size */
+    SHKV_ERR_UNSUPPORTED = 3,   /* outside the supported set (see shkv_decode_attention) */
+    SHKV_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    SHKV_ERR_DEVICE = 5         /* shkv_check_errors found device error bits */
+} shkv_status;
+
+/* Bits of the device error word. */
+#define SHKV_ERRF_PAGE_OOB 0x1u   /* block-table entry outside [0, num_pages) */
+#define SHKV_ERRF_SEQ_LEN 0x2u    /* device seq_lens disagrees with the pool's host copy */
+#define SHKV_ERRF_TIMEOUT 0x4u    /* a pipeline wait exceeded its time limit */
+
+/* Largest batch a single decode / append call accepts. */
+#define SHKV_MAX_BATCH 1024
+
+typedef struct shkv_pool shkv_pool; /* opaque host handle, owns no device memory */
+
+/*
+ * Pool description.  The pool is the paged KV cache of PrefillShare Sec. 3.3
+ * (vLLM blocks), shared by every decoder (ICaRus key design 2).
+ *   k_pages, v_pages  device bf16 [num_pages, num_kv_heads, page_size, head_dim]
+ *   block_table       device int32 [max_batch, max_pages_per_seq]; entry
+ *                     (b, i) is the physical page of request b's logical page
+ *                     i.  The caller fills it; one table serves all decoders.
+ *   seq_lens          device int32 [max_batch]; cached tokens per request.
+ *                     After creation the pool owns its contents: change it
+ *                     only through shkv_append_kv / shkv_pool_set_seq_lens.
+ *   error_word        device uint32 (one word), zeroed by shkv_pool_create.
+ *   initial_seq_lens  host int32 [max_batch] or NULL (all zero); copied to
+ *                     seq_lens and to the pool's host copy at creation.
+ */
+typedef struct {
+    int32_t num_pages;
+    int32_t page_size;        /* 16 or 32 tokens */
+    int32_t num_kv_heads;
+    int32_t head_dim;         /* 64 or 128 */
+    int32_t max_batch;
+    int32_t max_pages_per_seq;
+    void *k_pages;
+    void *v_pages;
+    int32_t *block_table;
+    int32_t *seq_lens;
+    uint32_t *error_word;
+    const int32_t *initial_seq_lens; /* host, nullable */
+} shkv_pool_config;
+
+/*
+ * Create a pool handle over caller-owned memory.  Validates the description,
+ * builds the TMA descriptors of the K and V pools, writes the initial
+ * sequence lengths and zeroes the error word (synchronously, on the current
+ * device).  Errors: SHKV_ERR_INVALID_ARG, SHKV_ERR_UNSUPPORTED (page size or
+ * head dim), SHKV_ERR_CUDA.  On success *out receives the handle.
+ */
+shkv_status shkv_pool_create(const shkv_pool_config *cfg, shkv_pool **out);
+
+/* Release the host handle.  Device memory stays with the caller. */
+shkv_status shkv_pool_destroy(shkv_pool *pool);
+
+/*
+ * Set the cached length of requests [0, batch) from host array `lens`
+ * (each in [0, max_pages_per_seq * page_size]).  Updates the pool's host copy
+ * and copies to seq_lens on `stream`, then synchronizes `stream`.
+ * Errors: SHKV_ERR_INVALID_ARG, SHKV_ERR_CAPACITY, SHKV_ERR_CUDA.
+ */
+shkv_status shkv_pool_set_seq_lens(shkv_pool *pool, int32_t batch, const int32_t *lens,
+                                   void *stream);
+
+/* Copy the pool's host copy of the lengths of requests [0, batch) to host
+ * array `lens`.  No device work. */
+shkv_status shkv_pool_get_seq_lens(const shkv_pool *pool, int32_t batch, int32_t *lens);
+
+/*
+ * Partial-prefill append (PrefillShare Sec. 3.3 / Sec. 7: a cache hit runs
+ * prefill on the new tokens only and hands the extended cache on).  For every
+ * request b < batch and new token t < n_new_tokens:
+ *   pool[block_table[b][(L_b+t)/P], g, (L_b+t)%P, :] = new[b, t, g, :]
+ * for K and V and every KV head g, then L_b += n_new_tokens.  A bit-exact
+ * copy.  The block table must already map the pages the new tokens land in.
+ *   k_new, v_new  device bf16 [batch, n_new_tokens, num_kv_heads, head_dim]
+ * Errors: SHKV_ERR_INVALID_ARG; SHKV_ERR_CAPACITY if L_b + n_new_tokens
+ * exceeds max_pages_per_seq * page_size; SHKV_ERR_CUDA.  A block-table entry
+ * outside the pool sets SHKV_ERRF_PAGE_OOB and that token is not written.
+ */
+shkv_status shkv_append_kv(shkv_pool *pool, int32_t batch, int32_t n_new_tokens,
+                           const void *k_new, const void *v_new, void *stream);
+
+/*
+ * Bytes of device workspace shkv_decode_attention needs for this shape
+ * (split-KV partials plus per-(request, KV head) arrival counters).
+ */
+shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int32_t n_models,
+                                       int32_t hq_per_model, size_t *bytes);
+
+/*
+ * Shared-KV decode attention (ICaRus key design 3 over the PrefillShare
+ * paged cache).  The n_models decoders' queries are stacked model-major
+ * along the head axis, row r = m * hq_per_model + h; query head h of every
+ * decoder uses KV head g = h / (hq_per_model / num_kv_heads).  For each
+ * request b < batch and row r:
+ *   s_t = scale * <q[b, r, :], K_b[t, g, :]>   for t < L_b (no causal mask)
+ *   out[b, r, :] = sum_t softmax(s)_t V_b[t, g, :]
+ *   lse_out[b, r] = ln sum_t exp(s_t)
+ * where K_b / V_b are read through the shared block table.  Each KV page of
+ * each head is read from HBM once for all n_models * group stacked rows.
+ * Long contexts are split across SMs (flash-decoding) and the splits merged
+ * by log-sum-exp inside the same launch.
+ *   q        device bf16 [batch, n_models * hq_per_model, head_dim]
+ *   out      device bf16, same shape (round to nearest even from fp32)
+ *   lse_out  device fp32 [batch, n_models * hq_per_model], or NULL
+ *   workspace, workspace_bytes
+ *            device scratch of at least shkv_decode_workspace_size() bytes.
+ *            It must be zero-filled before its first use; every call that
+ *            completes without device error bits leaves it zero-filled again,
+ *            so it can be reused.  Calls sharing one workspace must not
+ *            overlap on the GPU.
+ * Supported: batch in [1, SHKV_MAX_BATCH], every L_b >= 1,
+ * hq_per_model % num_kv_heads == 0, rows per KV head
+ * n_models * hq_per_model / num_kv_heads <= 64.
+ * Errors: SHKV_ERR_INVALID_ARG (null pointers, L_b == 0, shapes),
+ * SHKV_ERR_UNSUPPORTED (outside the set above), SHKV_ERR_CUDA.
+ */
+shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_models,
+                                  int32_t hq_per_model, const void *q, float scale, void *out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * Log-sum-exp merge of split-KV partials (the flash-decoding reduction for
+ * long contexts).  For every (b, row):
+ *   M = max_s lse_part[s, b, row];  w_s = exp(lse_part[s, b, row] - M)
+ *   out[b, row, :] = sum_s w_s o_part[s, b, row, :] / sum_s w_s
+ *   lse_out[b, row] = M + ln sum_s w_s
+ * Partials with lse = -inf carry no weight; a row whose partials are all
+ * -inf gets out = 0 and lse = -inf.
+ *   o_part   device fp32 [n_splits, batch, rows, head_dim] (each partial
+ *            already normalised by its own softmax sum)
+ *   lse_part device fp32 [n_splits, batch, rows] (natural log)
+ *   out      device bf16 [batch, rows, head_dim]
+ *   lse_out  device fp32 [batch, rows], or NULL
+ * head_dim must be a multiple of 4.  Errors: SHKV_ERR_INVALID_ARG, SHKV_ERR_CUDA.
+ */
+shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, int32_t head_dim,
+                               const float *o_part, const float *lse_part, void *out,
+                               float *lse_out, void *stream);
+
+/*
+ * Synchronize `stream`, then read and clear the pool's device error word.
+ * *flags receives the SHKV_ERRF_* bits.  Returns SHKV_ERR_DEVICE if any bit
+ * was set, SHKV_OK otherwise (SHKV_ERR_CUDA if the stream reported an error).
+ */
+shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags);
+
+/*
+ * Host-only view of how shkv_decode_attention divides work (no device
+ * needed).  The (request, KV head, page) chunks, ordered request-major, are
+ * cut into `num_ctas` contiguous ranges of equal size (+-1 chunk), one per
+ * persistent CTA; a (request, head) whose pages straddle a cut is split and
+ * merged by log-sum-exp.
+ *   seq_lens    host int32 [batch] (each >= 1)
+ *   max_ctas    upper bound on CTAs (normally the SM count)
+ *   cta_begin   host int64 [max_ctas + 1] or NULL; receives the first chunk
+ *               of every CTA and, at [num_ctas], the total chunk count
+ *   num_ctas    receives the CTA count used
+ *   num_splits  receives the number of (request, head) units that are split
+ */
+shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t page_size,
+                             int32_t num_kv_heads, int32_t max_ctas, int64_t *cta_begin,
+                             int32_t *num_ctas, int32_t *num_splits);
+
+/* Static description of a status code. */
+const char *shkv_status_string(shkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SHKV_H */

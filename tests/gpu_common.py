@@ -1,0 +1,74 @@
+"""Helpers shared by the GPU parity tests: build a libshkv pool from seeded
+inputs, read pages back for the oracle, and apply the stated tolerance.
+
+Tolerance (bf16 inputs, fp32 accumulation, fp64 oracle): elementwise
+max |gpu - ref| <= 1e-2, and per-row normwise max_k |gpu - ref| / max_k |ref|
+<= 2e-2 (outputs are convex combinations of V rows whose magnitude shrinks
+with context length, so an elementwise relative error is ill-posed near 0).
+"""
+import numpy as np
+import torch
+
+import oracle
+from cross_model_shared_gb300 import SharedKVPool
+from cross_model_shared_gb300 import workloads as W
+
+ABS_TOL = 1e-2
+REL_TOL = 2e-2
+LSE_TOL = 2e-3
+
+
+def bits_to_torch(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def torch_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_pool(wl: W.Workload, k, v, lens=None, extra_max_batch: int = 0) -> SharedKVPool:
+    """Pool over the given K/V (numpy bf16 bits or bf16 CUDA tensors)."""
+    if isinstance(k, np.ndarray):
+        k, v = bits_to_torch(k), bits_to_torch(v)
+    lens = wl.lens_final if lens is None else lens
+    pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B + extra_max_batch,
+                        max_pages_per_seq=wl.max_pages_per_seq, k_pages=k, v_pages=v,
+                        initial_seq_lens=np.asarray(lens, np.int32))
+    pool.block_table[: wl.B].copy_(torch.from_numpy(wl.block_table))
+    torch.cuda.synchronize()
+    return pool
+
+
+def compare(out_gpu: torch.Tensor, ref: np.ndarray, lse_gpu=None, lse_ref=None, what=""):
+    got = out_gpu.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    abs_err = float(err.max()) if err.size else 0.0
+    denom = np.maximum(np.abs(ref).max(axis=-1), 1e-30)
+    rel_err = float((err.max(axis=-1) / denom).max()) if err.size else 0.0
+    assert abs_err <= ABS_TOL, f"{what}: max abs error {abs_err:.3e} > {ABS_TOL}"
+    assert rel_err <= REL_TOL, f"{what}: max row-relative error {rel_err:.3e} > {REL_TOL}"
+    if lse_gpu is not None:
+        lg = lse_gpu.cpu().numpy().astype(np.float64)
+        lerr = float(np.abs(lg - lse_ref).max())
+        assert lerr <= LSE_TOL, f"{what}: lse error {lerr:.3e}"
+    return abs_err, rel_err
+
+
+def oracle_for_requests(wl: W.Workload, q_bits: np.ndarray, k_dev: torch.Tensor, v_dev: torch.Tensor,
+                        requests, lens=None, nthreads: int = 0):
+    """Run the oracle on a subset of requests, reading only their pages back
+    from the device pool.  Returns {b: (out [rows, D], lse [rows])}."""
+    lens = wl.lens_final if lens is None else np.asarray(lens)
+    res = {}
+    for b in requests:
+        npg = int((lens[b] + wl.P - 1) // wl.P)
+        ids = torch.from_numpy(wl.block_table[b, :npg].astype(np.int64)).to(k_dev.device)
+        kb = torch_to_bits(k_dev.index_select(0, ids))
+        vb = torch_to_bits(v_dev.index_select(0, ids))
+        bt = np.arange(npg, dtype=np.int32)[None, :]
+        out, lse = oracle.decode_attention(q_bits[b:b + 1], kb, vb, bt, np.array([lens[b]], np.int32),
+                                           n_models=wl.N, hq=wl.Hq, scale=wl.scale, nthreads=nthreads)
+        res[b] = (out[0], lse[0])
+    return res

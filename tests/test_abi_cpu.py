@@ -1,0 +1,84 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and its host-only entry points (status strings, the split
+plan) behave.  No compute call is made without a GPU."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from cross_model_shared_gb300 import _native as N
+from cross_model_shared_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "shkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(shkv_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(N.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    syms = os.popen(f"nm -D --defined-only {N.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", syms), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert N.status_string(st)
+    assert N.status_string(N.SHKV_OK) == "ok"
+
+
+def test_null_arguments_are_rejected_without_a_device(lib):
+    assert lib.shkv_pool_create(None, None) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_pool_destroy(None) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_decode_attention(None, 1, 1, 1, None, 1.0, None, None, None, 0, None) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_splitkv_merge(0, 1, 1, 4, None, None, None, None, None) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_splitkv_merge(1, 1, 1, 6, 16, 16, 16, None, None) == N.SHKV_ERR_INVALID_ARG  # D % 4
+
+
+@pytest.mark.parametrize("lens,P,H,C", [
+    ([256], 16, 2, 152),                       # tiny
+    ([1, 2, 3, 4000, 17], 16, 8, 152),
+    ([131584] * 4, 16, 8, 152),                # long context: every unit split
+    (list(range(1, 300)), 32, 8, 152),
+    ([5], 16, 1, 152),                         # fewer chunks than CTAs
+])
+def test_plan_is_balanced_and_covers_every_chunk(lib, lens, P, H, C):
+    begin, nc, ns = N.shkv_plan_decode(lens, P, H, C)
+    pages = [(l + P - 1) // P for l in lens]
+    W = H * sum(pages)
+    assert begin[0] == 0 and begin[-1] == W
+    sizes = np.diff(begin)
+    assert (sizes >= 1).all() and sizes.max() - sizes.min() <= 1
+    assert nc <= C and nc == min(C, max(1, -(-W // 8)))
+    # brute-force count of (request, head) units that straddle a cut
+    cuts = set(begin[1:-1].tolist())
+    n = 0
+    off = 0
+    for p in pages:
+        for _ in range(H):
+            n += any(off < c < off + p for c in cuts)
+            off += p
+    assert ns == n
+    assert ns <= nc - 1
+
+
+def test_plan_rejects_empty_requests_and_oversized_batches(lib):
+    with pytest.raises(N.ShkvError):
+        N.shkv_plan_decode([3, 0, 5], 16, 2, 152)
+    with pytest.raises(N.ShkvError):
+        N.shkv_plan_decode([1] * (N.SHKV_MAX_BATCH + 1), 16, 2, 152)
