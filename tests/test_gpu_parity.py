@@ -122,8 +122,9 @@ def test_long_context_with_partial_prefill_append():
     kn = torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
     vn = torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
     # pages the append touches, before
-    touched = sorted({int(wl.block_table[b, (int(wl.lens_prefill[b]) + t) // wl.P])
-                      for b in range(wl.B) for t in (0, wl.n_append - 1)})
+    first = [int(wl.lens_prefill[b]) // wl.P for b in range(wl.B)]
+    last = [(int(wl.lens_prefill[b]) + wl.n_append - 1) // wl.P for b in range(wl.B)]
+    touched = sorted({int(wl.block_table[b, pi]) for b in range(wl.B) for pi in range(first[b], last[b] + 1)})
     tt = torch.tensor(touched, device="cuda")
     k_before = torch_to_bits(k_dev.index_select(0, tt))
     v_before = torch_to_bits(v_dev.index_select(0, tt))
@@ -135,8 +136,7 @@ def test_long_context_with_partial_prefill_append():
     remap = {p: i for i, p in enumerate(touched)}
     bt_small = np.full_like(wl.block_table, -1)
     for b in range(wl.B):
-        for t in (0, wl.n_append - 1):
-            pi = (int(wl.lens_prefill[b]) + t) // wl.P
+        for pi in range(first[b], last[b] + 1):
             bt_small[b, pi] = remap[int(wl.block_table[b, pi])]
     k_exp, v_exp, lens_exp = oracle.append_kv(k_before, v_before, bt_small, wl.lens_prefill,
                                               torch_to_bits(kn), torch_to_bits(vn))
