@@ -30,8 +30,10 @@ SHKV_MAX_BATCH = 1024
 EXPORTS = [
     "shkv_pool_create", "shkv_pool_destroy", "shkv_pool_set_seq_lens", "shkv_pool_get_seq_lens",
     "shkv_append_kv", "shkv_decode_workspace_size", "shkv_decode_attention", "shkv_splitkv_merge",
-    "shkv_check_errors", "shkv_plan_decode", "shkv_status_string",
+    "shkv_check_errors", "shkv_plan_decode", "shkv_status_string", "shkv_decode_attention_noalloc",
 ]
+
+SHKV_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class shkv_pool_config(ctypes.Structure):
@@ -81,6 +83,7 @@ def load() -> ctypes.CDLL:
         "shkv_splitkv_merge": [i32, i32, i32, i32, vp, vp, vp, vp, vp],
         "shkv_check_errors": [vp, vp, u32p],
         "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+        "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -162,3 +165,11 @@ def shkv_plan_decode(lens, page_size: int, num_kv_heads: int, max_ctas: int):
     _check(load().shkv_plan_decode(len(lens), lens.ctypes.data, page_size, num_kv_heads, max_ctas,
                                    begin.ctypes.data, ctypes.byref(nc), ctypes.byref(ns)), "shkv_plan_decode")
     return begin[: nc.value + 1].copy(), nc.value, ns.value
+
+
+def shkv_decode_attention_noalloc(pool: int, batch: int, n_models: int, hq: int, q: int, scale: float, out: int,
+                                  lse_out: int, stream: int) -> None:
+    """Decode attention on the library's static device scratch (no workspace
+    argument, no allocation)."""
+    _check(load().shkv_decode_attention_noalloc(pool, batch, n_models, hq, q, scale, out, lse_out, stream),
+           "shkv_decode_attention_noalloc")

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -422,3 +423,66 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// decode without a caller workspace: static device scratch
+// ---------------------------------------------------------------------------
+// The split-KV scratch of shkv_decode_attention_noalloc.  Device globals are
+// zero-initialised when the module loads; each call re-zeroes the arrival
+// counters at its front before launching.
+static __device__ __align__(256) unsigned char shkv_noalloc_scratch[SHKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of shkv_noalloc_scratch on the current device, looked up
+// once per device and cached.  (In host code the array's name is only a
+// host-side stand-in, never a device address.)
+shkv_status noalloc_scratch(int device, void **ptr)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return SHKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, shkv_noalloc_scratch) != cudaSuccess || !p)
+            return SHKV_ERR_CUDA;
+        g_noalloc_ptr[device] = p;
+    }
+    *ptr = g_noalloc_ptr[device];
+    return SHKV_OK;
+}
+
+}  // namespace
+
+extern "C" shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t batch, int32_t n_models,
+                                                     int32_t hq_per_model, const void *q, float scale, void *out,
+                                                     float *lse_out, void *stream)
+{
+    if (!pool)
+        return SHKV_ERR_INVALID_ARG;
+    size_t need = 0;
+    shkv_status st = shkv_decode_workspace_size(pool, batch, n_models, hq_per_model, &need);
+    if (st != SHKV_OK)
+        return st;
+    if (need > (size_t)SHKV_NOALLOC_SCRATCH_BYTES)
+        return SHKV_ERR_UNSUPPORTED;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    if (device != pool->device)
+        return SHKV_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    st = noalloc_scratch(device, &scratch);
+    if (st != SHKV_OK)
+        return st;
+    // the per-(request, head) arrival counters lead the workspace and must start at zero
+    const size_t count_bytes = align_up((uint32_t)(batch * pool->cfg.num_kv_heads * 4), 256);
+    if (cudaMemsetAsync(scratch, 0, count_bytes, (cudaStream_t)stream) != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    return shkv_decode_attention(pool, batch, n_models, hq_per_model, q, scale, out, lse_out, scratch, need,
+                                 stream);
+}

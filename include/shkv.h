@@ -209,6 +209,43 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
                              int32_t num_kv_heads, int32_t max_ctas, int64_t *cta_begin,
                              int32_t *num_ctas, int32_t *num_splits);
 
+/*
+ * Bytes of the library's static device scratch used by
+ * shkv_decode_attention_noalloc.
+ */
+#define SHKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * shkv_decode_attention without a caller-provided workspace.  The pages have
+ * no counterpart to this call: it exists for callers that cannot call
+ * cudaMalloc -- code hosted inside a framework that owns all device memory
+ * through its own allocator or a fixed memory budget and offers no
+ * allocation hook, or code on a latency-critical path where cudaMalloc's
+ * implicit device synchronisation is not acceptable.
+ *
+ * Same arguments, layouts, results and errors as shkv_decode_attention, minus
+ * the workspace.  The split-KV scratch is a file-scope static device array of
+ * SHKV_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the library
+ * holds until the process exits.
+ *   - The call allocates nothing: no cudaMalloc / cudaFree / allocating
+ *     library routine.  Before each launch it clears the scratch's arrival
+ *     counters with cudaMemsetAsync on `stream`.
+ *   - Set-up: the first call on a device (the current device, which must be
+ *     the pool's device) looks up the scratch's device address with
+ *     cudaGetSymbolAddress and caches it.  Make that first call before any
+ *     stream capture on that device.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents; calls whose executions overlap on the GPU (different streams
+ *     without ordering) race on it and give wrong results.
+ * Errors: those of shkv_decode_attention; SHKV_ERR_UNSUPPORTED if the scratch
+ * this shape needs (shkv_decode_workspace_size) exceeds
+ * SHKV_NOALLOC_SCRATCH_BYTES; SHKV_ERR_INVALID_ARG if the current device is
+ * not the pool's.
+ */
+shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t batch, int32_t n_models,
+                                          int32_t hq_per_model, const void *q, float scale,
+                                          void *out, float *lse_out, void *stream);
+
 /* Static description of a status code. */
 const char *shkv_status_string(shkv_status status);
 
