@@ -23,6 +23,7 @@ SHKV_ERR_DEVICE = 5
 SHKV_ERRF_PAGE_OOB = 0x1
 SHKV_ERRF_SEQ_LEN = 0x2
 SHKV_ERRF_TIMEOUT = 0x4
+SHKV_ERRF_PIPELINE = 0x8
 
 SHKV_MAX_BATCH = 1024
 

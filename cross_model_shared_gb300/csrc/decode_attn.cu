@@ -18,13 +18,16 @@
 //   arrival counter, no waiting) merges them.  No CTA ever waits for another.
 //
 // Inside a CTA:
-//   * one producer warp issues TMA tensor loads (128-byte swizzle, L2
-//     evict-first) of whole (page, head) K and V chunks into an mbarrier ring
-//     of kStageTokens-token slots, plus a bulk copy of the segment's R query
-//     rows; block-table entries are prefetched 32 at a time;
-//   * consumer warps take slots round-robin.  Each warp owns 8 or 16 stacked
-//     rows (a row group); larger R uses several row groups that read the same
-//     slot.  Per slot a warp computes S^T = K Q^T with tokens as the MMA M
+//   * one producer warp streams K and V into an mbarrier ring of
+//     kStageTokens-token slots.  Each copy is one 3-D TMA box covering a whole
+//     row-block of one head's page (4 or 8 KiB, 128-byte swizzle, L2
+//     evict-first), and the copies of a slot are issued by several lanes in
+//     one instruction: a single thread issuing small copies one at a time
+//     cannot keep HBM busy.  A bulk copy brings the segment's R query rows;
+//     block-table entries are prefetched 32 at a time;
+//   * consumer warps take slots round-robin, fewer warps than slots so most
+//     of the ring stays in flight.  Each warp owns 8 or 16 stacked rows (a
+//     row group); larger R uses several row groups that read the same slot.  Per slot a warp computes S^T = K Q^T with tokens as the MMA M
 //     dimension (16 tokens x 8 rows per mma.sync m16n8k16), so R = 8 rows fill
 //     an MMA exactly; an online softmax in base 2 follows; P^T is transposed in
 //     registers (movmatrix) and O^T += V^T P^T accumulates in fp32;
@@ -127,17 +130,21 @@ __device__ __forceinline__ uint32_t qempty_bar(const Ctx &c, int i, int stages)
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
+// Stage j of a segment holds the kStageTokens logical tokens starting at
+// p0*P + j*kStageTokens, as one or two row-blocks of BR = min(P, kStageTokens)
+// rows, each row-block inside one page.
 template <int D>
 __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,
                          const Ctx &c)
 {
-    constexpr int NBOX = D / 64;
+    constexpr int TT = kStageTokens;
     const int lane = threadIdx.x & 31;
     const int stages = p.stages;
-    const int SP = p.pages_per_stage;
     const int P = p.page_size;
-    const uint32_t box_bytes = (uint32_t)P * 128u;
-    const uint32_t page_bytes_kv = 2u * (uint32_t)P * D * 2u;
+    const int BR = p.box_rows;
+    const int RB = TT / BR;                        // row-blocks per stage (1 or 2)
+    const int log2P = 31 - __clz(P);
+    const uint32_t rb_bytes_kv = 2u * (uint32_t)BR * D * 2u;
     const uint64_t pol = l2_evict_first_policy();
     if (lane == 0) {
         prefetch_tensormap(tmK);
@@ -167,57 +174,63 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
                           qfull_bar(c, qb, stages));
             q_issued[qb] = seg;
         }
-        // --- K/V pages of the segment
-        const int nst = (s.p1 - s.p0 + SP - 1) / SP;
+        // --- K/V row-blocks of the segment
+        const int tok_end = s.p1 * P;
+        const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
         const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
-        int w0 = s.p0;
+        int w0 = s.p0;                                   // block-table window [w0, w0+32)
         int cur = (w0 + lane < s.p1) ? __ldg(btrow + w0 + lane) : -1;
         int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
-        for (int j = 0; j < nst; ++j) {
-            const int k = kbase + j;
+        // Lane 4*sub + 2*rb + kv copies row-block rb of K (kv = 0) or V
+        // (kv = 1) for stage j + sub of this iteration.
+        const int sub = lane >> 2;
+        const int my_rb = (lane >> 1) & 1;
+        const int my_kv = lane & 1;
+        for (int j = 0; j < nst; j += kStagesPerIssue) {
+            const int jj = j + sub;
+            const bool in_iter = sub < kStagesPerIssue && jj < nst;
+            const int k = kbase + jj;
             const int slot = k % stages;
-            const int pg0 = s.p0 + j * SP;
-            if (pg0 >= w0 + 32) {
+            const int tok0 = s.p0 * P + jj * TT;
+            // window of block-table entries for the first page of this iteration
+            const int pg_first = (s.p0 * P + j * TT) >> log2P;
+            if (pg_first >= w0 + 32) {
                 w0 += 32;
                 cur = nxt;
                 nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
             }
-            const int id0 = __shfl_sync(0xffffffffu, cur, (pg0 - w0) & 31);
-            const int id1 = __shfl_sync(0xffffffffu, cur, (pg0 - w0 + 1) & 31);
-            if (alive) {
-                bool ok = mbar_wait_bounded(empty_bar(c, slot, stages), ((k / stages) & 1) ^ 1, c.abort_flag, p.err);
-                alive = __all_sync(0xffffffffu, ok);
-            }
-            if (alive && lane == 0) {
-                uint32_t mask = 0, bytes = 0;
-                for (int i = 0; i < SP; ++i) {
-                    const int id = i == 0 ? id0 : id1;
-                    if (pg0 + i >= s.p1)
-                        continue;
-                    if (id >= 0 && id < p.num_pages) {
-                        mask |= 1u << i;
-                        bytes += page_bytes_kv;
-                    } else {
+            const int my_tok = tok0 + my_rb * BR;
+            const int my_pg = my_tok >> log2P;
+            const int my_id = __shfl_sync(0xffffffffu, cur, (my_pg - w0) & 31);
+            bool ok = true;
+            if (alive && in_iter && (lane & 3) == 0)
+                ok = mbar_wait_bounded(empty_bar(c, slot, stages), ((k / stages) & 1) ^ 1, c.abort_flag, p.err);
+            alive = alive && __all_sync(0xffffffffu, ok);
+            const bool my_valid = in_iter && my_rb < RB && my_tok < tok_end && my_id >= 0 && my_id < p.num_pages;
+            const uint32_t vmask = __ballot_sync(0xffffffffu, my_valid && my_kv == 0);
+            if (alive && in_iter && (lane & 3) == 0) {
+                const uint32_t bits = vmask >> lane;     // bit 0: rb 0, bit 2: rb 1
+                uint32_t mask = 0;
+                for (int rb = 0; rb < RB; ++rb) {
+                    if ((bits >> (2 * rb)) & 1u)
+                        mask |= 1u << rb;
+                    else if (tok0 + rb * BR < tok_end)
                         atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
-                    }
                 }
                 volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
-                meta[slot] = mask;
-                const uint32_t kdst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
-                const uint32_t vdst = kdst + (uint32_t)(kStageTokens * D * 2);
-                mbar_arrive_expect_tx(full_bar(c, slot), bytes);
-                for (int i = 0; i < SP; ++i) {
-                    if (!(mask & (1u << i)))
-                        continue;
-                    const int y = ((i == 0 ? id0 : id1) * p.hkv + s.g) * P;
-#pragma unroll
-                    for (int x = 0; x < NBOX; ++x) {
-                        const uint32_t off = (uint32_t)x * (kStageTokens * 128u) + (uint32_t)i * box_bytes;
-                        tma_load_2d(kdst + off, tmK, x * 64, y, full_bar(c, slot), pol);
-                        tma_load_2d(vdst + off, tmV, x * 64, y, full_bar(c, slot), pol);
-                    }
-                }
-                last_issued_stage = k;
+                meta[slot] = mask | ((uint32_t)k << 8);   // valid row-blocks + stage tag
+                mbar_arrive_expect_tx(full_bar(c, slot), (uint32_t)__popc(mask) * rb_bytes_kv);
+            }
+            __syncwarp();
+            if (alive && my_valid) {
+                const uint32_t dst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes +
+                                     (uint32_t)my_kv * (TT * D * 2) + (uint32_t)my_rb * (BR * D * 2);
+                const int y = (my_id * p.hkv + s.g) * P + (my_tok & (P - 1));
+                tma_load_3d_row(dst, my_kv ? tmV : tmK, y, full_bar(c, slot), pol);
+            }
+            if (alive) {
+                const int last = kbase + (j + kStagesPerIssue < nst ? j + kStagesPerIssue : nst) - 1;
+                last_issued_stage = last;
             }
             __syncwarp();
         }
@@ -253,9 +266,16 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
     const int wtid = warp - rg * p.wt;
     const int row0 = rg * ROWS_W;
     const int stages = p.stages;
-    const int SP = p.pages_per_stage;
+    constexpr int TT = kStageTokens;
+    constexpr int MTS = TT / 16;                   // 16-token MMA tiles per stage
     const int P = p.page_size;
+    const int BR = p.box_rows;
+    const int log2BR = 31 - __clz(BR);
     const float sl2 = p.scale_log2;
+    // Stage layout: [row-block][column half][row][128 bytes], swizzled per 8 rows.
+    auto row_off = [&](int t) -> uint32_t {
+        return (uint32_t)((t >> log2BR) * (BR * D * 2) + (t & (BR - 1)) * 128);
+    };
 
     float *comb_o = reinterpret_cast<float *>(c.smem + c.lay.comb_o);
     float *comb_m = reinterpret_cast<float *>(c.smem + c.lay.comb_m);
@@ -273,7 +293,8 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
     int kbase = 0, seg = 0;
     while (idx < c.cta_end) {
         const Segment s = locate(p, idx, c.cta_end);
-        const int nst = (s.p1 - s.p0 + SP - 1) / SP;
+        const int tok_end = s.p1 * P;
+        const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
         const int qb = seg & 1;
 
         // --- query fragments (B operand of S^T = K Q^T): rows row0.., all D
@@ -309,6 +330,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
             L = L < 0 ? 0 : (L > s.pages_b * P ? s.pages_b * P : L);
         }
+        const int lim = L < tok_end ? L : tok_end;     // tokens of this segment that count
 
         float o[KSTEPS][NT][4];
         float mrow[NT][2], lrow[NT][2];
@@ -330,72 +352,88 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 ok = __all_sync(0xffffffffu, ok);
                 alive = ok;
             }
+            bool tag_ok = true;
+            if (ok && (meta[slot] >> 8) != ((uint32_t)k & 0xffffffu)) {
+                // The slot holds another stage: report it, stop this CTA
+                // (bounded) and do not arrive, so no copy is re-armed over it.
+                tag_ok = false;
+                ok = false;
+                alive = false;
+                if (lane == 0) {
+                    atomicOr(p.err, SHKV_ERRF_PIPELINE);
+                    *c.abort_flag = 1u;
+                }
+            }
             if (ok) {
                 const uint32_t kst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
-                const uint32_t vst = kst + (uint32_t)(kStageTokens * D * 2);
-                const uint32_t mask = meta[slot];
-                const int pg0 = s.p0 + j * SP;
-                const int tok_base = pg0 * P;   // logical token of slot row 0
-                const uint32_t full_mask = (1u << SP) - 1u;
-                const bool all_valid = (pg0 + SP <= s.p1) && (mask == full_mask) && (tok_base + kStageTokens <= L);
+                const uint32_t vst = kst + (uint32_t)(TT * D * 2);
+                const uint32_t mask = meta[slot] & 0xffu;
+                const int tok0 = s.p0 * P + j * TT;       // logical token of slot row 0
+                const uint32_t full_mask = (1u << (TT / BR)) - 1u;
+                const bool all_valid = (mask == full_mask) && (tok0 + TT <= lim);
                 auto tok_valid = [&](int t) -> bool {
-                    const int i = t / P;
-                    return ((mask >> i) & 1u) && (pg0 + i < s.p1) && (tok_base + t < L);
+                    return ((mask >> (t >> log2BR)) & 1u) && (tok0 + t < lim);
                 };
                 if (!all_valid) {
                     // Rows that are masked may hold stale or non-finite bits:
                     // zero their V so 0 * V stays 0 in the PV product.
-                    for (int e = lane; e < kStageTokens * (D / 8); e += 32) {
+                    for (int e = lane; e < TT * (D / 8); e += 32) {
                         const int t = e / (D / 8);
                         const int cchunk = e - t * (D / 8);
                         if (!tok_valid(t))
-                            st_shared_zero16(vst + (uint32_t)((cchunk >> 3) * (kStageTokens * 128) + t * 128 + (cchunk & 7) * 16));
+                            st_shared_zero16(vst + row_off(t) + (uint32_t)((cchunk >> 3) * (BR * 128) + (cchunk & 7) * 16));
                     }
                     __syncwarp();
                 }
 
-                // S^T[tok, row] = K[tok, :] . Q[row, :]
-                float sc[2][NT][4];
+                // S^T[tok, row] = K[tok, :] . Q[row, :]; even and odd k-steps
+                // accumulate separately to halve the dependent MMA chain.
+                float sc[MTS][NT][4], sc2[MTS][NT][4];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sc[mt][nt][e] = sc2[mt][nt][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
+                    for (int mt = 0; mt < MTS; ++mt) {
                         const int tok = mt * 16 + k_tok;
                         const int col = ks * 16 + k_col;
-                        const uint32_t addr = kst + (uint32_t)((col >> 6) * (kStageTokens * 128) + tok * 128 +
-                                                               ((((col & 63) >> 3) ^ (tok & 7)) << 4));
+                        const uint32_t addr = kst + row_off(tok) + (uint32_t)((col >> 6) * (BR * 128) +
+                                                                            ((((col & 63) >> 3) ^ (tok & 7)) << 4));
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma_bf16(sc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+                            mma_bf16((ks & 1) ? sc2[mt][nt] : sc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
                     }
                 }
 
                 // online softmax in base 2: x = s * scale * log2(e)
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float x = sc[mt][nt][e] * sl2;
+                            float x = (sc[mt][nt][e] + sc2[mt][nt][e]) * sl2;
                             if (!all_valid && !tok_valid(mt * 16 + (lane >> 2) + (e >> 1) * 8))
                                 x = -INFINITY;
                             sc[mt][nt][e] = x;
                         }
-                uint32_t pb[2][NT][2];
+                uint32_t pb[MTS][NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float mx[2];
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
-                        float v = fmaxf(fmaxf(sc[0][nt][i], sc[0][nt][i + 2]), fmaxf(sc[1][nt][i], sc[1][nt][i + 2]));
+                        float v = fmaxf(sc[0][nt][i], sc[0][nt][i + 2]);
+#pragma unroll
+                        for (int mt = 1; mt < MTS; ++mt)
+                            v = fmaxf(v, fmaxf(sc[mt][nt][i], sc[mt][nt][i + 2]));
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
@@ -411,7 +449,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     }
                     float rs[2] = {0.f, 0.f};
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
+                    for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float pv = ex2_approx(sc[mt][nt][e] - muse[e & 1]);
@@ -428,7 +466,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                         o[mt][nt][3] *= alpha[1];
                     }
 #pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
+                    for (int kt = 0; kt < MTS; ++kt) {
                         pb[kt][nt][0] = movmatrix_trans(pack_bf16x2(sc[kt][nt][0], sc[kt][nt][1]));
                         pb[kt][nt][1] = movmatrix_trans(pack_bf16x2(sc[kt][nt][2], sc[kt][nt][3]));
                     }
@@ -438,11 +476,11 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
 #pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
+                    for (int kt = 0; kt < MTS; ++kt) {
                         const int tok = kt * 16 + v_tok;
                         const int col = mt * 16 + v_col;
-                        const uint32_t addr = vst + (uint32_t)((col >> 6) * (kStageTokens * 128) + tok * 128 +
-                                                               ((((col & 63) >> 3) ^ (tok & 7)) << 4));
+                        const uint32_t addr = vst + row_off(tok) + (uint32_t)((col >> 6) * (BR * 128) +
+                                                                            ((((col & 63) >> 3) ^ (tok & 7)) << 4));
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_t(addr, a0, a1, a2, a3);
 #pragma unroll
@@ -454,7 +492,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     fence_proxy_async_smem();   // generic zero-writes before the next TMA into this slot
             }
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0 && tag_ok)
                 mbar_arrive(empty_bar(c, slot, stages));
         }
 

@@ -17,12 +17,46 @@
 
 namespace shkv {
 
-// Tokens staged per pipeline slot: two 16-token pages or one 32-token page.
-constexpr int kStageTokens = 32;
-// Upper bound on pipeline slots per CTA.
-constexpr int kMaxStages = 8;
+// Tokens staged per pipeline slot (16 or 32).  A slot holds one or two
+// row-blocks of min(page_size, kStageTokens) tokens of one KV head.
+#ifndef SHKV_STAGE_TOKENS
+#define SHKV_STAGE_TOKENS 32
+#endif
+constexpr int kStageTokens = SHKV_STAGE_TOKENS;
+static_assert(kStageTokens == 16 || kStageTokens == 32, "stage is 16 or 32 tokens");
+// Upper bound on pipeline slots per CTA (the ring also stops at the
+// shared-memory limit).
+#ifndef SHKV_MAX_STAGES
+#define SHKV_MAX_STAGES 16
+#endif
+constexpr int kMaxStages = SHKV_MAX_STAGES;
+// Consumer warps per row group, by number of row groups (1..4).  Fewer warps
+// than ring slots keeps most of the ring in flight while warps compute.
+#ifndef SHKV_WT_NRG1
+#define SHKV_WT_NRG1 4
+#endif
+#ifndef SHKV_WT_NRG2
+#define SHKV_WT_NRG2 3
+#endif
+#ifndef SHKV_WT_NRG3
+#define SHKV_WT_NRG3 2
+#endif
+#ifndef SHKV_WT_NRG4
+#define SHKV_WT_NRG4 1
+#endif
+// Ring slots the producer arms and fills per iteration; each slot's copies
+// are issued by four lanes, so one TMA instruction carries up to
+// 4 * kStagesPerIssue copies.
+#ifndef SHKV_STAGES_PER_ISSUE
+#define SHKV_STAGES_PER_ISSUE 4
+#endif
+constexpr int kStagesPerIssue = SHKV_STAGES_PER_ISSUE;
+static_assert(kStagesPerIssue >= 1 && kStagesPerIssue <= 8, "stages per issue in [1, 8]");
+constexpr int kWtOfNrg[5] = {0, SHKV_WT_NRG1, SHKV_WT_NRG2, SHKV_WT_NRG3, SHKV_WT_NRG4};
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
 // Largest block (consumer warps + one producer warp).
-constexpr int kMaxThreads = 320;
+constexpr int kMaxThreads =
+    32 * (1 + cmax(cmax(SHKV_WT_NRG1, 2 * SHKV_WT_NRG2), cmax(3 * SHKV_WT_NRG3, 4 * SHKV_WT_NRG4)));
 // Wall-clock limit for any single wait on an mbarrier.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Dynamic shared memory a CTA may use on sm_100-family parts.
@@ -40,7 +74,7 @@ struct DecodeParams {
     float *ws_part;            // [2*C, R, D]
     int32_t batch, n_models, hq, hkv, group, rows;   // rows = R = N*G per KV head
     int32_t nrg, wt, rpad, stages;                   // row groups, token warps per group
-    int32_t page_size, pages_per_stage, max_pages, num_pages;
+    int32_t page_size, box_rows, max_pages, num_pages;
     int32_t num_ctas, pad0;
     int64_t total_chunks;
     float scale_log2;
@@ -182,14 +216,15 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
-// 2-D tiled TMA load global -> shared, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            uint32_t bar, uint64_t policy)
+// 3-D tiled TMA load global -> shared at box origin (0, y, 0), completing on
+// an mbarrier.
+__device__ __forceinline__ void tma_load_3d_row(uint32_t dst, const CUtensorMap *tm, int y, uint32_t bar,
+                                                uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(y), "r"(0), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -57,19 +57,24 @@ EncodeTiledFn encode_tiled_fn()
     return fn;
 }
 
-// 2-D view of a [num_pages, Hkv, P, D] bf16 pool: rows = num_pages*Hkv*P,
-// columns = D; a 64-column x P-row box with 128-byte swizzle is one page of
-// one head (split in two boxes when D = 128).
+// 3-D view of a [num_pages, Hkv, P, D] bf16 pool: dim0 = 64 columns
+// (128 bytes, the swizzle span), dim1 = rows (num_pages*Hkv*P, stride D*2
+// bytes), dim2 = D/64 column halves (stride 128 bytes).  One box
+// {64, min(P, kStageTokens), D/64} with 128-byte swizzle is a whole row-block
+// of one head's page -- 4 or 8 KiB in a single copy -- laid out in shared
+// memory as [half][row][64 columns].
 bool make_pool_map(CUtensorMap *tm, void *base, const shkv_pool_config &c)
 {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc)
         return false;
-    cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_pages * c.num_kv_heads * c.page_size};
-    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)c.page_size};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+    const int halves = c.head_dim / 64;
+    cuuint64_t dims[3] = {64u, (cuuint64_t)c.num_pages * c.num_kv_heads * c.page_size, (cuuint64_t)halves};
+    cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, 128u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)(c.page_size < kStageTokens ? c.page_size : kStageTokens),
+                         (cuuint32_t)halves};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -124,8 +129,7 @@ DecodeShape decode_shape(int rows)
     DecodeShape s;
     s.nt = rows <= 8 ? 1 : 2;
     s.nrg = s.nt == 1 ? 1 : (rows + 15) / 16;
-    static const int wt_of_nrg[5] = {0, 8, 4, 3, 2};
-    s.wt = wt_of_nrg[s.nrg];
+    s.wt = kWtOfNrg[s.nrg];
     s.rpad = s.nrg * 8 * s.nt;
     return s;
 }
@@ -325,7 +329,12 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     int stages = (int)((kSmemLimit - (int64_t)probe.total - 64) / (probe.stage_bytes + 20));
     if (stages > kMaxStages)
         stages = kMaxStages;
-    if (stages < 2)
+    // Consumer warp w of a row group takes stages k = w (mod wt), so with a
+    // ring of a multiple of wt slots the previous occupant of its next slot
+    // is its own, already consumed, stage: its parity wait can never see an
+    // older phase of the slot.
+    stages -= stages % sh.wt;
+    if (stages < 2 || stages < sh.wt)
         return SHKV_ERR_UNSUPPORTED;
     const DecodeSmem lay = decode_smem_layout(c.head_dim, 8 * sh.nt, nreg, ncw, sh.rpad, stages);
     if (lay.total > (uint32_t)kSmemLimit)
@@ -354,7 +363,7 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     p.rpad = sh.rpad;
     p.stages = stages;
     p.page_size = c.page_size;
-    p.pages_per_stage = kStageTokens / c.page_size;
+    p.box_rows = c.page_size < kStageTokens ? c.page_size : kStageTokens;
     p.max_pages = c.max_pages_per_seq;
     p.num_pages = c.num_pages;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);

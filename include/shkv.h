@@ -51,6 +51,7 @@ typedef enum {
 #define SHKV_ERRF_PAGE_OOB 0x1u   /* block-table entry outside [0, num_pages) */
 #define SHKV_ERRF_SEQ_LEN 0x2u    /* device seq_lens disagrees with the pool's host copy */
 #define SHKV_ERRF_TIMEOUT 0x4u    /* a pipeline wait exceeded its time limit */
+#define SHKV_ERRF_PIPELINE 0x8u   /* a pipeline slot held a stage other than the one expected */
 
 /* Largest batch a single decode / append call accepts. */
 #define SHKV_MAX_BATCH 1024
