@@ -11,7 +11,8 @@
 //
 // Work decomposition (flash-decoding with a balanced static split):
 //   The (request b, KV head g, page p) chunks, ordered request-major, are cut
-//   into num_ctas equal contiguous ranges; one persistent CTA per SM walks its
+//   into num_ctas contiguous ranges of equal cost (chunks plus a fixed cost
+//   per segment, planned on the host); one persistent CTA per SM walks its
 //   range as a sequence of segments (one segment per (b, g) it touches).  A
 //   (b, g) that straddles a cut is split: each piece writes a normalised
 //   partial and its log-sum-exp, and the last piece to finish (an atomic
@@ -79,15 +80,47 @@ __device__ __forceinline__ Segment locate(const DecodeParams &p, int64_t idx, in
     return s;
 }
 
-__device__ __forceinline__ int64_t cta_start(const DecodeParams &p, int c)
+// Successor of a segment that ended at its unit's end: the next (request,
+// head) unit, from its first page, clipped to the CTA's range end.
+__device__ __forceinline__ Segment next_segment(const DecodeParams &p, const Segment &prev, int64_t cta_end)
 {
-    return (int64_t)c * p.total_chunks / p.num_ctas;
+    Segment s;
+    s.g = prev.g + 1;
+    s.b = prev.b;
+    if (s.g == p.hkv) {
+        s.g = 0;
+        s.b = prev.b + 1;
+    }
+    s.pages_b = p.page_prefix[s.b + 1] - p.page_prefix[s.b];
+    s.unit_begin = prev.unit_end;
+    s.unit_end = s.unit_begin + s.pages_b;
+    s.seg_begin = s.unit_begin;
+    s.seg_end = s.unit_end < cta_end ? s.unit_end : cta_end;
+    s.p0 = 0;
+    s.p1 = (int)(s.seg_end - s.seg_begin);
+    return s;
 }
 
-// CTA whose range holds chunk idx.
+__device__ __forceinline__ int64_t cta_start(const DecodeParams &p, int c) { return p.cta_cut[c]; }
+
+// CTA whose range [cta_cut[c], cta_cut[c+1]) holds chunk idx.
 __device__ __forceinline__ int cta_of(const DecodeParams &p, int64_t idx)
 {
-    return (int)(((idx + 1) * p.num_ctas - 1) / p.total_chunks);
+    int lo = 0, hi = p.num_ctas;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cta_cut[mid] <= idx)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Cached length of request b, from the split plan (the host's copy).
+__device__ __forceinline__ int plan_len(const DecodeParams &p, const Segment &s)
+{
+    return (s.pages_b - 1) * p.page_size + (int)p.last_fill[s.b];
 }
 
 // Partial slot written by CTA c for its piece of the unit starting at
@@ -152,12 +185,23 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
     }
 
     bool alive = true;
-    int64_t idx = c.cta_begin;
     int kbase = 0, seg = 0;
     int last_issued_stage = -1;     // highest stage index with copies issued
     int q_issued[2] = {-1, -1};     // segment whose Q was last issued per buffer
-    while (idx < c.cta_end) {
-        const Segment s = locate(p, idx, c.cta_end);
+    Segment s = locate(p, c.cta_begin, c.cta_end);
+    // first block-table window of the current segment, prefetched one
+    // segment ahead
+    int pre = (lane < s.p1) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
+    for (;;) {
+        const bool has_next = s.seg_end < c.cta_end;
+        Segment sn;
+        int pre_next = -1;
+        if (has_next) {
+            sn = next_segment(p, s, c.cta_end);
+            pre_next = (lane < sn.p1) ? __ldg(p.block_table + (int64_t)sn.b * p.max_pages + lane) : -1;
+        }
+        // device copy of the length, checked at the end of the segment
+        const int dev_len = (lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
         // --- query rows of this (b, g): N bulk copies of G contiguous rows
         const int qb = seg & 1;
         if (alive) {
@@ -179,7 +223,7 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
         const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
         const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
         int w0 = s.p0;                                   // block-table window [w0, w0+32)
-        int cur = (w0 + lane < s.p1) ? __ldg(btrow + w0 + lane) : -1;
+        int cur = pre;
         int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
         // Lane 4*sub + 2*rb + kv copies row-block rb of K (kv = 0) or V
         // (kv = 1) for stage j + sub of this iteration.
@@ -234,9 +278,14 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
             }
             __syncwarp();
         }
+        if (lane == 0 && dev_len != plan_len(p, s))
+            atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
         kbase += nst;
-        idx = s.seg_end;
         ++seg;
+        if (!has_next)
+            break;
+        s = sn;
+        pre = pre_next;
     }
     // After an abort, wait (bounded) for every copy this CTA still has in
     // flight so no TMA write lands after the CTA exits.
@@ -289,10 +338,9 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
     const int v_col = ((lane >> 3) & 1) * 8;                  // V: column offset within 16
 
     bool alive = true;
-    int64_t idx = c.cta_begin;
     int kbase = 0, seg = 0;
-    while (idx < c.cta_end) {
-        const Segment s = locate(p, idx, c.cta_end);
+    Segment s = locate(p, c.cta_begin, c.cta_end);
+    for (;;) {
         const int tok_end = s.p1 * P;
         const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
         const int qb = seg & 1;
@@ -323,13 +371,8 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 mbar_arrive(qempty_bar(c, qb, stages));
         }
 
-        // --- cached length; the plan was built from the host copy
-        int L = __ldg(p.seq_lens + s.b);
-        if ((L + P - 1) / P != s.pages_b) {
-            if (lane == 0 && wtid == 0 && rg == 0)
-                atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
-            L = L < 0 ? 0 : (L > s.pages_b * P ? s.pages_b * P : L);
-        }
+        // --- cached length, from the plan (the producer checks the device copy)
+        const int L = plan_len(p, s);
         const int lim = L < tok_end ? L : tok_end;     // tokens of this segment that count
 
         float o[KSTEPS][NT][4];
@@ -525,47 +568,75 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     comb_o[((size_t)warp * NREG + (mt * NT + nt) * 4 + e) * 32 + lane] = o[mt][nt][e];
         named_barrier(1, (uint32_t)ncw * 32u);
 
-        // ... and combine them, each warp taking every wt-th register slot
+        // ... then combine them.  Each lane first derives, for the 2*NT rows
+        // its registers touch, the factor exp2(m_w - M) / L of every warp w
+        // of the group; every element is then one FMA per warp.
         const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
         const int slot_id = whole ? 0 : 2 * (int)blockIdx.x + (s.seg_begin == c.cta_begin ? 0 : 1);
         const int w_first = rg * p.wt;
-        for (int reg = wtid; reg < NREG; reg += p.wt) {
-            const int e = reg & 3;
-            const int nt = (reg >> 2) % NT;
-            const int mt = (reg >> 2) / NT;
-            const int rl = nt * 8 + 2 * (lane & 3) + (e & 1);
-            const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
-            float M = -INFINITY;
-            for (int w = 0; w < p.wt; ++w)
-                M = fmaxf(M, comb_m[(w_first + w) * ROWS_W + rl]);
-            float lsum = 0.f, acc = 0.f;
-            if (M != -INFINITY) {
-                for (int w = 0; w < p.wt; ++w) {
-                    const float f = ex2_approx(comb_m[(w_first + w) * ROWS_W + rl] - M);
-                    lsum += comb_l[(w_first + w) * ROWS_W + rl] * f;
-                    acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * f;
+        float fac[NT][2][kWtMax];
+        int64_t orow_r[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int rl = nt * 8 + 2 * (lane & 3) + i;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWtMax; ++w)
+                    if (w < p.wt)
+                        M = fmaxf(M, comb_m[(w_first + w) * ROWS_W + rl]);
+                float lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWtMax; ++w) {
+                    fac[nt][i][w] = 0.f;
+                    if (w < p.wt && M != -INFINITY) {
+                        fac[nt][i][w] = ex2_approx(comb_m[(w_first + w) * ROWS_W + rl] - M);
+                        lsum += comb_l[(w_first + w) * ROWS_W + rl] * fac[nt][i][w];
+                    }
+                }
+                const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+#pragma unroll
+                for (int w = 0; w < kWtMax; ++w)
+                    fac[nt][i][w] *= inv;
+                const int r = row0 + rl;
+                orow_r[nt][i] = whole ? (int64_t)s.b * p.n_models * p.hq + q_row(p, s.g, r < p.rows ? r : 0)
+                                      : (int64_t)slot_id * p.rows + r;
+                if (wtid == 0 && (lane >> 2) == 0 && r < p.rows) {     // one writer per row
+                    const float lse = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+                    if (whole) {
+                        if (p.lse_out)
+                            p.lse_out[orow_r[nt][i]] = lse;
+                    } else {
+                        p.ws_lse[orow_r[nt][i]] = lse;
+                    }
                 }
             }
-            const int r = row0 + rl;
-            if (r >= p.rows)
-                continue;
-            const float val = lsum > 0.f ? acc / lsum : 0.f;
-            const bool lse_writer = (mt == 0) && (e < 2) && ((lane >> 2) == 0);
-            const float lse = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-            if (whole) {
-                const int qr = q_row(p, s.g, r);
-                const int64_t orow = (int64_t)s.b * p.n_models * p.hq + qr;
-                p.out[orow * D + d] = __float2bfloat16_rn(val);
-                if (lse_writer && p.lse_out)
-                    p.lse_out[orow] = lse;
-            } else {
-                p.ws_part[((int64_t)slot_id * p.rows + r) * D + d] = val;
-                if (lse_writer)
-                    p.ws_lse[(int64_t)slot_id * p.rows + r] = lse;
-            }
-        }
-        if (!whole)
-            __threadfence();   // partials visible device-wide before the arrival count below
+        // element (mt, nt, e) is register reg = (mt*NT + nt)*4 + e; warp wtid
+        // of the group takes the registers with reg % wt == wtid
+        int wsel = 0;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int reg = (mt * NT + nt) * 4 + e;
+                    const int r = row0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+                    if (wsel == wtid && r < p.rows) {
+                        const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kWtMax; ++w)
+                            if (w < p.wt)
+                                acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * fac[nt][e & 1][w];
+                        if (whole)
+                            p.out[orow_r[nt][e & 1] * D + d] = __float2bfloat16_rn(acc);
+                        else
+                            p.ws_part[orow_r[nt][e & 1] * D + d] = acc;
+                    }
+                    wsel = (wsel + 1 == p.wt) ? 0 : wsel + 1;
+                }
         named_barrier(1, (uint32_t)ncw * 32u);
 
         // --- split unit: the last piece to arrive merges all pieces
@@ -574,48 +645,63 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
             const int c1 = cta_of(p, s.unit_end - 1);
             uint32_t *counter = p.ws_count + (int64_t)s.b * p.hkv + s.g;
             if (threadIdx.x == 0) {
-                __threadfence();
+                __threadfence();     // this CTA's partial (ordered by the barrier above) before the count
                 const uint32_t prev = atomicAdd(counter, 1u);
                 *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
             }
             named_barrier(1, (uint32_t)ncw * 32u);
             if (*c.bcast) {
                 __threadfence();
+                // one warp per stacked row: the split log-sum-exps, then the
+                // weighted sum of the split outputs, loads issued together
                 const int dq = D / 4;
-                for (int it = threadIdx.x; it < p.rows * dq; it += ncw * 32) {
-                    const int r = it / dq;
-                    const int d4 = it - r * dq;
+                for (int r = warp; r < p.rows; r += ncw) {
                     float M = -INFINITY;
-                    for (int cc = c0; cc <= c1; ++cc) {
-                        const int sl = piece_slot(p, cc, s.unit_begin);
-                        M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)sl * p.rows + r));
-                    }
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int cc = c0 + lane; cc <= c1; cc += 32)
+                        M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)piece_slot(p, cc, s.unit_begin) * p.rows + r));
+#pragma unroll
+                    for (int o_ = 16; o_ > 0; o_ >>= 1)
+                        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o_));
                     float wsum = 0.f;
+                    float4 acc[D / 128 > 0 ? D / 128 : 1];
+#pragma unroll
+                    for (int h = 0; h < (D / 128 > 0 ? D / 128 : 1); ++h)
+                        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (M != -INFINITY) {
                         for (int cc = c0; cc <= c1; ++cc) {
                             const int sl = piece_slot(p, cc, s.unit_begin);
-                            const float l = __ldcg(p.ws_lse + (int64_t)sl * p.rows + r);
-                            const float w = ex2_approx((l - M) * 1.4426950408889634f);
-                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                p.ws_part + ((int64_t)sl * p.rows + r) * D) + d4);
+                            const float w = ex2_approx((__ldcg(p.ws_lse + (int64_t)sl * p.rows + r) - M) *
+                                                       1.4426950408889634f);
                             wsum += w;
-                            acc.x += w * v.x;
-                            acc.y += w * v.y;
-                            acc.z += w * v.z;
-                            acc.w += w * v.w;
+                            const float4 *src = reinterpret_cast<const float4 *>(p.ws_part + ((int64_t)sl * p.rows + r) * D);
+#pragma unroll
+                            for (int h = 0; h < (D / 128 > 0 ? D / 128 : 1); ++h) {
+                                const int d4 = lane + 32 * h;
+                                if (d4 < dq) {
+                                    const float4 v = __ldcg(src + d4);
+                                    acc[h].x += w * v.x;
+                                    acc[h].y += w * v.y;
+                                    acc[h].z += w * v.z;
+                                    acc[h].w += w * v.w;
+                                }
+                            }
                         }
                     }
                     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-                    const int qr = q_row(p, s.g, r);
-                    const int64_t orow = (int64_t)s.b * p.n_models * p.hq + qr;
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-                    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-                    uint2 packed;
-                    packed.x = *reinterpret_cast<uint32_t *>(&lo);
-                    packed.y = *reinterpret_cast<uint32_t *>(&hi);
-                    *reinterpret_cast<uint2 *>(p.out + orow * D + d4 * 4) = packed;
-                    if (d4 == 0 && p.lse_out)
+                    const int64_t orow = (int64_t)s.b * p.n_models * p.hq + q_row(p, s.g, r);
+#pragma unroll
+                    for (int h = 0; h < (D / 128 > 0 ? D / 128 : 1); ++h) {
+                        const int d4 = lane + 32 * h;
+                        if (d4 < dq) {
+                            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
+                            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[h].z * inv, acc[h].w * inv);
+                            uint2 packed;
+                            packed.x = *reinterpret_cast<uint32_t *>(&lo);
+                            packed.y = *reinterpret_cast<uint32_t *>(&hi);
+                            *reinterpret_cast<uint2 *>(p.out + orow * D + d4 * 4) = packed;
+                        }
+                    }
+                    if (lane == 0 && p.lse_out)
                         p.lse_out[orow] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
                 }
                 if (threadIdx.x == 0)
@@ -625,8 +711,10 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
         }
 
         kbase += nst;
-        idx = s.seg_end;
         ++seg;
+        if (s.seg_end >= c.cta_end)
+            break;
+        s = next_segment(p, s, c.cta_end);
     }
 }
 
@@ -650,8 +738,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     c.lay = decode_smem_layout(D, 8 * NT, KSTEPS * NT * 4, ncw, p.rpad, p.stages);
     c.abort_flag = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.misc);
     c.bcast = reinterpret_cast<uint32_t *>(c.smem + c.lay.misc + 4);
-    c.cta_begin = cta_start(p, blockIdx.x);
-    c.cta_end = cta_start(p, blockIdx.x + 1);
+    c.cta_begin = p.cta_cut[blockIdx.x];
+    c.cta_end = p.cta_cut[blockIdx.x + 1];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {

@@ -32,8 +32,11 @@ static_assert(kStageTokens == 16 || kStageTokens == 32, "stage is 16 or 32 token
 constexpr int kMaxStages = SHKV_MAX_STAGES;
 // Consumer warps per row group, by number of row groups (1..4).  Fewer warps
 // than ring slots keeps most of the ring in flight while warps compute.
+#ifndef SHKV_WT_NT1
+#define SHKV_WT_NT1 4          // rows per warp = 8 (R <= 8)
+#endif
 #ifndef SHKV_WT_NRG1
-#define SHKV_WT_NRG1 4
+#define SHKV_WT_NRG1 3         // rows per warp = 16, one row group
 #endif
 #ifndef SHKV_WT_NRG2
 #define SHKV_WT_NRG2 3
@@ -56,7 +59,17 @@ constexpr int kWtOfNrg[5] = {0, SHKV_WT_NRG1, SHKV_WT_NRG2, SHKV_WT_NRG3, SHKV_W
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 // Largest block (consumer warps + one producer warp).
 constexpr int kMaxThreads =
-    32 * (1 + cmax(cmax(SHKV_WT_NRG1, 2 * SHKV_WT_NRG2), cmax(3 * SHKV_WT_NRG3, 4 * SHKV_WT_NRG4)));
+    32 * (1 + cmax(cmax(cmax(SHKV_WT_NT1, SHKV_WT_NRG1), 2 * SHKV_WT_NRG2), cmax(3 * SHKV_WT_NRG3, 4 * SHKV_WT_NRG4)));
+// Largest number of consumer warps in one row group.
+constexpr int kWtMax = cmax(cmax(SHKV_WT_NT1, SHKV_WT_NRG1), cmax(cmax(SHKV_WT_NRG2, SHKV_WT_NRG3), SHKV_WT_NRG4));
+// Upper bound on persistent CTAs (one per SM).
+constexpr int kMaxCtas = 256;
+// Fixed cost of one (request, head) segment in the split plan, in page
+// chunks: a CTA that crosses many short requests gets fewer chunks.
+#ifndef SHKV_SEGMENT_COST_CHUNKS
+#define SHKV_SEGMENT_COST_CHUNKS 32
+#endif
+constexpr int kSegmentCostChunks = SHKV_SEGMENT_COST_CHUNKS;
 // Wall-clock limit for any single wait on an mbarrier.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Dynamic shared memory a CTA may use on sm_100-family parts.
@@ -79,7 +92,9 @@ struct DecodeParams {
     int64_t total_chunks;
     float scale_log2;
     float pad1;
-    int32_t page_prefix[SHKV_MAX_BATCH + 1];
+    int32_t cta_cut[kMaxCtas + 1];             // first chunk of each CTA; [num_ctas] = total
+    int32_t page_prefix[SHKV_MAX_BATCH + 1];   // pages before each request
+    uint8_t last_fill[SHKV_MAX_BATCH];         // tokens in each request's last page (1..P)
 };
 
 struct AppendParams {

@@ -82,31 +82,90 @@ bool make_pool_map(CUtensorMap *tm, void *base, const shkv_pool_config &c)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Page prefix over requests and the CTA count; shared by the plan query and
-// the decode launch so both describe the same split.
+// The split plan, shared by the plan query and the decode launch so both
+// describe the same work division.  Chunks are (request, head, page) triples
+// in request-major order; W = Hkv * sum_b ceil(L_b / P).  Each (request,
+// head) unit costs its pages plus kSegmentCostChunks (the fixed work of
+// starting and finishing a segment), and the weighted sequence is cut into
+// `num_ctas` equal parts.  Cuts are then made strictly increasing so every
+// CTA owns at least one chunk.
+//   prefix     [batch + 1] pages before each request
+//   last_fill  [batch] tokens in each request's last page (nullable)
+//   cuts       [num_ctas + 1] first chunk of each CTA, cuts[num_ctas] = W
 shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv, int32_t max_ctas,
-                       int32_t *prefix, int64_t *total_chunks, int32_t *num_ctas)
+                       int32_t *prefix, uint8_t *last_fill, int32_t *cuts, int64_t *total_chunks,
+                       int32_t *num_ctas)
 {
-    if (batch < 1 || batch > SHKV_MAX_BATCH || !lens || page_size <= 0 || hkv <= 0 || max_ctas <= 0)
+    if (batch < 1 || batch > SHKV_MAX_BATCH || !lens || page_size <= 0 || page_size > 255 || hkv <= 0 ||
+        max_ctas <= 0)
         return SHKV_ERR_INVALID_ARG;
     prefix[0] = 0;
     for (int b = 0; b < batch; ++b) {
         if (lens[b] < 1)
             return SHKV_ERR_INVALID_ARG;
-        int64_t next = (int64_t)prefix[b] + ceil_div(lens[b], page_size);
-        if (next > INT32_MAX)
+        const int64_t pages = ceil_div(lens[b], page_size);
+        const int64_t next = (int64_t)prefix[b] + pages;
+        if (next * hkv > INT32_MAX)
             return SHKV_ERR_UNSUPPORTED;
         prefix[b + 1] = (int32_t)next;
+        if (last_fill)
+            last_fill[b] = (uint8_t)(lens[b] - (pages - 1) * page_size);
     }
     const int64_t W = (int64_t)hkv * prefix[batch];
     int64_t C = ceil_div(W, kMinChunksPerCta);
     if (C > max_ctas)
         C = max_ctas;
+    if (C > kMaxCtas)
+        C = kMaxCtas;
     if (C < 1)
         C = 1;
+
+    const int64_t alpha = kSegmentCostChunks;
+    const int64_t T = W + alpha * (int64_t)batch * hkv;
+    int64_t c = 1, cw = 0, cb = 0;   // next cut, weight and chunks before the current unit
+    for (int b = 0; b < batch && c < C; ++b) {
+        const int64_t pg = prefix[b + 1] - prefix[b];
+        for (int g = 0; g < hkv && c < C; ++g) {
+            const int64_t wu = pg + alpha;
+            while (c < C) {
+                const int64_t target = c * T / C;
+                if (target >= cw + wu)
+                    break;
+                const int64_t o = target - cw - alpha;
+                cuts[c] = (int32_t)(cb + (o > 0 ? o : 0));
+                ++c;
+            }
+            cw += wu;
+            cb += pg;
+        }
+    }
+    for (; c < C; ++c)
+        cuts[c] = (int32_t)W;
+    cuts[0] = 0;
+    cuts[C] = (int32_t)W;
+    for (int64_t i = 1; i < C; ++i)
+        if (cuts[i] <= cuts[i - 1])
+            cuts[i] = cuts[i - 1] + 1;
+    for (int64_t i = C - 1; i >= 1; --i)
+        if (cuts[i] >= cuts[i + 1])
+            cuts[i] = cuts[i + 1] - 1;
     *total_chunks = W;
     *num_ctas = (int32_t)C;
     return SHKV_OK;
+}
+
+// CTA whose range [cuts[c], cuts[c+1]) holds chunk idx.
+int32_t cta_of_host(const int32_t *cuts, int32_t C, int64_t idx)
+{
+    int32_t lo = 0, hi = C;
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) / 2;
+        if (cuts[mid] <= idx)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
 }
 
 size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms)
@@ -129,7 +188,7 @@ DecodeShape decode_shape(int rows)
     DecodeShape s;
     s.nt = rows <= 8 ? 1 : 2;
     s.nrg = s.nt == 1 ? 1 : (rows + 15) / 16;
-    s.wt = kWtOfNrg[s.nrg];
+    s.wt = s.nt == 1 ? SHKV_WT_NT1 : kWtOfNrg[s.nrg];
     s.rpad = s.nrg * 8 * s.nt;
     return s;
 }
@@ -319,7 +378,7 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     DecodeParams p;
     memset(&p, 0, sizeof p);
     shkv_status st = build_plan(batch, pool->lens.data(), c.page_size, c.num_kv_heads, pool->num_sms,
-                                p.page_prefix, &p.total_chunks, &p.num_ctas);
+                                p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas);
     if (st != SHKV_OK)
         return st;
     const DecodeShape sh = decode_shape(rows);
@@ -406,23 +465,24 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
     if (!num_ctas)
         return SHKV_ERR_INVALID_ARG;
     std::vector<int32_t> prefix((size_t)SHKV_MAX_BATCH + 1);
+    std::vector<int32_t> cuts((size_t)kMaxCtas + 1);
     int64_t W = 0;
     int32_t C = 0;
-    shkv_status st = build_plan(batch, seq_lens, page_size, num_kv_heads, max_ctas, prefix.data(), &W, &C);
+    shkv_status st = build_plan(batch, seq_lens, page_size, num_kv_heads, max_ctas, prefix.data(), nullptr,
+                                cuts.data(), &W, &C);
     if (st != SHKV_OK)
         return st;
     *num_ctas = C;
     if (cta_begin)
         for (int c = 0; c <= C; ++c)
-            cta_begin[c] = (int64_t)c * W / C;
+            cta_begin[c] = cuts[c];
     if (num_splits) {
         int32_t n = 0;
         for (int b = 0; b < batch; ++b) {
             const int64_t pages = prefix[b + 1] - prefix[b];
             for (int g = 0; g < num_kv_heads; ++g) {
                 const int64_t u0 = (int64_t)num_kv_heads * prefix[b] + g * pages;
-                const int64_t u1 = u0 + pages - 1;
-                if (((u0 + 1) * C - 1) / W != ((u1 + 1) * C - 1) / W)
+                if (cta_of_host(cuts.data(), C, u0) != cta_of_host(cuts.data(), C, u0 + pages - 1))
                     ++n;
             }
         }

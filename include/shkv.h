@@ -196,9 +196,10 @@ shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags);
 /*
  * Host-only view of how shkv_decode_attention divides work (no device
  * needed).  The (request, KV head, page) chunks, ordered request-major, are
- * cut into `num_ctas` contiguous ranges of equal size (+-1 chunk), one per
- * persistent CTA; a (request, head) whose pages straddle a cut is split and
- * merged by log-sum-exp.
+ * cut into `num_ctas` contiguous, non-empty ranges, one per persistent CTA,
+ * of equal cost where a range costs its chunks plus a fixed amount per
+ * (request, head) it touches; a (request, head) whose pages straddle a cut
+ * is split and merged by log-sum-exp.
  *   seq_lens    host int32 [batch] (each >= 1)
  *   max_ctas    upper bound on CTAs (normally the SM count)
  *   cta_begin   host int64 [max_ctas + 1] or NULL; receives the first chunk

@@ -50,31 +50,42 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.shkv_splitkv_merge(1, 1, 1, 6, 16, 16, 16, None, None) == N.SHKV_ERR_INVALID_ARG  # D % 4
 
 
+SEGMENT_COST = 32  # chunks charged per (request, head) segment by the planner
+
+
 @pytest.mark.parametrize("lens,P,H,C", [
     ([256], 16, 2, 152),                       # tiny
     ([1, 2, 3, 4000, 17], 16, 8, 152),
     ([131584] * 4, 16, 8, 152),                # long context: every unit split
     (list(range(1, 300)), 32, 8, 152),
     ([5], 16, 1, 152),                         # fewer chunks than CTAs
+    ([512] * 40 + [32768] * 3, 16, 8, 152),    # many short requests next to long ones
 ])
-def test_plan_is_balanced_and_covers_every_chunk(lib, lens, P, H, C):
+def test_plan_covers_every_chunk_with_balanced_cost(lib, lens, P, H, C):
     begin, nc, ns = N.shkv_plan_decode(lens, P, H, C)
     pages = [(l + P - 1) // P for l in lens]
     W = H * sum(pages)
     assert begin[0] == 0 and begin[-1] == W
     sizes = np.diff(begin)
-    assert (sizes >= 1).all() and sizes.max() - sizes.min() <= 1
+    assert (sizes >= 1).all()                                   # every CTA owns work
     assert nc <= C and nc == min(C, max(1, -(-W // 8)))
-    # brute-force count of (request, head) units that straddle a cut
-    cuts = set(begin[1:-1].tolist())
-    n = 0
+    # brute force: segments per CTA and units straddling a cut
+    units = []
     off = 0
-    for p in pages:
+    for p_ in pages:
         for _ in range(H):
-            n += any(off < c < off + p for c in cuts)
-            off += p
-    assert ns == n
-    assert ns <= nc - 1
+            units.append((off, off + p_))
+            off += p_
+    cuts = begin.tolist()
+    n_split = sum(1 for u0, u1 in units if any(u0 < c < u1 for c in cuts[1:-1]))
+    assert ns == n_split and ns <= nc - 1
+    cost = []
+    for c in range(nc):
+        a, b = cuts[c], cuts[c + 1]
+        segs = sum(1 for u0, u1 in units if u0 < b and u1 > a)
+        cost.append((b - a) + SEGMENT_COST * segs)
+    target = (W + SEGMENT_COST * len(units)) / nc
+    assert max(cost) <= target + 3 * SEGMENT_COST + 2, (max(cost), target)
 
 
 def test_plan_rejects_empty_requests_and_oversized_batches(lib):
