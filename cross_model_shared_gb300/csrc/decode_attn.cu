@@ -501,12 +501,15 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                         }
                     lrow[nt][0] = lrow[nt][0] * alpha[0] + rs[0];
                     lrow[nt][1] = lrow[nt][1] * alpha[1] + rs[1];
+                    // rescale O only if some row's running max moved
+                    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-                    for (int mt = 0; mt < KSTEPS; ++mt) {
-                        o[mt][nt][0] *= alpha[0];
-                        o[mt][nt][1] *= alpha[1];
-                        o[mt][nt][2] *= alpha[0];
-                        o[mt][nt][3] *= alpha[1];
+                        for (int mt = 0; mt < KSTEPS; ++mt) {
+                            o[mt][nt][0] *= alpha[0];
+                            o[mt][nt][1] *= alpha[1];
+                            o[mt][nt][2] *= alpha[0];
+                            o[mt][nt][3] *= alpha[1];
+                        }
                     }
 #pragma unroll
                     for (int kt = 0; kt < MTS; ++kt) {
@@ -721,7 +724,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 }  // namespace
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
     shkv_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ DecodeParams p)
 {

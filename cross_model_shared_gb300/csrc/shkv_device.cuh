@@ -56,12 +56,24 @@ constexpr int kMaxStages = SHKV_MAX_STAGES;
 constexpr int kStagesPerIssue = SHKV_STAGES_PER_ISSUE;
 static_assert(kStagesPerIssue >= 1 && kStagesPerIssue <= 8, "stages per issue in [1, 8]");
 constexpr int kWtOfNrg[5] = {0, SHKV_WT_NRG1, SHKV_WT_NRG2, SHKV_WT_NRG3, SHKV_WT_NRG4};
+// More than 16 stacked rows: use 8-row groups (no padding of R to 16) when
+// set, else 16-row groups.  8-row groups take up to kNt1MultiWarps consumer
+// warps in total.
+#ifndef SHKV_R_ABOVE16_NT1
+#define SHKV_R_ABOVE16_NT1 1
+#endif
+#ifndef SHKV_NT1_MULTI_WARPS
+#define SHKV_NT1_MULTI_WARPS 10
+#endif
+constexpr int kNt1MultiWarps = SHKV_NT1_MULTI_WARPS;
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-// Largest block (consumer warps + one producer warp).
-constexpr int kMaxThreads =
-    32 * (1 + cmax(cmax(cmax(SHKV_WT_NT1, SHKV_WT_NRG1), 2 * SHKV_WT_NRG2), cmax(3 * SHKV_WT_NRG3, 4 * SHKV_WT_NRG4)));
+// Largest blocks (consumer warps + one producer warp), per rows per warp.
+constexpr int kMaxThreadsNT1 = 32 * (1 + cmax(SHKV_WT_NT1, kNt1MultiWarps));
+constexpr int kMaxThreadsNT2 =
+    32 * (1 + cmax(cmax(SHKV_WT_NRG1, 2 * SHKV_WT_NRG2), cmax(3 * SHKV_WT_NRG3, 4 * SHKV_WT_NRG4)));
 // Largest number of consumer warps in one row group.
-constexpr int kWtMax = cmax(cmax(SHKV_WT_NT1, SHKV_WT_NRG1), cmax(cmax(SHKV_WT_NRG2, SHKV_WT_NRG3), SHKV_WT_NRG4));
+constexpr int kWtMax = cmax(cmax(cmax(SHKV_WT_NT1, kNt1MultiWarps / 2), SHKV_WT_NRG1),
+                            cmax(cmax(SHKV_WT_NRG2, SHKV_WT_NRG3), SHKV_WT_NRG4));
 // Upper bound on persistent CTAs (one per SM).
 constexpr int kMaxCtas = 256;
 // Fixed cost of one (request, head) segment in the split plan, in page

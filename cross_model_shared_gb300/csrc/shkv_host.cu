@@ -186,9 +186,21 @@ struct DecodeShape {
 DecodeShape decode_shape(int rows)
 {
     DecodeShape s;
-    s.nt = rows <= 8 ? 1 : 2;
-    s.nrg = s.nt == 1 ? 1 : (rows + 15) / 16;
-    s.wt = s.nt == 1 ? SHKV_WT_NT1 : kWtOfNrg[s.nrg];
+    if (rows <= 8) {
+        s.nt = 1;
+        s.nrg = 1;
+        s.wt = SHKV_WT_NT1;
+    } else if (rows <= 16 || !SHKV_R_ABOVE16_NT1) {
+        s.nt = 2;
+        s.nrg = (rows + 15) / 16;
+        s.wt = kWtOfNrg[s.nrg];
+    } else {
+        s.nt = 1;
+        s.nrg = (rows + 7) / 8;
+        s.wt = kNt1MultiWarps / s.nrg > 0 ? kNt1MultiWarps / s.nrg : 1;
+        if (s.wt > kWtMax)
+            s.wt = kWtMax;
+    }
     s.rpad = s.nrg * 8 * s.nt;
     return s;
 }
