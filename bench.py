@@ -49,10 +49,20 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="llama8b", choices=W.CONFIG_ORDER)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first B requests of the workload (reduced case for profiling)")
     ap.add_argument("--impl", default="shkv", choices=["shkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     return ap.parse_args()
+
+
+def load_workload(args) -> W.Workload:
+    wl = W.make_workload(args.config)
+    if args.batch and args.batch < wl.B:
+        wl = W.custom_workload(f"{wl.name}[:{args.batch}]", B=args.batch, N=wl.N, Hq=wl.Hq, Hkv=wl.Hkv, D=wl.D,
+                               P=wl.P, lens_prefill=wl.lens_prefill[:args.batch], n_append=wl.n_append, seed=wl.seed)
+    return wl
 
 
 def dist_env():
@@ -173,12 +183,18 @@ def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float):
     description)."""
     import oracle
     order = np.argsort(wl.lens_final, kind="stable")
-    picks = [int(order[len(order) // 2])]
     kv_bytes, elapsed, done = 0, 0.0, []
+    cache = {}
     i = 0
-    while elapsed < budget_s and i < wl.B:
-        b = picks[0] if i == 0 else int(order[(len(order) // 2 + i) % len(order)])
-        kb, vb, npg = fetch_pages(b)
+    # whole requests, starting at the median length and cycling through the
+    # batch, until the time budget is spent
+    while elapsed < budget_s and i < 64 * wl.B:
+        b = int(order[(len(order) // 2 + i) % len(order)])
+        if b not in cache:
+            cache[b] = fetch_pages(b)
+            if len(cache) > 8:
+                cache.pop(next(iter(cache)))
+        kb, vb, npg = cache[b]
         bt = np.arange(npg, dtype=np.int32)[None, :]
         t0 = time.perf_counter()
         oracle.decode_attention(q_bits[b:b + 1], kb, vb, bt, np.array([wl.lens_final[b]], np.int32),
@@ -187,8 +203,8 @@ def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float):
         kv_bytes += npg * wl.P * wl.Hkv * wl.D * 4
         done.append(b)
         i += 1
-    desc = (f"{len(done)} whole requests of {wl.name} (all {wl.rows} stacked rows, full context, "
-            f"{sum(int(wl.lens_final[b]) for b in done)} tokens), fp64, {oracle.num_threads()} threads")
+    desc = (f"{len(done)} whole requests of {wl.name} ({len(set(done))} distinct; all {wl.rows} stacked rows, "
+            f"full context, {sum(int(wl.lens_final[b]) for b in done)} tokens), fp64, {oracle.num_threads()} threads")
     return kv_bytes / elapsed / 1e9, oracle.num_threads(), desc, elapsed
 
 
@@ -198,7 +214,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    wl = W.make_workload(args.config)
+    wl = load_workload(args)
     q = W.gen_q(wl)
     rng = np.random.default_rng(wl.seed + 77)
     R = wl.R
@@ -256,7 +272,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    wl = W.make_workload(args.config)
+    wl = load_workload(args)
     q_bits = W.gen_q(wl)
     k_dev, v_dev = W.gen_pool_device(wl, device=dev)
     pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
