@@ -108,6 +108,23 @@ def profiled_traffic(config: str):
         return None
 
 
+def max_over_ranks(value: float, world_size: int, device) -> float:
+    """Largest value over all ranks (the slowest rank's time sets the job's
+    time); identity on one rank."""
+    if world_size == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(bytes_per_step: int, steps: int, world_size: int, seconds: float) -> float:
+    """Whole-job GB/s: every rank processes its own replica of the step."""
+    return world_size * bytes_per_step * steps / seconds / 1e9
+
+
 def step_bytes(wl: W.Workload) -> int:
     """Algorithmic bytes of one step: unique KV pages + Q read + O written."""
     qo = 2 * wl.B * wl.rows * wl.D * 2
@@ -323,18 +340,14 @@ def run_gpu(args):
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     flags = pool.check_errors()
     if flags:
         raise RuntimeError(f"device error bits 0x{flags:x} in the timed region")
 
     ms_per_step = ms / args.steps
     nbytes = step_bytes(wl)
-    value = ws * nbytes * args.steps / (ms * 1e-3) / 1e9
+    value = job_throughput_gbs(nbytes, args.steps, ws, ms * 1e-3)
     per_gpu = nbytes / (ms_per_step * 1e-3) / 1e9
 
     # --- the same kernel once per decoder, without sharing (N launches/step)
@@ -373,12 +386,8 @@ def run_gpu(args):
     for _ in range(e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = ws * nbytes * e_steps / e2e_s / 1e9
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
+    e2e_value = job_throughput_gbs(nbytes, e_steps, ws, e2e_s)
     qbytes = q.numel() * 2
 
     cpu = None
