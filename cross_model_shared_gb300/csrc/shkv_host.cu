@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -16,6 +17,9 @@
 namespace shkv {
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const DecodeParams &p, uint32_t smem, cudaStream_t stream);
+cudaError_t launch_decode_umma(int D, const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+                               uint32_t smem, cudaStream_t stream);
+uint32_t umma_smem_bytes(int D, int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
                          const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream);
@@ -203,6 +207,18 @@ DecodeShape decode_shape(int rows)
     }
     s.rpad = s.nrg * 8 * s.nt;
     return s;
+}
+
+// Which consumer runs for R stacked rows: the automatic policy, or the one
+// named by SHKV_DECODE_CONSUMER ("mma" or "umma"; read on every call).
+bool use_umma_consumer(int rows)
+{
+    const char *env = getenv("SHKV_DECODE_CONSUMER");
+    if (env && strcmp(env, "umma") == 0)
+        return rows <= kUmmaMaxRows;
+    if (env && strcmp(env, "mma") == 0)
+        return false;
+    return rows >= kUmmaMinRows && rows <= kUmmaMaxRows;
 }
 
 }  // namespace
@@ -393,6 +409,7 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                                 p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas);
     if (st != SHKV_OK)
         return st;
+    const bool use_umma = use_umma_consumer(rows);
     const DecodeShape sh = decode_shape(rows);
     const int ncw = sh.nrg * sh.wt;
     const int nreg = (c.head_dim / 16) * sh.nt * 4;
@@ -405,11 +422,23 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     // is its own, already consumed, stage: its parity wait can never see an
     // older phase of the slot.
     stages -= stages % sh.wt;
-    if (stages < 2 || stages < sh.wt)
-        return SHKV_ERR_UNSUPPORTED;
-    const DecodeSmem lay = decode_smem_layout(c.head_dim, 8 * sh.nt, nreg, ncw, sh.rpad, stages);
-    if (lay.total > (uint32_t)kSmemLimit)
-        return SHKV_ERR_UNSUPPORTED;
+    uint32_t smem_bytes = 0;
+    if (use_umma) {
+        // one consumer (the MMA issuer) takes every stage in order: any ring size
+        stages = kMaxStages;
+        while (stages >= 2 && umma_smem_bytes(c.head_dim, rows, stages) > (uint32_t)kSmemLimit)
+            --stages;
+        if (stages < 2)
+            return SHKV_ERR_UNSUPPORTED;
+        smem_bytes = umma_smem_bytes(c.head_dim, rows, stages);
+    } else {
+        if (stages < 2 || stages < sh.wt)
+            return SHKV_ERR_UNSUPPORTED;
+        const DecodeSmem lay = decode_smem_layout(c.head_dim, 8 * sh.nt, nreg, ncw, sh.rpad, stages);
+        if (lay.total > (uint32_t)kSmemLimit)
+            return SHKV_ERR_UNSUPPORTED;
+        smem_bytes = lay.total;
+    }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const size_t count_bytes = align_up((uint32_t)(batch * c.num_kv_heads * 4), 256);
@@ -438,7 +467,9 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     p.max_pages = c.max_pages_per_seq;
     p.num_pages = c.num_pages;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    cudaError_t e = launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, lay.total, (cudaStream_t)stream);
+    cudaError_t e = use_umma ? launch_decode_umma(c.head_dim, pool->tm_k, pool->tm_v, p, smem_bytes, (cudaStream_t)stream)
+                             : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
+                                             (cudaStream_t)stream);
     return cuda_status(e);
 }
 

@@ -156,6 +156,10 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
  *            completes without device error bits leaves it zero-filled again,
  *            so it can be reused.  Calls sharing one workspace must not
  *            overlap on the GPU.
+ * Two interchangeable consumers implement the same result: warp-level
+ * mma.sync tiles (the default) and tcgen05 tensor-memory tiles; setting the
+ * environment variable SHKV_DECODE_CONSUMER to "mma" or "umma" selects one
+ * (read on every call).
  * Supported: batch in [1, SHKV_MAX_BATCH], every L_b >= 1,
  * hq_per_model % num_kv_heads == 0, rows per KV head
  * n_models * hq_per_model / num_kv_heads <= 64.
