@@ -32,7 +32,11 @@ EXPORTS = [
     "shkv_pool_create", "shkv_pool_destroy", "shkv_pool_set_seq_lens", "shkv_pool_get_seq_lens",
     "shkv_append_kv", "shkv_decode_workspace_size", "shkv_decode_attention", "shkv_splitkv_merge",
     "shkv_check_errors", "shkv_plan_decode", "shkv_status_string", "shkv_decode_attention_noalloc",
+    "shkv_decode_consumer",
 ]
+
+SHKV_CONSUMER_MMA_SYNC = 0
+SHKV_CONSUMER_TCGEN05 = 1
 
 SHKV_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -85,6 +89,7 @@ def load() -> ctypes.CDLL:
         "shkv_check_errors": [vp, vp, u32p],
         "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
+        "shkv_decode_consumer": [vp, i32, i32, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -174,3 +179,11 @@ def shkv_decode_attention_noalloc(pool: int, batch: int, n_models: int, hq: int,
     argument, no allocation)."""
     _check(load().shkv_decode_attention_noalloc(pool, batch, n_models, hq, q, scale, out, lse_out, stream),
            "shkv_decode_attention_noalloc")
+
+
+def shkv_decode_consumer(pool: int, n_models: int, hq: int) -> int:
+    """SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05: the consumer a decode
+    call with this shape would run now."""
+    out = ctypes.c_int32()
+    _check(load().shkv_decode_consumer(pool, n_models, hq, ctypes.byref(out)), "shkv_decode_consumer")
+    return out.value

@@ -160,7 +160,7 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
     Segment s = locate(p, c.cta_begin, c.cta_end);
     // first block-table window of the current segment, prefetched one
     // segment ahead
-    int pre = (lane < s.p1) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
+    int pre = (lane < s.p1 - s.p0) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
     for (;;) {
         const bool has_next = s.seg_end < c.cta_end;
         Segment sn;

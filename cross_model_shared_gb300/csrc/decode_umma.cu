@@ -1,26 +1,40 @@
 // decode_umma.cu -- shared-KV decode attention on the 5th-generation tensor
-// cores (tcgen05 / TMEM), for many stacked rows per KV head.
+// cores (tcgen05 / TMEM) for many stacked query rows per KV head (D = 128).
 //
 // Same method and work split as decode_attn.cu (ICaRus key design 3 over the
-// PrefillShare paged cache; persistent CTAs over cost-balanced chunk
-// ranges; split units merged by the last arriving CTA), with the consumer
-// side rebuilt around tcgen05.mma:
+// PrefillShare paged cache: the N decoders' query rows of one KV head are
+// stacked and share every K/V page load; persistent CTAs over cost-balanced
+// chunk ranges; split units merged by the last arriving CTA).  Here tokens
+// run along the MMA's M dimension.  A pipeline stage is 128 tokens of one
+// (request, KV head), and per stage
 //
-//   warp 3  producer: TMA of K/V row-blocks into the mbarrier ring and bulk
-//           copies of each segment's query rows (shared with decode_attn.cu);
-//   warp 2  MMA issuer (one lane): S = Q K^T into a double-buffered TMEM
-//           tile (M = 128 query-row lanes, N = the stage's tokens), one stage
-//           ahead of O += P V (V read MN-major straight from the ring slot);
-//   warps 0-1 softmax: one thread per stacked row (TMEM lanes 0..63).  Each
-//           reads its row of S from TMEM, masks, keeps a base-2 running max
-//           and sum, writes its row of P (bf16) to a swizzled shared tile, and
-//           at the end of a segment reads its row of O from TMEM.  The running
-//           max is refreshed lazily: O (in TMEM) is rescaled only when a tile
-//           raises a row's max by more than 2^8, so P stays below 256.
+//   S^T[t, r]  = sum_d K[t, d] Q[r, d]        M = 128 tokens,  N = rows
+//   O^T[d, r] += sum_t V[t, d] P^T[t, r]      M = 128 = D,     N = rows
+//   L[., r]   += sum_t 1 * P^T[t, r]          (a ones operand: row sums)
+//   Llo[., r] += sum_t 1 * P_lo^T[t, r]
 //
-// Because every row lives in exactly one thread, there is no cross-warp
-// combine at a segment end.  Rows R..127 of the MMA tiles are padding: they
-// read whatever the shared memory holds and their results are never used.
+// so a TMEM lane is one token of S^T, or one head-dim column of O^T, and
+// every lane of L holds all R row sums.  P is rounded to bf16 for the MMAs
+// and O is normalised by the sums of those same rounded weights (so a row
+// dominated by one token returns that token's V unchanged); P_lo = p -
+// bf16(p) (also bf16) adds the rounding residue for the log-sum-exp, which
+// is then accurate to fp32 rather than to the bf16 rounding of P.
+// Roles (192 threads):
+//
+//   warps 0-3  softmax: thread t owns token t of the stage and all R of its
+//              scores; it writes its rows of P^T and P_lo^T (bf16) over the
+//              stage's two K halves, which the QK MMA no longer needs.  At a
+//              segment end thread d reads column d of O^T and the row sums.
+//   warp 4     MMA issuer (one lane): QK of stage k, then PV of stage k-1.
+//   warp 5     producer: TMA of each page's K and V halves (one copy per
+//              lane) into a ring of 64 KiB stages, and bulk copies of the
+//              query rows of the next segment.
+//
+// The running max m[r] is shared by all 128 tokens of a stage (O^T column r
+// collects all of them), and it is refreshed lazily: every stage the four
+// warps vote, in one bar.red, whether any score exceeds m[r] + kRescaleLog2.
+// Only then do they reduce the stage max across the CTA, rescale O^T and L
+// in TMEM and move m.  Unscaled exponentials stay below 2^kRescaleLog2.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,89 +49,232 @@ namespace {
 
 using namespace detail;
 
-static_assert(kStageTokens == 32, "the tcgen05 consumer reads 32 tokens of S per stage");
+constexpr int kTT = 128;                    // tokens per stage (the MMA's M)
+constexpr int kD = 128;                     // head dim (O^T's M)
+constexpr int kHalves = kD / 64;            // 128-byte swizzle spans per row
+constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kMmaWarp = 4;
+constexpr int kProducerWarp = 5;
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;               // S^T buffers at columns 0 and 64
+constexpr uint32_t kColO = 128;             // O^T
+constexpr uint32_t kColL = 192;             // row sums of the bf16 weights
+constexpr uint32_t kColLlo = 256;           // row sums of their rounding residues
+constexpr float kRescaleLog2 = 10.f;
+constexpr uint32_t kOnesBytes = 4096;       // 128 x 16 bf16 ones, no swizzle
+constexpr int kTcMaxStages = 4;
 
-constexpr int kUmmaThreads = 128;
-constexpr int kSoftmaxWarps = 2;            // TMEM lanes 0..63: up to 64 stacked rows
-constexpr int kMmaWarp = 2;
-constexpr int kProducerWarp = 3;
-constexpr uint32_t kTmemCols = 256;         // S[2] (2 x 32 columns) + O (up to 128 columns)
-constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 64;
-constexpr float kRescaleLog2 = 8.f;
-constexpr float kLn2u = 0.6931471805599453f;
+static_assert(kTT == kSoftmaxThreads, "one softmax thread per token of a stage");
+static_assert(kD == kSoftmaxThreads, "one softmax thread per column of O^T");
 
-// extra barriers: s_full[2], s_free[2], p_full[2], p_free[2], q_ready, q_tile_free, fin
-constexpr int kNumXbars = 11;
+// Padded row count N of the MMAs for R stacked rows.
+__host__ __device__ constexpr int tc_nr(int rows) { return (rows + 15) / 16 * 16; }
+// N of the PV MMAs: 48 is rounded up to a whole 64-column swizzle span.
+__host__ __device__ constexpr int tc_npv(int nr) { return nr == 48 ? 64 : nr; }
 
-struct UmmaSmem {
-    DecodeSmem s;     // ring, Q staging, ring/Q barriers, meta, misc (shared with the producer)
-    uint32_t qtile;   // Q as the A operand: [D/64 halves][128 rows][128 B], swizzled
-    uint32_t ptile0;  // P tiles ([rows][128 B], swizzled) in the unused rows 64..127 of the Q tile
-    uint32_t ptile1;
-    uint32_t xbars;
-    uint32_t tslot;   // TMEM base address written by tcgen05.alloc
+struct TcSmem {
+    uint32_t ring, stage_bytes, qtile, qhalf, ones, qbuf, qbuf_bytes, red, rowoff, bars, meta, misc, tslot, total;
 };
 
-__host__ __device__ inline UmmaSmem umma_smem_layout(int D, int rows, int stages)
+// Ring of `stages` slots of [K | V][half][128 tokens][128 B] (both 128-byte
+// swizzled), the Q tile [half][NR rows][128 B] (swizzled, K-major), the ones
+// tile, one staging buffer of the next segment's query rows, the cross-warp
+// max scratch (four warps' maxima, new max, rescale factor; 64 columns
+// each) and the row-offset table, then the barriers.
+__host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
 {
-    UmmaSmem u;
-    DecodeSmem &s = u.s;
-    const uint32_t half_bytes = 128u * 128u;        // one column half of the 128-row Q tile
-    s.stage_bytes = (uint32_t)(2 * kStageTokens * D * 2);
-    s.ring = 0;
-    u.qtile = s.ring + (uint32_t)stages * s.stage_bytes;
-    u.ptile0 = u.qtile + 64u * 128u;                // half 0, rows 64..127
-    u.ptile1 = D >= 128 ? u.qtile + half_bytes + 64u * 128u : u.qtile + half_bytes;
-    const uint32_t qtile_end = u.qtile + (uint32_t)(D / 64) * half_bytes + (D >= 128 ? 0u : 64u * 128u);
-    s.qbuf = align_up(qtile_end > u.ptile1 + 64u * 128u ? qtile_end : u.ptile1 + 64u * 128u, 128);
-    s.qbuf_bytes = align_up((uint32_t)(rows * D * 2), 128);
-    s.comb_o = s.comb_m = s.comb_l = 0;
-    s.bars = align_up(s.qbuf + 2 * s.qbuf_bytes, 8);
-    u.xbars = s.bars + (uint32_t)((2 * stages + 4) * 8);
-    s.meta = u.xbars + (uint32_t)(kNumXbars * 8);
-    s.misc = s.meta + (uint32_t)(stages * 4);
-    u.tslot = s.misc + 8;
-    // The MMAs read both P tiles and the Q tile as full 128-row operands, so
-    // the padding rows of the last tile must also lie inside the allocation.
-    const uint32_t mma_end = u.ptile1 + 128u * 128u;
-    const uint32_t used = s.misc + 16 > mma_end ? s.misc + 16 : mma_end;
-    s.total = used + 1024;   // + slack to align the base to 1024 bytes
+    TcSmem u;
+    const int nr = tc_nr(rows);
+    u.stage_bytes = (uint32_t)(2 * kTT * kD * 2);
+    u.ring = 0;
+    u.qhalf = (uint32_t)nr * 128u;
+    u.qtile = u.ring + (uint32_t)stages * u.stage_bytes;
+    u.ones = u.qtile + (uint32_t)kHalves * u.qhalf;
+    u.qbuf = u.ones + kOnesBytes;
+    u.qbuf_bytes = align_up((uint32_t)(rows * kD * 2), 128);
+    u.red = u.qbuf + u.qbuf_bytes;
+    u.rowoff = u.red + (uint32_t)((kSoftmaxWarps + 2) * 64 * 4);
+    // full[stages], empty[stages], qfull, qempty, s_full[2], s_free[2],
+    // p_full[2], q_ready, q_tile_free, fin
+    u.bars = align_up(u.rowoff + 64u * 4u, 8);
+    u.meta = u.bars + (uint32_t)((2 * stages + 11) * 8);
+    u.misc = u.meta + (uint32_t)(stages * 4);
+    u.tslot = u.misc + 8;
+    u.total = u.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
     return u;
 }
 
-struct UCtx {
-    Ctx c;
-    UmmaSmem u;
+struct TcCtx {
+    uint8_t *smem;
+    uint32_t base;
+    TcSmem lay;
+    int stages;
+    volatile uint32_t *abort_flag;
+    uint32_t *bcast;
+    int64_t cta_begin, cta_end;
 };
 
-__device__ __forceinline__ uint32_t xbar(const UCtx &x, int i) { return x.c.base + x.u.xbars + 8u * i; }
-__device__ __forceinline__ uint32_t s_full_bar(const UCtx &x, int b) { return xbar(x, 0 + b); }
-__device__ __forceinline__ uint32_t s_free_bar(const UCtx &x, int b) { return xbar(x, 2 + b); }
-__device__ __forceinline__ uint32_t p_full_bar(const UCtx &x, int b) { return xbar(x, 4 + b); }
-__device__ __forceinline__ uint32_t p_free_bar(const UCtx &x, int b) { return xbar(x, 6 + b); }
-__device__ __forceinline__ uint32_t q_ready_bar(const UCtx &x) { return xbar(x, 8); }
-__device__ __forceinline__ uint32_t q_tile_free_bar(const UCtx &x) { return xbar(x, 9); }
-__device__ __forceinline__ uint32_t fin_bar(const UCtx &x) { return xbar(x, 10); }
+__device__ __forceinline__ uint32_t bar_at(const TcCtx &c, int i) { return c.base + c.lay.bars + 8u * i; }
+__device__ __forceinline__ uint32_t full_b(const TcCtx &c, int s) { return bar_at(c, s); }
+__device__ __forceinline__ uint32_t empty_b(const TcCtx &c, int s) { return bar_at(c, c.stages + s); }
+__device__ __forceinline__ uint32_t qfull_b(const TcCtx &c) { return bar_at(c, 2 * c.stages); }
+__device__ __forceinline__ uint32_t qempty_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 1); }
+__device__ __forceinline__ uint32_t s_full_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 2 + b); }
+__device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 4 + b); }
+__device__ __forceinline__ uint32_t p_full_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 6 + b); }
+__device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 8); }
+__device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 9); }
+__device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 10); }
+__device__ __forceinline__ uint32_t slot_addr(const TcCtx &c, int slot)
+{
+    return c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+}
 
-__device__ __forceinline__ uint32_t ptile(const UCtx &x, int b) { return x.c.base + (b ? x.u.ptile1 : x.u.ptile0); }
+// N consecutive TMEM columns (N a multiple of 16) of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c)
+        tmem_ld16_nowait(taddr + 16u * c, r + 16 * c);
+    tmem_wait_ld();
+}
+
+// ---------------------------------------------------------------------------
+// producer warp
+// ---------------------------------------------------------------------------
+// Stage j of a segment is the 128 tokens from p0*P + j*128: 128/P pages,
+// each copied as 2 (K, V) x 2 (column halves) boxes of P rows x 128 bytes,
+// one box per lane.  Stage layout [K | V][half][token][128 B].
+__device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,
+                            const TcCtx &c)
+{
+    const int lane = threadIdx.x & 31;
+    const int stages = c.stages;
+    const int P = p.page_size;
+    const int RB = kTT / P;                              // pages per stage (4 or 8)
+    const int log2P = 31 - __clz(P);
+    const int my_kv = lane / (kHalves * RB);
+    const int my_h = (lane / RB) % kHalves;
+    const int my_rb = lane % RB;
+    const bool copier = lane < 2 * kHalves * RB;
+    const uint32_t page_bytes = 2u * kHalves * (uint32_t)P * 128u;   // K and V of one page
+    const uint64_t pol = l2_evict_first_policy();
+    if (lane == 0) {
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
+    }
+
+    bool alive = true;
+    int kbase = 0, seg = 0;
+    int last_issued_stage = -1;
+    int q_issued = -1;
+    Segment s = locate(p, c.cta_begin, c.cta_end);
+    int pre = (lane < s.p1 - s.p0) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
+    for (;;) {
+        const bool has_next = s.seg_end < c.cta_end;
+        Segment sn;
+        int pre_next = -1;
+        if (has_next) {
+            sn = next_segment(p, s, c.cta_end);
+            pre_next = (lane < sn.p1) ? __ldg(p.block_table + (int64_t)sn.b * p.max_pages + lane) : -1;
+        }
+        const int dev_len = (lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
+        // --- query rows of this (b, g): N bulk copies of G contiguous rows
+        if (alive) {
+            bool ok = mbar_wait_bounded(qempty_b(c), (uint32_t)((seg & 1) ^ 1), c.abort_flag, p.err);
+            alive = __all_sync(0xffffffffu, ok);
+        }
+        if (alive && lane == 0) {
+            const uint32_t rows_bytes = (uint32_t)p.group * kD * 2u;
+            mbar_arrive_expect_tx(qfull_b(c), rows_bytes * p.n_models);
+            const __nv_bfloat16 *qsrc = p.q + ((int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group) * kD;
+            const uint32_t qdst = c.base + c.lay.qbuf;
+            for (int m = 0; m < p.n_models; ++m)
+                bulk_load(qdst + m * rows_bytes, qsrc + (int64_t)m * p.hq * kD, rows_bytes, qfull_b(c));
+            q_issued = seg;
+        }
+        // --- K/V pages of the segment
+        const int tok_end = s.p1 * P;
+        const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
+        const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
+        int w0 = s.p0;                                   // block-table window [w0, w0+32)
+        int cur = pre;
+        int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+        for (int j = 0; j < nst; ++j) {
+            const int k = kbase + j;
+            const int slot = k % stages;
+            const int tok0 = s.p0 * P + j * kTT;
+            // a stage's pages start at a multiple of RB from p0, so they never
+            // straddle a 32-entry window
+            if ((tok0 >> log2P) >= w0 + 32) {
+                w0 += 32;
+                cur = nxt;
+                nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+            }
+            const int my_tok = tok0 + my_rb * P;
+            const int my_id = __shfl_sync(0xffffffffu, cur, ((my_tok >> log2P) - w0) & 31);
+            bool ok = true;
+            if (alive && lane == 0)
+                ok = mbar_wait_bounded(empty_b(c, slot), (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
+            alive = alive && __all_sync(0xffffffffu, ok);
+            const bool my_valid = copier && my_tok < tok_end && my_id >= 0 && my_id < p.num_pages;
+            // lanes 0..RB-1 copy the K half-0 boxes: their ballot is the page mask
+            const uint32_t mask = __ballot_sync(0xffffffffu, my_valid) & ((1u << RB) - 1u);
+            if (alive && lane == 0) {
+                for (int rb = 0; rb < RB; ++rb)
+                    if (!((mask >> rb) & 1u) && tok0 + rb * P < tok_end)
+                        atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
+                volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
+                meta[slot] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
+                mbar_arrive_expect_tx(full_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
+            }
+            __syncwarp();
+            if (alive && my_valid) {
+                const uint32_t dst = slot_addr(c, slot) + (uint32_t)my_kv * (kTT * kD * 2) +
+                                     (uint32_t)my_h * (kTT * 128) + (uint32_t)my_rb * (uint32_t)P * 128u;
+                tma_load_2d(dst, my_kv ? tmV : tmK, my_h * 64, (my_id * p.hkv + s.g) * P, full_b(c, slot), pol);
+            }
+            if (alive)
+                last_issued_stage = k;
+            __syncwarp();
+        }
+        if (lane == 0 && dev_len != plan_len(p, s))
+            atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
+        kbase += nst;
+        ++seg;
+        if (!has_next)
+            break;
+        s = sn;
+        pre = pre_next;
+    }
+    // After an abort, wait (bounded) for every copy still in flight so no TMA
+    // write lands after the CTA exits.
+    if (!alive && lane == 0) {
+        for (int k = last_issued_stage - stages + 1; k <= last_issued_stage; ++k)
+            if (k >= 0)
+                mbar_drain_bounded(full_b(c, k % stages), (uint32_t)((k / stages) & 1));
+        if (q_issued >= 0)
+            mbar_drain_bounded(qfull_b(c), (uint32_t)(q_issued & 1));
+    }
+}
 
 // ---------------------------------------------------------------------------
 // MMA issuer (one lane)
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ void mma_issuer(const DecodeParams &p, const UCtx &x, uint32_t tmem)
+template <int NR>
+__device__ void tc_mma(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
-    constexpr int TT = kStageTokens;
-    constexpr int HALVES = D / 64;
-    const Ctx &c = x.c;
-    const int stages = p.stages;
+    constexpr int NPV = tc_npv(NR);
+    const int stages = c.stages;
     const int P = p.page_size;
-    const int BR = p.box_rows;
-    const int RB = TT / BR;
-    const uint32_t idesc_qk = umma_idesc_bf16(128, BR, false, false);
-    const uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
-    const uint32_t qtile = c.base + x.u.qtile;
+    const uint32_t idesc_qk = umma_idesc_bf16(128, NR, false, false);
+    const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
+    const uint32_t idesc_l = umma_idesc_bf16(128, NPV, false, true);
+    const uint32_t qtile = c.base + c.lay.qtile;
+    const uint64_t ones = umma_sdesc_noswz(c.base + c.lay.ones, 128u, 256u);
     bool alive = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (alive)
@@ -125,90 +282,97 @@ __device__ void mma_issuer(const DecodeParams &p, const UCtx &x, uint32_t tmem)
         return alive;
     };
 
-    // O += P(k) V(k) for stage k of the current segment
+    // O^T += V^T P^T, L += 1 P^T and Llo += 1 P_lo^T for stage k; P^T and
+    // P_lo^T sit over the two halves of the stage's K tile.
     auto pv = [&](int k, bool first) {
         const int buf = k & 1;
         const int slot = k % stages;
-        if (wait(p_full_bar(x, buf), (uint32_t)((k >> 1) & 1))) {
+        if (wait(p_full_b(c, buf), (uint32_t)((k >> 1) & 1))) {
             tc_fence_after();
-            const uint32_t vst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)(TT * D * 2);
+            const uint32_t kst = slot_addr(c, slot);
+            const uint32_t vst = kst + (uint32_t)(kTT * kD * 2);
 #pragma unroll
-            for (int ks = 0; ks < TT / 16; ++ks) {
-                const int t0 = ks * 16;
-                const uint32_t va = vst + (uint32_t)((t0 / BR) * (BR * D * 2) + (t0 % BR) * 128);
-                const uint64_t bd = umma_sdesc_sw128(va, (uint32_t)(BR * 128), 1024u);
-                const uint64_t ad = umma_sdesc_sw128(ptile(x, buf) + (uint32_t)(ks * 32), 16u, 1024u);
-                umma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+            for (int ks = 0; ks < kTT / 16; ++ks) {
+                const uint64_t ad = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
+                const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
+                const uint64_t bl =
+                    umma_sdesc_sw128(kst + (uint32_t)(kTT * 128) + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
+                const uint32_t acc = (first && ks == 0) ? 0u : 1u;
+                umma_bf16(tmem + kColO, ad, bd, idesc_pv, acc);
+                umma_bf16(tmem + kColL, ones, bd, idesc_l, acc);
+                umma_bf16(tmem + kColLlo, ones, bl, idesc_l, acc);
             }
         }
-        umma_commit(empty_bar(c, slot, stages));
-        umma_commit(p_free_bar(x, buf));
+        umma_commit(empty_b(c, slot));
     };
 
     int kbase = 0, seg = 0;
+    int pend = -1;
+    bool pend_first = false;
     Segment s = locate(p, c.cta_begin, c.cta_end);
     for (;;) {
-        const int nst = (s.p1 * P - s.p0 * P + TT - 1) / TT;
-        wait(q_ready_bar(x), (uint32_t)(seg & 1));
+        const int nst = (s.p1 * P - s.p0 * P + kTT - 1) / kTT;
+        wait(q_ready_b(c), (uint32_t)(seg & 1));
         tc_fence_after();
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int buf = k & 1;
             const int slot = k % stages;
-            wait(full_bar(c, slot), (uint32_t)((k / stages) & 1));
-            wait(s_free_bar(x, buf), (uint32_t)(((k >> 1) & 1) ^ 1));
+            wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
+            wait(s_free_b(c, buf), (uint32_t)(((k >> 1) & 1) ^ 1));
             if (alive) {
                 tc_fence_after();
-                const uint32_t kst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
-                for (int rb = 0; rb < RB; ++rb) {
+                const uint32_t kst = slot_addr(c, slot);
 #pragma unroll
-                    for (int h = 0; h < HALVES; ++h)
+                for (int h = 0; h < kHalves; ++h)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = umma_sdesc_sw128(qtile + (uint32_t)(h * 128 * 128 + kk * 32), 16u, 1024u);
-                            const uint64_t bd = umma_sdesc_sw128(
-                                kst + (uint32_t)(rb * (BR * D * 2) + h * (BR * 128) + kk * 32), 16u, 1024u);
-                            umma_bf16(tmem + kTmemS + (uint32_t)(buf * TT + rb * BR), ad, bd, idesc_qk,
-                                      (h | kk) ? 1u : 0u);
-                        }
-                }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad =
+                            umma_sdesc_sw128(kst + (uint32_t)(h * kTT * 128 + kk * 32), 16u, 1024u);
+                        const uint64_t bd =
+                            umma_sdesc_sw128(qtile + (uint32_t)h * c.lay.qhalf + (uint32_t)(kk * 32), 16u, 1024u);
+                        umma_bf16(tmem + kColS + (uint32_t)(buf * 64), ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
+                    }
             }
-            umma_commit(s_full_bar(x, buf));
-            if (j >= 1)
-                pv(k - 1, j == 1);
+            umma_commit(s_full_b(c, buf));
+            if (j == nst - 1)
+                umma_commit(q_tile_free_b(c));
+            if (pend >= 0)
+                pv(pend, pend_first);
+            pend = k;
+            pend_first = (j == 0);
         }
-        pv(kbase + nst - 1, nst == 1);
-        umma_commit(q_tile_free_bar(x));
         kbase += nst;
         ++seg;
         if (s.seg_end >= c.cta_end)
             break;
         s = next_segment(p, s, c.cta_end);
     }
+    if (pend >= 0)
+        pv(pend, pend_first);
     // every MMA issued above has completed once this arrives
-    umma_commit(fin_bar(x));
-    mbar_drain_bounded(fin_bar(x), 0u);
+    umma_commit(fin_b(c));
+    mbar_drain_bounded(fin_b(c), 0u);
 }
 
 // ---------------------------------------------------------------------------
-// softmax warps (thread = stacked row)
+// softmax warps (thread = token of the stage; = column of O^T at a segment end)
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem)
+template <int NR>
+__device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
-    constexpr int TT = kStageTokens;
-    const Ctx &c = x.c;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int r = warp * 32 + lane;            // stacked row == TMEM lane
-    const bool active = r < p.rows;
-    const int stages = p.stages;
+    const int t = threadIdx.x;
+    const int warp = t >> 5;
+    const int lane = t & 31;
+    const int stages = c.stages;
     const int P = p.page_size;
-    const int BR = p.box_rows;
-    const int log2BR = 31 - __clz(BR);
+    const int R = p.rows;
+    const int log2P = 31 - __clz(P);
     const float sl2 = p.scale_log2;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const volatile uint32_t *meta = reinterpret_cast<const volatile uint32_t *>(c.smem + c.lay.meta);
+    float *red = reinterpret_cast<float *>(c.smem + c.lay.red);
+    const int *rowoff = reinterpret_cast<const int *>(c.smem + c.lay.rowoff);
     bool alive = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
         bool ok = false;
@@ -218,52 +382,60 @@ __device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem
         return alive;
     };
 
-    int kbase = 0, seg = 0;
-    Segment s = locate(p, c.cta_begin, c.cta_end);
-    for (;;) {
-        const int tok_end = s.p1 * P;
-        const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
-        const int L = plan_len(p, s);
-        const int lim = L < tok_end ? L : tok_end;
-
-        // --- query row r: staging buffer -> swizzled Q tile (A operand)
-        if (seg > 0)
-            wait(q_tile_free_bar(x), (uint32_t)((seg - 1) & 1));
-        const int qb = seg & 1;
-        wait(qfull_bar(c, qb, stages), (uint32_t)((seg >> 1) & 1));
-        if (alive && active) {
-            const uint8_t *src = c.smem + c.lay.qbuf + qb * c.lay.qbuf_bytes + (size_t)r * D * 2;
-#pragma unroll
-            for (int ch = 0; ch < D / 8; ++ch) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(src + ch * 16);
-                const uint32_t off = (uint32_t)((ch >> 3) * 128 * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
-                *reinterpret_cast<uint4 *>(c.smem + x.u.qtile + off) = v;
+    // query rows of segment `sg`: staging buffer -> swizzled K-major Q tile
+    auto stage_q = [&](int sg) {
+        wait(qfull_b(c), (uint32_t)(sg & 1));
+        if (alive) {
+            const uint8_t *src = c.smem + c.lay.qbuf;
+            for (int e = t; e < R * (kD / 8); e += kSoftmaxThreads) {
+                const int rr = e >> 4, ch = e & 15;
+                const uint4 v = *reinterpret_cast<const uint4 *>(src + rr * (kD * 2) + ch * 16);
+                const uint32_t off = (uint32_t)(ch >> 3) * c.lay.qhalf + (uint32_t)rr * 128u +
+                                     (uint32_t)(((ch & 7) ^ (rr & 7)) << 4);
+                *reinterpret_cast<uint4 *>(c.smem + c.lay.qtile + off) = v;
             }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(qempty_bar(c, qb, stages));
-            mbar_arrive(q_ready_bar(x));
+            mbar_arrive(qempty_b(c));
+            mbar_arrive(q_ready_b(c));
         }
+    };
 
-        float m_use = -INFINITY, lsum = 0.f;
+    int kbase = 0, seg = 0;
+    Segment s = locate(p, c.cta_begin, c.cta_end);
+    stage_q(0);
+    for (;;) {
+        const int tok_end = s.p1 * P;
+        const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
+        const int L = plan_len(p, s);
+        const int lim = L < tok_end ? L : tok_end;
+        float m_use[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            m_use[r] = -INFINITY;
+
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int buf = k & 1;
             const int slot = k % stages;
-            // --- this row of S for the stage's tokens
-            uint32_t sv[32];
-            if (wait(s_full_bar(x, buf), (uint32_t)((k >> 1) & 1))) {
+            // --- this token's scores for all stacked rows
+            uint32_t sv[NR];
+            if (wait(s_full_b(c, buf), (uint32_t)((k >> 1) & 1))) {
                 tc_fence_after();
-                tmem_ld32(tmem + lane_base + kTmemS + (uint32_t)(buf * TT), sv);
+                tmem_ld_cols<NR>(tmem + lane_base + kColS + (uint32_t)(buf * 64), sv);
+            } else {
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    sv[r] = 0u;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(s_free_bar(x, buf));
-            // the slot's TMA data (V rows to mask, the validity word)
-            wait(full_bar(c, slot), (uint32_t)((k / stages) & 1));
+                mbar_arrive(s_free_b(c, buf));
+            // the slot's validity word (the QK MMA has already consumed the data)
+            wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
             const uint32_t tagged = alive ? meta[slot] : 0u;
             if (alive && (tagged >> 8) != ((uint32_t)k & 0xffffffu)) {
                 if (lane == 0) {
@@ -272,151 +444,176 @@ __device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem
                 }
                 alive = false;
             }
-            const uint32_t mask = tagged & 0xffu;
-            const int tok0 = s.p0 * P + j * TT;
-            const bool all_valid = (mask == (1u << (TT / BR)) - 1u) && (tok0 + TT <= lim);
-            auto tok_valid = [&](int t) -> bool { return ((mask >> (t >> log2BR)) & 1u) && (tok0 + t < lim); };
-            if (alive && !all_valid && warp == 0) {
-                // masked V rows may hold stale or non-finite bits: zero them
-                const uint32_t vst = c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)(TT * D * 2);
-                for (int e = lane; e < TT * (D / 8); e += 32) {
-                    const int t = e / (D / 8);
-                    const int ch = e - t * (D / 8);
-                    if (!tok_valid(t))
-                        *reinterpret_cast<uint4 *>(c.smem + vst + (uint32_t)((t >> log2BR) * (BR * D * 2) +
-                                                                                (ch >> 3) * (BR * 128) +
-                                                                                (t & (BR - 1)) * 128 + (ch & 7) * 16)) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            // --- masked, scaled scores and the tile max (base 2)
-            float xs[32];
-            float mt = -INFINITY;
+            const int tok0 = s.p0 * P + j * kTT;
+            const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) && (tok0 + t < lim);
+            const uint32_t kst = c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+            if (alive && !valid) {
+                // this token's V row may hold stale or non-finite bits: zero it
+                const uint32_t vrow = c.base + kst + (uint32_t)(kTT * kD * 2) + (uint32_t)t * 128u;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                float v = __uint_as_float(sv[t]) * sl2;
-                if (!all_valid && !tok_valid(t))
-                    v = -INFINITY;
-                xs[t] = v;
-                mt = fmaxf(mt, v);
+                for (int h = 0; h < kHalves; ++h)
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_zero16(vrow + (uint32_t)(h * kTT * 128 + ch * 16));
             }
-            // --- lazy rescale of this row's O when its max jumps by > 2^8
-            const bool need = alive && m_use != -INFINITY && mt > m_use + kRescaleLog2;
-            if (__any_sync(0xffffffffu, need) && alive && j >= 1) {
-                // O must hold PV of the previous stage before it is touched
-                wait(p_free_bar(x, (k - 1) & 1), (uint32_t)(((k - 1) >> 1) & 1));
+            float xs[NR];
+            bool need = false;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                xs[r] = valid ? __uint_as_float(sv[r]) * sl2 : -INFINITY;
+                need = need || (xs[r] > m_use[r] + kRescaleLog2);
+            }
+            // --- lazy max refresh: the four warps agree on a new m[] together
+            if (bar_red_or(1, kSoftmaxThreads, need)) {
+                float *red_m = red + kSoftmaxWarps * 64;      // new max per column
+                float *red_a = red_m + 64;                    // rescale factor per column
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    float v = xs[r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    if (lane == 0)
+                        red[warp * 64 + r] = v;
+                }
+                named_barrier(1, kSoftmaxThreads);
+                if (t < NR) {
+                    float mo = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < NR; ++r)
+                        mo = r == t ? m_use[r] : mo;
+                    const float mn = fmaxf(fmaxf(mo, fmaxf(red[t], red[64 + t])), fmaxf(red[128 + t], red[192 + t]));
+                    red_m[t] = mn;
+                    red_a[t] = mn == -INFINITY ? 1.f : ex2_approx(mo - mn);
+                }
+                named_barrier(1, kSoftmaxThreads);
+                if (j >= 1) {
+                    // O^T, L and Llo hold stages up to k-1: rescale them once PV(k-1) is done
+                    const int kp = k - 1;
+                    wait(empty_b(c, kp % stages), (uint32_t)((kp / stages) & 1));
+                    if (alive) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int part = 0; part < 3; ++part) {
+                            const uint32_t col = tmem + lane_base + (part == 0 ? kColO : part == 1 ? kColL : kColLlo);
+#pragma unroll
+                            for (int c16 = 0; c16 < NR / 16; ++c16) {
+                                uint32_t v[16];
+                                tmem_ld16_nowait(col + 16u * c16, v);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * red_a[c16 * 16 + e]);
+                                tmem_st16_nowait(col + 16u * c16, v);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    m_use[r] = red_m[r];
+            }
+            // --- this token's rows of P^T and P_lo^T, over the stage's K halves
+            uint8_t *prow = c.smem + kst + (uint32_t)t * 128u;
+#pragma unroll
+            for (int ch = 0; ch < NR / 8; ++ch) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = ch * 8 + 2 * e;
+                    const float mu0 = m_use[r] == -INFINITY ? 0.f : m_use[r];
+                    const float mu1 = m_use[r + 1] == -INFINITY ? 0.f : m_use[r + 1];
+                    const float p0 = ex2_approx(xs[r] - mu0);
+                    const float p1 = ex2_approx(xs[r + 1] - mu1);
+                    hi[e] = pack_bf16x2(p0, p1);
+                    lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16), p1 - __uint_as_float(hi[e] & 0xffff0000u));
+                }
                 if (alive) {
-                    tc_fence_after();
-                    const float alpha = need ? ex2_approx(m_use - mt) : 1.f;
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(cc * 32), ov);
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
-                        tmem_st32(tmem + lane_base + kTmemO + (uint32_t)(cc * 32), ov);
-                    }
-                    tc_fence_before();
-                    if (need) {
-                        lsum *= alpha;
-                        m_use = mt;
-                    }
+                    const uint32_t sw = (uint32_t)((ch ^ (t & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(prow + kTT * 128 + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
-            }
-            if (m_use == -INFINITY)
-                m_use = mt;                      // first scored tile of the segment
-            const float mu = m_use == -INFINITY ? 0.f : m_use;
-            uint32_t pk[16];
-#pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-                const float p0 = ex2_approx(xs[t] - mu);
-                const float p1 = ex2_approx(xs[t + 1] - mu);
-                lsum += p0 + p1;
-                pk[t / 2] = pack_bf16x2(p0, p1);
-            }
-            // --- this row of P into the tile of this stage's parity
-            wait(p_free_bar(x, buf), (uint32_t)(((k >> 1) & 1) ^ 1));
-            if (alive && active) {
-                const uint32_t prow = ptile(x, buf) - c.base + (uint32_t)r * 128u;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4 *>(c.smem + prow + (uint32_t)((ch ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
             }
             fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(p_full_bar(x, buf));
+                mbar_arrive(p_full_b(c, buf));
         }
 
-        // --- segment end: this row of O, normalised
+        // --- next segment's query rows, as soon as the last QK of this one is done
+        const bool has_next = s.seg_end < c.cta_end;
+        if (has_next) {
+            wait(q_tile_free_b(c), (uint32_t)(seg & 1));
+            stage_q(seg + 1);
+        }
+
+        // --- segment end: column d = t of O^T, normalised by the row sums
         const int last = kbase + nst - 1;
-        wait(p_free_bar(x, last & 1), (uint32_t)((last >> 1) & 1));
-        const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
-        const int slot_id = whole ? 0 : 2 * (int)blockIdx.x + (s.seg_begin == c.cta_begin ? 0 : 1);
-        const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
-        const int64_t orow = whole ? (int64_t)s.b * p.n_models * p.hq + q_row(p, s.g, active ? r : 0)
-                                   : (int64_t)slot_id * p.rows + r;
+        wait(empty_b(c, last % stages), (uint32_t)((last / stages) & 1));
         if (alive)
             tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
-            if (alive)
-                tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(cc * 32), ov);
-            if (alive && active) {
-                if (whole) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + cc * 32);
+        const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
+        const int slot_id = whole ? 0 : 2 * (int)blockIdx.x + (s.seg_begin == c.cta_begin ? 0 : 1);
+        const int64_t row0 = (int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group;
+        float my_m = -INFINITY, my_l = 0.f;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
+        for (int c16 = 0; c16 < NR / 16; ++c16) {
+            uint32_t ov[16], lv[16], llo[16];
+            if (alive) {
+                tmem_ld16_nowait(tmem + lane_base + kColO + 16u * c16, ov);
+                tmem_ld16_nowait(tmem + lane_base + kColL + 16u * c16, lv);
+                tmem_ld16_nowait(tmem + lane_base + kColLlo + 16u * c16, llo);
+                tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 2 * e]) * inv,
-                                               __uint_as_float(ov[q4 * 8 + 2 * e + 1]) * inv);
-                        dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 16; ++e) {
+                    const int r = c16 * 16 + e;
+                    const float l = __uint_as_float(lv[e]);
+                    if (r == t) {
+                        my_m = m_use[r];
+                        my_l = l + __uint_as_float(llo[e]);
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_part + orow * D + cc * 32);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(__uint_as_float(ov[4 * q4]) * inv, __uint_as_float(ov[4 * q4 + 1]) * inv,
-                                              __uint_as_float(ov[4 * q4 + 2]) * inv,
-                                              __uint_as_float(ov[4 * q4 + 3]) * inv);
+                    if (r < R) {
+                        const float o = __uint_as_float(ov[e]) * (l > 0.f ? __frcp_rn(l) : 0.f);
+                        if (whole)
+                            p.out[(row0 + rowoff[r]) * kD + t] = __float2bfloat16_rn(o);
+                        else
+                            p.ws_part[((int64_t)slot_id * R + r) * kD + t] = o;
+                    }
                 }
             }
         }
         tc_fence_before();
-        if (alive && active) {
-            const float lse = lsum > 0.f ? (m_use + log2f(lsum)) * kLn2u : -INFINITY;
+        if (alive && t < R) {
+            const float lse = my_l > 0.f ? (my_m + log2f(my_l)) * kLn2 : -INFINITY;
             if (whole) {
                 if (p.lse_out)
-                    p.lse_out[orow] = lse;
+                    p.lse_out[row0 + rowoff[t]] = lse;
             } else {
-                p.ws_lse[orow] = lse;
+                p.ws_lse[(int64_t)slot_id * R + t] = lse;
             }
         }
-        named_barrier(1, 32u * kSoftmaxWarps);
+        named_barrier(1, kSoftmaxThreads);
 
         // --- split unit: the last piece to arrive merges all pieces
         if (!whole) {
             const int c0 = cta_of(p, s.unit_begin);
             const int c1 = cta_of(p, s.unit_end - 1);
             uint32_t *counter = p.ws_count + (int64_t)s.b * p.hkv + s.g;
-            if (threadIdx.x == 0) {
+            if (t == 0) {
                 __threadfence();
                 const uint32_t prev = atomicAdd(counter, 1u);
                 *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
             }
-            named_barrier(1, 32u * kSoftmaxWarps);
+            named_barrier(1, kSoftmaxThreads);
             if (*c.bcast) {
                 __threadfence();
-                const int dq = D / 4;
-                for (int rr = warp; rr < p.rows; rr += kSoftmaxWarps) {
+                const int dq = kD / 4;
+                for (int rr = warp; rr < R; rr += kSoftmaxWarps) {
                     float M = -INFINITY;
                     for (int cc = c0 + lane; cc <= c1; cc += 32)
-                        M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)piece_slot(p, cc, s.unit_begin) * p.rows + rr));
+                        M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)piece_slot(p, cc, s.unit_begin) * R + rr));
 #pragma unroll
                     for (int o_ = 16; o_ > 0; o_ >>= 1)
                         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o_));
@@ -425,12 +622,12 @@ __device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem
                     if (M != -INFINITY) {
                         for (int cc = c0; cc <= c1; ++cc) {
                             const int sl = piece_slot(p, cc, s.unit_begin);
-                            const float w = ex2_approx((__ldcg(p.ws_lse + (int64_t)sl * p.rows + rr) - M) *
+                            const float w = ex2_approx((__ldcg(p.ws_lse + (int64_t)sl * R + rr) - M) *
                                                        1.4426950408889634f);
                             wsum += w;
                             if (lane < dq) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                                            p.ws_part + ((int64_t)sl * p.rows + rr) * D) + lane);
+                                const float4 v = __ldcg(
+                                    reinterpret_cast<const float4 *>(p.ws_part + ((int64_t)sl * R + rr) * kD) + lane);
                                 acc.x += w * v.x;
                                 acc.y += w * v.y;
                                 acc.z += w * v.z;
@@ -439,25 +636,25 @@ __device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem
                         }
                     }
                     const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-                    const int64_t orr = (int64_t)s.b * p.n_models * p.hq + q_row(p, s.g, rr);
+                    const int64_t orr = row0 + rowoff[rr];
                     if (lane < dq) {
                         uint2 packed;
                         packed.x = pack_bf16x2(acc.x * winv, acc.y * winv);
                         packed.y = pack_bf16x2(acc.z * winv, acc.w * winv);
-                        *reinterpret_cast<uint2 *>(p.out + orr * D + lane * 4) = packed;
+                        *reinterpret_cast<uint2 *>(p.out + orr * kD + lane * 4) = packed;
                     }
                     if (lane == 0 && p.lse_out)
                         p.lse_out[orr] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
                 }
-                if (threadIdx.x == 0)
+                if (t == 0)
                     *counter = 0u;
             }
-            named_barrier(1, 32u * kSoftmaxWarps);
+            named_barrier(1, kSoftmaxThreads);
         }
 
         kbase += nst;
         ++seg;
-        if (s.seg_end >= c.cta_end)
+        if (!has_next)
             break;
         s = next_segment(p, s, c.cta_end);
     }
@@ -465,22 +662,21 @@ __device__ void softmax_rows(const DecodeParams &p, const UCtx &x, uint32_t tmem
 
 }  // namespace
 
-template <int D>
-__global__ void __launch_bounds__(kUmmaThreads, 1)
+template <int NR>
+__global__ void __launch_bounds__(kTcThreads, 1)
     shkv_decode_umma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    UCtx x;
-    Ctx &c = x.c;
+    TcCtx c;
     {
         const uint32_t raw = smem_u32(smem_raw);
         const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
         c.smem = smem_raw + pad;
         c.base = raw + pad;
     }
-    x.u = umma_smem_layout(D, p.rows, p.stages);
-    c.lay = x.u.s;
+    c.stages = p.stages;
+    c.lay = tc_smem_layout(p.rows, p.stages);
     c.abort_flag = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.misc);
     c.bcast = reinterpret_cast<uint32_t *>(c.smem + c.lay.misc + 4);
     c.cta_begin = p.cta_cut[blockIdx.x];
@@ -488,39 +684,52 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(full_bar(c, s), 1);
-            mbar_init(empty_bar(c, s, p.stages), 1);         // one tcgen05.commit per stage
+        for (int s = 0; s < c.stages; ++s) {
+            mbar_init(full_b(c, s), 1);
+            mbar_init(empty_b(c, s), 1);                     // one tcgen05.commit per stage
         }
+        mbar_init(qfull_b(c), 1);
+        mbar_init(qempty_b(c), kSoftmaxWarps);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(qfull_bar(c, i, p.stages), 1);
-            mbar_init(qempty_bar(c, i, p.stages), kSoftmaxWarps);
-            mbar_init(s_full_bar(x, i), 1);
-            mbar_init(s_free_bar(x, i), kSoftmaxWarps);
-            mbar_init(p_full_bar(x, i), kSoftmaxWarps);
-            mbar_init(p_free_bar(x, i), 1);
+            mbar_init(s_full_b(c, i), 1);
+            mbar_init(s_free_b(c, i), kSoftmaxWarps);
+            mbar_init(p_full_b(c, i), kSoftmaxWarps);
         }
-        mbar_init(q_ready_bar(x), kSoftmaxWarps);
-        mbar_init(q_tile_free_bar(x), 1);
-        mbar_init(fin_bar(x), 1);
+        mbar_init(q_ready_b(c), kSoftmaxWarps);
+        mbar_init(q_tile_free_b(c), 1);
+        mbar_init(fin_b(c), 1);
         *c.abort_flag = 0u;
         *c.bcast = 0u;
         fence_barrier_init();
     }
+    if (warp < kSoftmaxWarps) {
+        // ones operand, zeroed Q tile (its padding rows stay zero), row offsets
+        const uint32_t one2 = 0x3F803F80u;   // two bf16 1.0
+        for (uint32_t i = threadIdx.x; i < kOnesBytes / 16; i += kSoftmaxThreads)
+            *reinterpret_cast<uint4 *>(c.smem + c.lay.ones + 16 * i) = make_uint4(one2, one2, one2, one2);
+        for (uint32_t i = threadIdx.x; i < (uint32_t)kHalves * c.lay.qhalf / 16; i += kSoftmaxThreads)
+            *reinterpret_cast<uint4 *>(c.smem + c.lay.qtile + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x < 64) {
+            const int r = threadIdx.x;
+            const int m = r / p.group, jj = r - (r / p.group) * p.group;
+            reinterpret_cast<int *>(c.smem + c.lay.rowoff)[r] = m * p.hq + jj;
+        }
+        fence_proxy_async_smem();
+    }
     if (warp == 0)
-        tmem_alloc(c.base + x.u.tslot, kTmemCols);
+        tmem_alloc(c.base + c.lay.tslot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + x.u.tslot);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.tslot);
 
     if (warp == kProducerWarp)
-        producer<D>(&tmK, &tmV, p, c);
+        tc_producer(&tmK, &tmV, p, c);
     else if (warp == kMmaWarp) {
         if ((threadIdx.x & 31) == 0)
-            mma_issuer<D>(p, x, tmem);
+            tc_mma<NR>(p, c, tmem);
     } else
-        softmax_rows<D>(p, x, tmem);
+        tc_softmax<NR>(p, c, tmem);
 
     tc_fence_before();
     __syncthreads();
@@ -532,24 +741,45 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-uint32_t umma_smem_bytes(int D, int rows, int stages) { return umma_smem_layout(D, rows, stages).s.total; }
+// Stages of 64 KiB that fit with the rest of the layout (0 if fewer than 2).
+int umma_stages(int rows)
+{
+    int st = kTcMaxStages;
+    while (st >= 2 && tc_smem_layout(rows, st).total > (uint32_t)kSmemLimit)
+        --st;
+    return st >= 2 ? st : 0;
+}
 
-template <int D>
+uint32_t umma_smem_bytes(int rows, int stages) { return tc_smem_layout(rows, stages).total; }
+
+template <int NR>
 static cudaError_t launch_umma_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                                  uint32_t smem, cudaStream_t stream)
 {
-    auto kern = shkv_decode_umma_kernel<D>;
+    auto kern = shkv_decode_umma_kernel<NR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<p.num_ctas, kUmmaThreads, smem, stream>>>(tmK, tmV, p);
+    kern<<<p.num_ctas, kTcThreads, smem, stream>>>(tmK, tmV, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_umma(int D, const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
-                               uint32_t smem, cudaStream_t stream)
+// tmK/tmV: 2-D maps of the pool (128-byte swizzle, box of 64 columns x P rows).
+cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p, uint32_t smem,
+                               cudaStream_t stream)
 {
-    return D == 128 ? launch_umma_t<128>(tmK, tmV, p, smem, stream) : launch_umma_t<64>(tmK, tmV, p, smem, stream);
+    switch (tc_nr(p.rows)) {
+    case 16:
+        return launch_umma_t<16>(tmK, tmV, p, smem, stream);
+    case 32:
+        return launch_umma_t<32>(tmK, tmV, p, smem, stream);
+    case 48:
+        return launch_umma_t<48>(tmK, tmV, p, smem, stream);
+    case 64:
+        return launch_umma_t<64>(tmK, tmV, p, smem, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace shkv

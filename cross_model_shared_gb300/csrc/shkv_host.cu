@@ -17,9 +17,10 @@
 namespace shkv {
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const DecodeParams &p, uint32_t smem, cudaStream_t stream);
-cudaError_t launch_decode_umma(int D, const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
-                               uint32_t smem, cudaStream_t stream);
-uint32_t umma_smem_bytes(int D, int rows, int stages);
+cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p, uint32_t smem,
+                               cudaStream_t stream);
+int umma_stages(int rows);
+uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
                          const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream);
@@ -31,8 +32,10 @@ struct shkv_pool {
     shkv_pool_config cfg;
     int device;
     int num_sms;
-    CUtensorMap tm_k;
+    CUtensorMap tm_k;      // 3-D maps: whole row-blocks (mma.sync consumer)
     CUtensorMap tm_v;
+    CUtensorMap tm_k2;     // 2-D maps: one 64-column half of a page (tcgen05 consumer)
+    CUtensorMap tm_v2;
     std::vector<int32_t> lens;   // host copy of seq_lens
 };
 
@@ -79,6 +82,25 @@ bool make_pool_map(CUtensorMap *tm, void *base, const shkv_pool_config &c)
                          (cuuint32_t)halves};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D view of the same pool: dim0 = D columns, dim1 = rows.  One box
+// {64, P} with 128-byte swizzle is one column half of one head's page,
+// landing as [row][64 columns] so that consecutive pages of a stage stack
+// into one 128-row operand per half.
+bool make_pool_map_2d(CUtensorMap *tm, void *base, const shkv_pool_config &c)
+{
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_pages * c.num_kv_heads * c.page_size};
+    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)c.page_size};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -209,16 +231,19 @@ DecodeShape decode_shape(int rows)
     return s;
 }
 
-// Which consumer runs for R stacked rows: the automatic policy, or the one
-// named by SHKV_DECODE_CONSUMER ("mma" or "umma"; read on every call).
-bool use_umma_consumer(int rows)
+// Which consumer runs for R stacked rows of head dim D: the automatic
+// policy, or the one named by SHKV_DECODE_CONSUMER ("mma" or "umma"; read on
+// every call).  The tcgen05 consumer covers D = 128 and R <= 64 only.
+bool use_umma_consumer(int rows, int head_dim)
 {
+    if (head_dim != 128 || rows > kUmmaMaxRows || umma_stages(rows) == 0)
+        return false;
     const char *env = getenv("SHKV_DECODE_CONSUMER");
     if (env && strcmp(env, "umma") == 0)
-        return rows <= kUmmaMaxRows;
+        return true;
     if (env && strcmp(env, "mma") == 0)
         return false;
-    return rows >= kUmmaMinRows && rows <= kUmmaMaxRows;
+    return rows >= kUmmaMinRows;
 }
 
 }  // namespace
@@ -279,7 +304,8 @@ shkv_status shkv_pool_create(const shkv_pool_config *cfg, shkv_pool **out)
         delete pool;
         return SHKV_ERR_CUDA;
     }
-    if (!make_pool_map(&pool->tm_k, c.k_pages, c) || !make_pool_map(&pool->tm_v, c.v_pages, c)) {
+    if (!make_pool_map(&pool->tm_k, c.k_pages, c) || !make_pool_map(&pool->tm_v, c.v_pages, c) ||
+        !make_pool_map_2d(&pool->tm_k2, c.k_pages, c) || !make_pool_map_2d(&pool->tm_v2, c.v_pages, c)) {
         delete pool;
         return SHKV_ERR_CUDA;
     }
@@ -409,7 +435,7 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                                 p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas);
     if (st != SHKV_OK)
         return st;
-    const bool use_umma = use_umma_consumer(rows);
+    const bool use_umma = use_umma_consumer(rows, c.head_dim);
     const DecodeShape sh = decode_shape(rows);
     const int ncw = sh.nrg * sh.wt;
     const int nreg = (c.head_dim / 16) * sh.nt * 4;
@@ -425,12 +451,8 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     uint32_t smem_bytes = 0;
     if (use_umma) {
         // one consumer (the MMA issuer) takes every stage in order: any ring size
-        stages = kMaxStages;
-        while (stages >= 2 && umma_smem_bytes(c.head_dim, rows, stages) > (uint32_t)kSmemLimit)
-            --stages;
-        if (stages < 2)
-            return SHKV_ERR_UNSUPPORTED;
-        smem_bytes = umma_smem_bytes(c.head_dim, rows, stages);
+        stages = umma_stages(rows);
+        smem_bytes = umma_smem_bytes(rows, stages);
     } else {
         if (stages < 2 || stages < sh.wt)
             return SHKV_ERR_UNSUPPORTED;
@@ -467,10 +489,23 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     p.max_pages = c.max_pages_per_seq;
     p.num_pages = c.num_pages;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    cudaError_t e = use_umma ? launch_decode_umma(c.head_dim, pool->tm_k, pool->tm_v, p, smem_bytes, (cudaStream_t)stream)
+    cudaError_t e = use_umma ? launch_decode_umma(pool->tm_k2, pool->tm_v2, p, smem_bytes, (cudaStream_t)stream)
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);
     return cuda_status(e);
+}
+
+shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)
+{
+    if (!pool || !consumer || n_models < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    if (hq_per_model % pool->cfg.num_kv_heads)
+        return SHKV_ERR_UNSUPPORTED;
+    const int rows = n_models * (hq_per_model / pool->cfg.num_kv_heads);
+    if (rows > 64)
+        return SHKV_ERR_UNSUPPORTED;
+    *consumer = use_umma_consumer(rows, pool->cfg.head_dim) ? SHKV_CONSUMER_TCGEN05 : SHKV_CONSUMER_MMA_SYNC;
+    return SHKV_OK;
 }
 
 shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, int32_t head_dim, const float *o_part,

@@ -138,6 +138,12 @@ class SharedKVPool:
                                 _stream_ptr(stream))
         return (out, lse) if (return_lse or lse is not None) else out
 
+    def decode_consumer(self, n_models: int, hq: int) -> str:
+        """'tcgen05' or 'mma.sync': the consumer kernel decode_attention runs
+        for this shape under the current environment."""
+        c = N.shkv_decode_consumer(self.handle, n_models, hq)
+        return "tcgen05" if c == N.SHKV_CONSUMER_TCGEN05 else "mma.sync"
+
     def check_errors(self, stream=None) -> int:
         """Synchronize and return (then clear) the device error bits."""
         return N.shkv_check_errors(self.handle, _stream_ptr(stream))

@@ -157,9 +157,11 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
  *            so it can be reused.  Calls sharing one workspace must not
  *            overlap on the GPU.
  * Two interchangeable consumers implement the same result: warp-level
- * mma.sync tiles (the default) and tcgen05 tensor-memory tiles; setting the
- * environment variable SHKV_DECODE_CONSUMER to "mma" or "umma" selects one
- * (read on every call).
+ * mma.sync tiles and, for head_dim 128, tcgen05 tiles with the accumulators
+ * in tensor memory (tokens along the MMA's M dimension, 128-token stages).
+ * shkv_decode_consumer() reports which one a call runs; setting the
+ * environment variable SHKV_DECODE_CONSUMER to "mma" or "umma" overrides the
+ * automatic choice where the shape allows it (read on every call).
  * Supported: batch in [1, SHKV_MAX_BATCH], every L_b >= 1,
  * hq_per_model % num_kv_heads == 0, rows per KV head
  * n_models * hq_per_model / num_kv_heads <= 64.
@@ -170,6 +172,21 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                                   int32_t hq_per_model, const void *q, float scale, void *out,
                                   float *lse_out, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/* Consumer kernels of shkv_decode_attention. */
+#define SHKV_CONSUMER_MMA_SYNC 0
+#define SHKV_CONSUMER_TCGEN05 1
+
+/*
+ * Which consumer shkv_decode_attention would run on this pool for n_models
+ * decoders of hq_per_model query heads, given the environment as it is now:
+ * *consumer = SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05.  Host-only; no
+ * device work.  Errors: SHKV_ERR_INVALID_ARG (null pointers, counts < 1),
+ * SHKV_ERR_UNSUPPORTED (hq_per_model % num_kv_heads != 0 or more than 64
+ * rows per KV head).
+ */
+shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model,
+                                 int32_t *consumer);
 
 /*
  * Log-sum-exp merge of split-KV partials (the flash-decoding reduction for
