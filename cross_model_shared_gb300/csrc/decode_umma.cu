@@ -19,16 +19,21 @@
 // dominated by one token returns that token's V unchanged); P_lo = p -
 // bf16(p) (also bf16) adds the rounding residue for the log-sum-exp, which
 // is then accurate to fp32 rather than to the bf16 rounding of P.
-// Roles (192 threads):
+// Roles (224 threads):
 //
 //   warps 0-3  softmax: thread t owns token t of the stage and all R of its
 //              scores; it writes its rows of P^T and P_lo^T (bf16) over the
 //              stage's two K halves, which the QK MMA no longer needs.  At a
 //              segment end thread d reads column d of O^T and the row sums.
-//   warp 4     MMA issuer (one lane): QK of stage k, then PV of stage k-1.
+//   warp 4     QK issuer (one lane): S^T of each stage as soon as its data
+//              has landed and an S buffer is free.
 //   warp 5     producer: TMA of each page's K and V halves (one copy per
 //              lane) into a ring of 64 KiB stages, and bulk copies of the
 //              query rows of the next segment.
+//   warp 6     PV issuer (one lane): O^T and the row sums of each stage as
+//              soon as its P is written; its completion frees the ring slot.
+//              (tcgen05.commit tracks the issuing thread's MMAs, so the two
+//              issuers' commits are independent.)
 //
 // The running max m[r] is shared by all 128 tokens of a stage (O^T column r
 // collects all of them), and it is refreshed lazily: every stage the four
@@ -54,9 +59,10 @@ constexpr int kD = 128;                     // head dim (O^T's M)
 constexpr int kHalves = kD / 64;            // 128-byte swizzle spans per row
 constexpr int kSoftmaxWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kMmaWarp = 4;
+constexpr int kQkWarp = 4;
 constexpr int kProducerWarp = 5;
-constexpr int kTcThreads = 192;
+constexpr int kPvWarp = 6;
+constexpr int kTcThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;               // S^T buffers at columns 0 and 64
 constexpr uint32_t kColO = 128;             // O^T
@@ -96,10 +102,10 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
     u.qbuf_bytes = align_up((uint32_t)(rows * kD * 2), 128);
     u.red = u.qbuf + u.qbuf_bytes;
     u.rowoff = u.red + (uint32_t)((kSoftmaxWarps + 2) * 64 * 4);
-    // full[stages], empty[stages], qfull, qempty, s_full[2], s_free[2],
-    // p_full[2], q_ready, q_tile_free, fin
+    // full[stages], empty[stages], p_full[stages], qfull, qempty, s_full[2],
+    // s_free[2], q_ready, q_tile_free, fin
     u.bars = align_up(u.rowoff + 64u * 4u, 8);
-    u.meta = u.bars + (uint32_t)((2 * stages + 11) * 8);
+    u.meta = u.bars + (uint32_t)((3 * stages + 9) * 8);
     u.misc = u.meta + (uint32_t)(stages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
@@ -119,14 +125,16 @@ struct TcCtx {
 __device__ __forceinline__ uint32_t bar_at(const TcCtx &c, int i) { return c.base + c.lay.bars + 8u * i; }
 __device__ __forceinline__ uint32_t full_b(const TcCtx &c, int s) { return bar_at(c, s); }
 __device__ __forceinline__ uint32_t empty_b(const TcCtx &c, int s) { return bar_at(c, c.stages + s); }
-__device__ __forceinline__ uint32_t qfull_b(const TcCtx &c) { return bar_at(c, 2 * c.stages); }
-__device__ __forceinline__ uint32_t qempty_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 1); }
-__device__ __forceinline__ uint32_t s_full_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 2 + b); }
-__device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 4 + b); }
-__device__ __forceinline__ uint32_t p_full_b(const TcCtx &c, int b) { return bar_at(c, 2 * c.stages + 6 + b); }
-__device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 8); }
-__device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 9); }
-__device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 2 * c.stages + 10); }
+// P of the stage in ring slot s is written (one phase per occupancy of the
+// slot: the softmax reaches the slot's next stage only after PV freed it).
+__device__ __forceinline__ uint32_t p_full_b(const TcCtx &c, int s) { return bar_at(c, 2 * c.stages + s); }
+__device__ __forceinline__ uint32_t qfull_b(const TcCtx &c) { return bar_at(c, 3 * c.stages); }
+__device__ __forceinline__ uint32_t qempty_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 1); }
+__device__ __forceinline__ uint32_t s_full_b(const TcCtx &c, int b) { return bar_at(c, 3 * c.stages + 2 + b); }
+__device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar_at(c, 3 * c.stages + 4 + b); }
+__device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 6); }
+__device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 7); }
+__device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 8); }
 __device__ __forceinline__ uint32_t slot_addr(const TcCtx &c, int slot)
 {
     return c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
@@ -262,53 +270,22 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one lane)
+// MMA issuers (one lane each)
 // ---------------------------------------------------------------------------
 template <int NR>
-__device__ void tc_mma(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
+__device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
-    constexpr int NPV = tc_npv(NR);
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_qk = umma_idesc_bf16(128, NR, false, false);
-    const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
-    const uint32_t idesc_l = umma_idesc_bf16(128, NPV, false, true);
     const uint32_t qtile = c.base + c.lay.qtile;
-    const uint64_t ones = umma_sdesc_noswz(c.base + c.lay.ones, 128u, 256u);
     bool alive = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (alive)
             alive = mbar_wait_bounded(bar, parity, c.abort_flag, p.err);
         return alive;
     };
-
-    // O^T += V^T P^T, L += 1 P^T and Llo += 1 P_lo^T for stage k; P^T and
-    // P_lo^T sit over the two halves of the stage's K tile.
-    auto pv = [&](int k, bool first) {
-        const int buf = k & 1;
-        const int slot = k % stages;
-        if (wait(p_full_b(c, buf), (uint32_t)((k >> 1) & 1))) {
-            tc_fence_after();
-            const uint32_t kst = slot_addr(c, slot);
-            const uint32_t vst = kst + (uint32_t)(kTT * kD * 2);
-#pragma unroll
-            for (int ks = 0; ks < kTT / 16; ++ks) {
-                const uint64_t ad = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                const uint64_t bl =
-                    umma_sdesc_sw128(kst + (uint32_t)(kTT * 128) + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                const uint32_t acc = (first && ks == 0) ? 0u : 1u;
-                umma_bf16(tmem + kColO, ad, bd, idesc_pv, acc);
-                umma_bf16(tmem + kColL, ones, bd, idesc_l, acc);
-                umma_bf16(tmem + kColLlo, ones, bl, idesc_l, acc);
-            }
-        }
-        umma_commit(empty_b(c, slot));
-    };
-
     int kbase = 0, seg = 0;
-    int pend = -1;
-    bool pend_first = false;
     Segment s = locate(p, c.cta_begin, c.cta_end);
     for (;;) {
         const int nst = (s.p1 * P - s.p0 * P + kTT - 1) / kTT;
@@ -337,10 +314,6 @@ __device__ void tc_mma(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             umma_commit(s_full_b(c, buf));
             if (j == nst - 1)
                 umma_commit(q_tile_free_b(c));
-            if (pend >= 0)
-                pv(pend, pend_first);
-            pend = k;
-            pend_first = (j == 0);
         }
         kbase += nst;
         ++seg;
@@ -348,9 +321,55 @@ __device__ void tc_mma(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             break;
         s = next_segment(p, s, c.cta_end);
     }
-    if (pend >= 0)
-        pv(pend, pend_first);
-    // every MMA issued above has completed once this arrives
+    // every MMA this thread issued has completed once fin's phase ends
+    umma_commit(fin_b(c));
+    mbar_drain_bounded(fin_b(c), 0u);
+}
+
+// O^T += V^T P^T, L += 1 P^T and Llo += 1 P_lo^T for each stage; P^T and
+// P_lo^T sit over the two halves of the stage's K tile.
+template <int NR>
+__device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
+{
+    constexpr int NPV = tc_npv(NR);
+    const int stages = c.stages;
+    const int P = p.page_size;
+    const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
+    const uint32_t idesc_l = umma_idesc_bf16(128, NPV, false, true);
+    const uint64_t ones = umma_sdesc_noswz(c.base + c.lay.ones, 128u, 256u);
+    bool alive = true;
+    int kbase = 0;
+    Segment s = locate(p, c.cta_begin, c.cta_end);
+    for (;;) {
+        const int nst = (s.p1 * P - s.p0 * P + kTT - 1) / kTT;
+        for (int j = 0; j < nst; ++j) {
+            const int k = kbase + j;
+            const int slot = k % stages;
+            if (alive)
+                alive = mbar_wait_bounded(p_full_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
+            if (alive) {
+                tc_fence_after();
+                const uint32_t kst = slot_addr(c, slot);
+                const uint32_t vst = kst + (uint32_t)(kTT * kD * 2);
+#pragma unroll
+                for (int ks = 0; ks < kTT / 16; ++ks) {
+                    const uint64_t ad = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
+                    const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
+                    const uint64_t bl = umma_sdesc_sw128(kst + (uint32_t)(kTT * 128) + (uint32_t)ks * 2048u,
+                                                         (uint32_t)(kTT * 128), 1024u);
+                    const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
+                    umma_bf16(tmem + kColO, ad, bd, idesc_pv, acc);
+                    umma_bf16(tmem + kColL, ones, bd, idesc_l, acc);
+                    umma_bf16(tmem + kColLlo, ones, bl, idesc_l, acc);
+                }
+            }
+            umma_commit(empty_b(c, slot));
+        }
+        kbase += nst;
+        if (s.seg_end >= c.cta_end)
+            break;
+        s = next_segment(p, s, c.cta_end);
+    }
     umma_commit(fin_b(c));
     mbar_drain_bounded(fin_b(c), 0u);
 }
@@ -539,7 +558,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(p_full_b(c, buf));
+                mbar_arrive(p_full_b(c, slot));
         }
 
         // --- next segment's query rows, as soon as the last QK of this one is done
@@ -687,17 +706,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int s = 0; s < c.stages; ++s) {
             mbar_init(full_b(c, s), 1);
             mbar_init(empty_b(c, s), 1);                     // one tcgen05.commit per stage
+            mbar_init(p_full_b(c, s), kSoftmaxWarps);
         }
         mbar_init(qfull_b(c), 1);
         mbar_init(qempty_b(c), kSoftmaxWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full_b(c, i), 1);
             mbar_init(s_free_b(c, i), kSoftmaxWarps);
-            mbar_init(p_full_b(c, i), kSoftmaxWarps);
         }
         mbar_init(q_ready_b(c), kSoftmaxWarps);
         mbar_init(q_tile_free_b(c), 1);
-        mbar_init(fin_b(c), 1);
+        mbar_init(fin_b(c), 2);                              // one commit per MMA issuer
         *c.abort_flag = 0u;
         *c.bcast = 0u;
         fence_barrier_init();
@@ -725,9 +744,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kProducerWarp)
         tc_producer(&tmK, &tmV, p, c);
-    else if (warp == kMmaWarp) {
+    else if (warp == kQkWarp) {
         if ((threadIdx.x & 31) == 0)
-            tc_mma<NR>(p, c, tmem);
+            tc_qk<NR>(p, c, tmem);
+    } else if (warp == kPvWarp) {
+        if ((threadIdx.x & 31) == 0)
+            tc_pv<NR>(p, c, tmem);
     } else
         tc_softmax<NR>(p, c, tmem);
 
