@@ -10,36 +10,35 @@
 //
 //   S^T[t, r]  = sum_d K[t, d] Q[r, d]        M = 128 tokens,  N = rows
 //   O^T[d, r] += sum_t V[t, d] P^T[t, r]      M = 128 = D,     N = rows
-//   L[., r]   += sum_t 1 * P^T[t, r]          (a ones operand: row sums)
-//   Llo[., r] += sum_t 1 * P_lo^T[t, r]
 //
-// so a TMEM lane is one token of S^T, or one head-dim column of O^T, and
-// every lane of L holds all R row sums.  P is rounded to bf16 for the MMAs
-// and O is normalised by the sums of those same rounded weights (so a row
-// dominated by one token returns that token's V unchanged); P_lo = p -
-// bf16(p) (also bf16) adds the rounding residue for the log-sum-exp, which
-// is then accurate to fp32 rather than to the bf16 rounding of P.
-// Roles (224 threads):
+// so a TMEM lane is one token of S^T, or one head-dim column of O^T.  P is
+// rounded to bf16 for the PV MMA; O is normalised by the sum of those same
+// rounded weights (a row dominated by one token returns that token's V
+// unchanged), and the log-sum-exp uses the fp32 sum of the unrounded ones.
+// Roles (352 threads):
 //
-//   warps 0-3  softmax: thread t owns token t of the stage and all R of its
-//              scores; it writes its rows of P^T and P_lo^T (bf16) over the
-//              stage's two K halves, which the QK MMA no longer needs.  At a
-//              segment end thread d reads column d of O^T and the row sums.
-//   warp 4     QK issuer (one lane): S^T of each stage as soon as its data
+//   warps 0-7  softmax: warp w owns tokens 32*(w%4) .. +31 of each stage
+//              (the TMEM lanes its sub-partition can reach) and half w/4 of
+//              the stacked rows; each thread keeps fp32 row sums for its
+//              token, reduced across the CTA at a segment end.  P^T (bf16)
+//              is written over the stage's K tile, which the QK MMA no
+//              longer needs.  At a segment end the same split reads O^T.
+//   warp 8     QK issuer (one lane): S^T of each stage as soon as its data
 //              has landed and an S buffer is free.
-//   warp 5     producer: TMA of each page's K and V halves (one copy per
+//   warp 9     producer: TMA of each page's K and V halves (one copy per
 //              lane) into a ring of 64 KiB stages, and bulk copies of the
 //              query rows of the next segment.
-//   warp 6     PV issuer (one lane): O^T and the row sums of each stage as
-//              soon as its P is written; its completion frees the ring slot.
-//              (tcgen05.commit tracks the issuing thread's MMAs, so the two
-//              issuers' commits are independent.)
+//   warp 10    PV issuer (one lane): O^T of each stage as soon as its P is
+//              written; its completion frees the ring slot.  (tcgen05.commit
+//              tracks the issuing thread's MMAs, so the two issuers'
+//              commits are independent.)
 //
 // The running max m[r] is shared by all 128 tokens of a stage (O^T column r
-// collects all of them), and it is refreshed lazily: every stage the four
+// collects all of them), and it is refreshed lazily: every stage the eight
 // warps vote, in one bar.red, whether any score exceeds m[r] + kRescaleLog2.
-// Only then do they reduce the stage max across the CTA, rescale O^T and L
-// in TMEM and move m.  Unscaled exponentials stay below 2^kRescaleLog2.
+// Only then do they reduce the stage max across the CTA, rescale O^T in TMEM
+// and the row sums in registers, and move m.  Unscaled exponentials stay
+// below 2^kRescaleLog2.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,38 +56,40 @@ using namespace detail;
 constexpr int kTT = 128;                    // tokens per stage (the MMA's M)
 constexpr int kD = 128;                     // head dim (O^T's M)
 constexpr int kHalves = kD / 64;            // 128-byte swizzle spans per row
-constexpr int kSoftmaxWarps = 4;
+constexpr int kTokenGroups = 4;             // 32-lane TMEM sub-partitions
+constexpr int kSoftmaxWarps = 8;            // token group x row half
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kQkWarp = 4;
-constexpr int kProducerWarp = 5;
-constexpr int kPvWarp = 6;
-constexpr int kTcThreads = 224;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kQkWarp = 8;
+constexpr int kProducerWarp = 9;
+constexpr int kPvWarp = 10;
+constexpr int kTcThreads = 352;
+constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;               // S^T buffers at columns 0 and 64
 constexpr uint32_t kColO = 128;             // O^T
-constexpr uint32_t kColL = 192;             // row sums of the bf16 weights
-constexpr uint32_t kColLlo = 256;           // row sums of their rounding residues
 constexpr float kRescaleLog2 = 10.f;
-constexpr uint32_t kOnesBytes = 4096;       // 128 x 16 bf16 ones, no swizzle
 constexpr int kTcMaxStages = 4;
+// scratch rows of 64 floats: stage maxima [token group], new max, rescale
+// factor, row-sum partials [token group] (rounded and exact), running max,
+// the two row sums
+constexpr int kScrMax = 0, kScrNew = 4, kScrAlpha = 5, kScrLhi = 6, kScrLex = 10, kScrM = 14, kScrSumHi = 15,
+              kScrSumEx = 16, kScrRows = 17;
 
-static_assert(kTT == kSoftmaxThreads, "one softmax thread per token of a stage");
-static_assert(kD == kSoftmaxThreads, "one softmax thread per column of O^T");
+static_assert(kTT == 32 * kTokenGroups, "one softmax thread per token of a stage and row half");
+static_assert(kD == 32 * kTokenGroups, "one softmax thread per column of O^T and row half");
 
 // Padded row count N of the MMAs for R stacked rows.
 __host__ __device__ constexpr int tc_nr(int rows) { return (rows + 15) / 16 * 16; }
-// N of the PV MMAs: 48 is rounded up to a whole 64-column swizzle span.
+// N of the PV MMA: 48 is rounded up to a whole 64-column swizzle span.
 __host__ __device__ constexpr int tc_npv(int nr) { return nr == 48 ? 64 : nr; }
 
 struct TcSmem {
-    uint32_t ring, stage_bytes, qtile, qhalf, ones, qbuf, qbuf_bytes, red, rowoff, bars, meta, misc, tslot, total;
+    uint32_t ring, stage_bytes, qtile, qhalf, qbuf, qbuf_bytes, scr, rowoff, bars, meta, misc, tslot, total;
 };
 
 // Ring of `stages` slots of [K | V][half][128 tokens][128 B] (both 128-byte
-// swizzled), the Q tile [half][NR rows][128 B] (swizzled, K-major), the ones
-// tile, one staging buffer of the next segment's query rows, the cross-warp
-// max scratch (four warps' maxima, new max, rescale factor; 64 columns
-// each) and the row-offset table, then the barriers.
+// swizzled), the Q tile [half][NR rows][128 B] (swizzled, K-major), one
+// staging buffer of the next segment's query rows, the cross-warp scratch
+// and the row-offset table, then the barriers.
 __host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
 {
     TcSmem u;
@@ -97,11 +98,10 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
     u.ring = 0;
     u.qhalf = (uint32_t)nr * 128u;
     u.qtile = u.ring + (uint32_t)stages * u.stage_bytes;
-    u.ones = u.qtile + (uint32_t)kHalves * u.qhalf;
-    u.qbuf = u.ones + kOnesBytes;
+    u.qbuf = u.qtile + (uint32_t)kHalves * u.qhalf;
     u.qbuf_bytes = align_up((uint32_t)(rows * kD * 2), 128);
-    u.red = u.qbuf + u.qbuf_bytes;
-    u.rowoff = u.red + (uint32_t)((kSoftmaxWarps + 2) * 64 * 4);
+    u.scr = u.qbuf + u.qbuf_bytes;
+    u.rowoff = u.scr + (uint32_t)(kScrRows * 64 * 4);
     // full[stages], empty[stages], p_full[stages], qfull, qempty, s_full[2],
     // s_free[2], q_ready, q_tile_free, fin
     u.bars = align_up(u.rowoff + 64u * 4u, 8);
@@ -140,14 +140,29 @@ __device__ __forceinline__ uint32_t slot_addr(const TcCtx &c, int slot)
     return c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
 }
 
-// N consecutive TMEM columns (N a multiple of 16) of this warp's lanes.
+// A softmax thread's rows: 8-row chunks alternate between the two row
+// halves, so element i of half hh is stacked row 16*(i/8) + 8*hh + i%8, and
+// every TMEM access is 8 columns at a multiple of 8.
+__device__ __forceinline__ int half_row(int hh, int i) { return ((i >> 3) << 4) + (hh << 3) + (i & 7); }
+
+// This thread's N columns (N a multiple of 8) of a TMEM region starting at
+// column `taddr`, as N/8 chunks of 8 at a stride of 16 from `taddr + 8*hh`.
 template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N])
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, int hh, uint32_t (&r)[N])
 {
 #pragma unroll
-    for (int c = 0; c < N / 16; ++c)
-        tmem_ld16_nowait(taddr + 16u * c, r + 16 * c);
+    for (int c = 0; c < N / 8; ++c)
+        tmem_ld8_nowait(taddr + (uint32_t)(16 * c + 8 * hh), r + 8 * c);
     tmem_wait_ld();
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_half(uint32_t taddr, int hh, const uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c)
+        tmem_st8_nowait(taddr + (uint32_t)(16 * c + 8 * hh), r + 8 * c);
+    tmem_wait_st();
 }
 
 // ---------------------------------------------------------------------------
@@ -326,8 +341,7 @@ __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     mbar_drain_bounded(fin_b(c), 0u);
 }
 
-// O^T += V^T P^T, L += 1 P^T and Llo += 1 P_lo^T for each stage; P^T and
-// P_lo^T sit over the two halves of the stage's K tile.
+// O^T += V^T P^T for each stage; P^T sits over the stage's K tile (half 0).
 template <int NR>
 __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
@@ -335,8 +349,6 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
-    const uint32_t idesc_l = umma_idesc_bf16(128, NPV, false, true);
-    const uint64_t ones = umma_sdesc_noswz(c.base + c.lay.ones, 128u, 256u);
     bool alive = true;
     int kbase = 0;
     Segment s = locate(p, c.cta_begin, c.cta_end);
@@ -355,12 +367,7 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 for (int ks = 0; ks < kTT / 16; ++ks) {
                     const uint64_t ad = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
                     const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                    const uint64_t bl = umma_sdesc_sw128(kst + (uint32_t)(kTT * 128) + (uint32_t)ks * 2048u,
-                                                         (uint32_t)(kTT * 128), 1024u);
-                    const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
-                    umma_bf16(tmem + kColO, ad, bd, idesc_pv, acc);
-                    umma_bf16(tmem + kColL, ones, bd, idesc_l, acc);
-                    umma_bf16(tmem + kColLlo, ones, bl, idesc_l, acc);
+                    umma_bf16(tmem + kColO, ad, bd, idesc_pv, (j == 0 && ks == 0) ? 0u : 1u);
                 }
             }
             umma_commit(empty_b(c, slot));
@@ -375,22 +382,27 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 }
 
 // ---------------------------------------------------------------------------
-// softmax warps (thread = token of the stage; = column of O^T at a segment end)
+// softmax warps
 // ---------------------------------------------------------------------------
+// Thread (warp w, lane l): token / O^T column t = 32*(w%4) + l, and the
+// stacked rows half_row(w/4, i) for i < NR/2.
 template <int NR>
 __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
-    const int t = threadIdx.x;
-    const int warp = t >> 5;
-    const int lane = t & 31;
+    constexpr int NH = NR / 2;                 // rows per thread
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tg = warp & (kTokenGroups - 1);
+    const int hh = warp / kTokenGroups;
+    const int t = tg * 32 + lane;
     const int stages = c.stages;
     const int P = p.page_size;
     const int R = p.rows;
     const int log2P = 31 - __clz(P);
     const float sl2 = p.scale_log2;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(tg * 32) << 16;
     const volatile uint32_t *meta = reinterpret_cast<const volatile uint32_t *>(c.smem + c.lay.meta);
-    float *red = reinterpret_cast<float *>(c.smem + c.lay.red);
+    float *scr = reinterpret_cast<float *>(c.smem + c.lay.scr);
     const int *rowoff = reinterpret_cast<const int *>(c.smem + c.lay.rowoff);
     bool alive = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -406,7 +418,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
         wait(qfull_b(c), (uint32_t)(sg & 1));
         if (alive) {
             const uint8_t *src = c.smem + c.lay.qbuf;
-            for (int e = t; e < R * (kD / 8); e += kSoftmaxThreads) {
+            for (int e = threadIdx.x; e < R * (kD / 8); e += kSoftmaxThreads) {
                 const int rr = e >> 4, ch = e & 15;
                 const uint4 v = *reinterpret_cast<const uint4 *>(src + rr * (kD * 2) + ch * 16);
                 const uint32_t off = (uint32_t)(ch >> 3) * c.lay.qhalf + (uint32_t)rr * 128u +
@@ -430,24 +442,27 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
         const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
         const int L = plan_len(p, s);
         const int lim = L < tok_end ? L : tok_end;
-        float m_use[NR];
+        float m_use[NH], lhi[NH], lex[NH];
 #pragma unroll
-        for (int r = 0; r < NR; ++r)
-            m_use[r] = -INFINITY;
+        for (int i = 0; i < NH; ++i) {
+            m_use[i] = -INFINITY;
+            lhi[i] = 0.f;
+            lex[i] = 0.f;
+        }
 
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int buf = k & 1;
             const int slot = k % stages;
-            // --- this token's scores for all stacked rows
-            uint32_t sv[NR];
+            // --- this token's scores for this thread's rows
+            uint32_t sv[NH];
             if (wait(s_full_b(c, buf), (uint32_t)((k >> 1) & 1))) {
                 tc_fence_after();
-                tmem_ld_cols<NR>(tmem + lane_base + kColS + (uint32_t)(buf * 64), sv);
+                tmem_ld_half<NH>(tmem + lane_base + kColS + (uint32_t)(buf * 64), hh, sv);
             } else {
 #pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    sv[r] = 0u;
+                for (int i = 0; i < NH; ++i)
+                    sv[i] = 0u;
             }
             tc_fence_before();
             __syncwarp();
@@ -467,91 +482,88 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) && (tok0 + t < lim);
             const uint32_t kst = c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
             if (alive && !valid) {
-                // this token's V row may hold stale or non-finite bits: zero it
-                const uint32_t vrow = c.base + kst + (uint32_t)(kTT * kD * 2) + (uint32_t)t * 128u;
+                // this token's V row (this warp's column half) may hold stale
+                // or non-finite bits: zero it
+                const uint32_t vrow =
+                    c.base + kst + (uint32_t)(kTT * kD * 2) + (uint32_t)(hh * kTT * 128) + (uint32_t)t * 128u;
 #pragma unroll
-                for (int h = 0; h < kHalves; ++h)
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_zero16(vrow + (uint32_t)(h * kTT * 128 + ch * 16));
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_zero16(vrow + (uint32_t)(ch * 16));
             }
-            float xs[NR];
+            float xs[NH];
             bool need = false;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                xs[r] = valid ? __uint_as_float(sv[r]) * sl2 : -INFINITY;
-                need = need || (xs[r] > m_use[r] + kRescaleLog2);
+            for (int i = 0; i < NH; ++i) {
+                xs[i] = valid ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
+                need = need || (xs[i] > m_use[i] + kRescaleLog2);
             }
-            // --- lazy max refresh: the four warps agree on a new m[] together
+            // --- lazy max refresh: the eight warps agree on a new m[] together
             if (bar_red_or(1, kSoftmaxThreads, need)) {
-                float *red_m = red + kSoftmaxWarps * 64;      // new max per column
-                float *red_a = red_m + 64;                    // rescale factor per column
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    float v = xs[r];
+                for (int i = 0; i < NH; ++i) {
+                    float v = xs[i];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1)
                         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
                     if (lane == 0)
-                        red[warp * 64 + r] = v;
+                        scr[(kScrMax + tg) * 64 + half_row(hh, i)] = v;
                 }
                 named_barrier(1, kSoftmaxThreads);
-                if (t < NR) {
-                    float mo = -INFINITY;
+                if (threadIdx.x < NR) {
+                    const int r = threadIdx.x;
+                    const float mo = scr[kScrM * 64 + r];
+                    float mn = mo;
 #pragma unroll
-                    for (int r = 0; r < NR; ++r)
-                        mo = r == t ? m_use[r] : mo;
-                    const float mn = fmaxf(fmaxf(mo, fmaxf(red[t], red[64 + t])), fmaxf(red[128 + t], red[192 + t]));
-                    red_m[t] = mn;
-                    red_a[t] = mn == -INFINITY ? 1.f : ex2_approx(mo - mn);
+                    for (int g = 0; g < kTokenGroups; ++g)
+                        mn = fmaxf(mn, scr[(kScrMax + g) * 64 + r]);
+                    scr[kScrNew * 64 + r] = mn;
+                    scr[kScrAlpha * 64 + r] = mn == -INFINITY ? 1.f : ex2_approx(mo - mn);
+                    scr[kScrM * 64 + r] = mn;
                 }
                 named_barrier(1, kSoftmaxThreads);
+                const float *alpha = scr + kScrAlpha * 64;
                 if (j >= 1) {
-                    // O^T, L and Llo hold stages up to k-1: rescale them once PV(k-1) is done
+                    // O^T holds stages up to k-1: rescale this thread's part once PV(k-1) is done
                     const int kp = k - 1;
                     wait(empty_b(c, kp % stages), (uint32_t)((kp / stages) & 1));
                     if (alive) {
                         tc_fence_after();
+                        uint32_t ov[NH];
+                        tmem_ld_half<NH>(tmem + lane_base + kColO, hh, ov);
 #pragma unroll
-                        for (int part = 0; part < 3; ++part) {
-                            const uint32_t col = tmem + lane_base + (part == 0 ? kColO : part == 1 ? kColL : kColLlo);
-#pragma unroll
-                            for (int c16 = 0; c16 < NR / 16; ++c16) {
-                                uint32_t v[16];
-                                tmem_ld16_nowait(col + 16u * c16, v);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 16; ++e)
-                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * red_a[c16 * 16 + e]);
-                                tmem_st16_nowait(col + 16u * c16, v);
-                            }
-                        }
-                        tmem_wait_st();
+                        for (int i = 0; i < NH; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[half_row(hh, i)]);
+                        tmem_st_half<NH>(tmem + lane_base + kColO, hh, ov);
                     }
                 }
 #pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    m_use[r] = red_m[r];
+                for (int i = 0; i < NH; ++i) {
+                    m_use[i] = scr[kScrNew * 64 + half_row(hh, i)];
+                    lhi[i] *= alpha[half_row(hh, i)];
+                    lex[i] *= alpha[half_row(hh, i)];
+                }
             }
-            // --- this token's rows of P^T and P_lo^T, over the stage's K halves
+            // --- this token's part of P^T, over the stage's K tile (half 0)
             uint8_t *prow = c.smem + kst + (uint32_t)t * 128u;
 #pragma unroll
-            for (int ch = 0; ch < NR / 8; ++ch) {
-                uint32_t hi[4], lo[4];
+            for (int ch = 0; ch < NH / 8; ++ch) {
+                uint32_t hi[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int r = ch * 8 + 2 * e;
-                    const float mu0 = m_use[r] == -INFINITY ? 0.f : m_use[r];
-                    const float mu1 = m_use[r + 1] == -INFINITY ? 0.f : m_use[r + 1];
-                    const float p0 = ex2_approx(xs[r] - mu0);
-                    const float p1 = ex2_approx(xs[r + 1] - mu1);
+                    const int i = ch * 8 + 2 * e;
+                    const float mu0 = m_use[i] == -INFINITY ? 0.f : m_use[i];
+                    const float mu1 = m_use[i + 1] == -INFINITY ? 0.f : m_use[i + 1];
+                    const float p0 = ex2_approx(xs[i] - mu0);
+                    const float p1 = ex2_approx(xs[i + 1] - mu1);
                     hi[e] = pack_bf16x2(p0, p1);
-                    lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16), p1 - __uint_as_float(hi[e] & 0xffff0000u));
+                    lex[i] += p0;
+                    lex[i + 1] += p1;
+                    lhi[i] += __uint_as_float(hi[e] << 16);
+                    lhi[i + 1] += __uint_as_float(hi[e] & 0xffff0000u);
                 }
                 if (alive) {
-                    const uint32_t sw = (uint32_t)((ch ^ (t & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(prow + kTT * 128 + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    const int gch = 2 * ch + hh;
+                    *reinterpret_cast<uint4 *>(prow + ((gch ^ (t & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -568,62 +580,79 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             stage_q(seg + 1);
         }
 
-        // --- segment end: column d = t of O^T, normalised by the row sums
-        const int last = kbase + nst - 1;
-        wait(empty_b(c, last % stages), (uint32_t)((last / stages) & 1));
-        if (alive)
-            tc_fence_after();
+        // --- segment end: row sums across the 128 tokens, log-sum-exp
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+            float a = lhi[i], b = lex[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, o);
+                b += __shfl_xor_sync(0xffffffffu, b, o);
+            }
+            if (lane == 0) {
+                scr[(kScrLhi + tg) * 64 + half_row(hh, i)] = a;
+                scr[(kScrLex + tg) * 64 + half_row(hh, i)] = b;
+            }
+        }
+        named_barrier(1, kSoftmaxThreads);
         const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
         const int slot_id = whole ? 0 : 2 * (int)blockIdx.x + (s.seg_begin == c.cta_begin ? 0 : 1);
         const int64_t row0 = (int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group;
-        float my_m = -INFINITY, my_l = 0.f;
+        if (threadIdx.x < NR) {
+            const int r = threadIdx.x;
+            float a = 0.f, b = 0.f;
 #pragma unroll
-        for (int c16 = 0; c16 < NR / 16; ++c16) {
-            uint32_t ov[16], lv[16], llo[16];
-            if (alive) {
-                tmem_ld16_nowait(tmem + lane_base + kColO + 16u * c16, ov);
-                tmem_ld16_nowait(tmem + lane_base + kColL + 16u * c16, lv);
-                tmem_ld16_nowait(tmem + lane_base + kColLlo + 16u * c16, llo);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = c16 * 16 + e;
-                    const float l = __uint_as_float(lv[e]);
-                    if (r == t) {
-                        my_m = m_use[r];
-                        my_l = l + __uint_as_float(llo[e]);
-                    }
-                    if (r < R) {
-                        const float o = __uint_as_float(ov[e]) * (l > 0.f ? __frcp_rn(l) : 0.f);
-                        if (whole)
-                            p.out[(row0 + rowoff[r]) * kD + t] = __float2bfloat16_rn(o);
-                        else
-                            p.ws_part[((int64_t)slot_id * R + r) * kD + t] = o;
-                    }
-                }
+            for (int g = 0; g < kTokenGroups; ++g) {
+                a += scr[(kScrLhi + g) * 64 + r];
+                b += scr[(kScrLex + g) * 64 + r];
             }
-        }
-        tc_fence_before();
-        if (alive && t < R) {
-            const float lse = my_l > 0.f ? (my_m + log2f(my_l)) * kLn2 : -INFINITY;
-            if (whole) {
-                if (p.lse_out)
-                    p.lse_out[row0 + rowoff[t]] = lse;
-            } else {
-                p.ws_lse[(int64_t)slot_id * R + t] = lse;
+            scr[kScrSumHi * 64 + r] = a;
+            const float m = scr[kScrM * 64 + r];
+            scr[kScrM * 64 + r] = -INFINITY;        // the next segment starts afresh
+            if (alive && r < R) {
+                const float lse = b > 0.f ? (m + log2f(b)) * kLn2 : -INFINITY;
+                if (whole) {
+                    if (p.lse_out)
+                        p.lse_out[row0 + rowoff[r]] = lse;
+                } else {
+                    p.ws_lse[(int64_t)slot_id * R + r] = lse;
+                }
             }
         }
         named_barrier(1, kSoftmaxThreads);
 
+        // --- column d = t of O^T for this thread's rows, normalised
+        const int last = kbase + nst - 1;
+        wait(empty_b(c, last % stages), (uint32_t)((last / stages) & 1));
+        if (alive) {
+            tc_fence_after();
+            uint32_t ov[NH];
+            tmem_ld_half<NH>(tmem + lane_base + kColO, hh, ov);
+#pragma unroll
+            for (int i = 0; i < NH; ++i) {
+                const int r = half_row(hh, i);
+                if (r < R) {
+                    const float l = scr[kScrSumHi * 64 + r];
+                    const float o = __uint_as_float(ov[i]) * (l > 0.f ? __frcp_rn(l) : 0.f);
+                    if (whole)
+                        p.out[(row0 + rowoff[r]) * kD + t] = __float2bfloat16_rn(o);
+                    else
+                        p.ws_part[((int64_t)slot_id * R + r) * kD + t] = o;
+                }
+            }
+        }
+        tc_fence_before();
+        named_barrier(1, kSoftmaxThreads);
+
         // --- split unit: the last piece to arrive merges all pieces
         if (!whole) {
-            const int c0 = cta_of(p, s.unit_begin);
-            const int c1 = cta_of(p, s.unit_end - 1);
+            const int cb = cta_of(p, s.unit_begin);
+            const int ce = cta_of(p, s.unit_end - 1);
             uint32_t *counter = p.ws_count + (int64_t)s.b * p.hkv + s.g;
-            if (t == 0) {
+            if (threadIdx.x == 0) {
                 __threadfence();
                 const uint32_t prev = atomicAdd(counter, 1u);
-                *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
+                *c.bcast = (prev == (uint32_t)(ce - cb)) ? 1u : 0u;
             }
             named_barrier(1, kSoftmaxThreads);
             if (*c.bcast) {
@@ -631,7 +660,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 const int dq = kD / 4;
                 for (int rr = warp; rr < R; rr += kSoftmaxWarps) {
                     float M = -INFINITY;
-                    for (int cc = c0 + lane; cc <= c1; cc += 32)
+                    for (int cc = cb + lane; cc <= ce; cc += 32)
                         M = fmaxf(M, __ldcg(p.ws_lse + (int64_t)piece_slot(p, cc, s.unit_begin) * R + rr));
 #pragma unroll
                     for (int o_ = 16; o_ > 0; o_ >>= 1)
@@ -639,7 +668,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     float wsum = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (M != -INFINITY) {
-                        for (int cc = c0; cc <= c1; ++cc) {
+                        for (int cc = cb; cc <= ce; ++cc) {
                             const int sl = piece_slot(p, cc, s.unit_begin);
                             const float w = ex2_approx((__ldcg(p.ws_lse + (int64_t)sl * R + rr) - M) *
                                                        1.4426950408889634f);
@@ -665,7 +694,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     if (lane == 0 && p.lse_out)
                         p.lse_out[orr] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
                 }
-                if (t == 0)
+                if (threadIdx.x == 0)
                     *counter = 0u;
             }
             named_barrier(1, kSoftmaxThreads);
@@ -681,6 +710,8 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 
 }  // namespace
 
+// 11 warps at one CTA per SM: three warps share a 16K-register SM
+// sub-partition, so at most 168 registers a thread.
 template <int NR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     shkv_decode_umma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -722,14 +753,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_barrier_init();
     }
     if (warp < kSoftmaxWarps) {
-        // ones operand, zeroed Q tile (its padding rows stay zero), row offsets
-        const uint32_t one2 = 0x3F803F80u;   // two bf16 1.0
-        for (uint32_t i = threadIdx.x; i < kOnesBytes / 16; i += kSoftmaxThreads)
-            *reinterpret_cast<uint4 *>(c.smem + c.lay.ones + 16 * i) = make_uint4(one2, one2, one2, one2);
+        // zeroed Q tile (its padding rows stay zero), running maxima, row offsets
         for (uint32_t i = threadIdx.x; i < (uint32_t)kHalves * c.lay.qhalf / 16; i += kSoftmaxThreads)
             *reinterpret_cast<uint4 *>(c.smem + c.lay.qtile + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
         if (threadIdx.x < 64) {
             const int r = threadIdx.x;
+            reinterpret_cast<float *>(c.smem + c.lay.scr)[kScrM * 64 + r] = -INFINITY;
             const int m = r / p.group, jj = r - (r / p.group) * p.group;
             reinterpret_cast<int *>(c.smem + c.lay.rowoff)[r] = m * p.hq + jj;
         }
