@@ -39,7 +39,15 @@ METRIC = "shared-KV decode attention: KV GB/s (% of HBM peak) and decode steps/s
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-KERNEL_SOURCES = ["cross_model_shared_gb300/csrc/decode_attn.cu", "cross_model_shared_gb300/csrc/shkv_device.cuh"]
+# The decode kernel each consumer runs, the source files that define it, and
+# the stem of its committed ncu summaries under profiles/.
+_CSRC = "cross_model_shared_gb300/csrc/"
+KERNELS = {
+    "mma.sync": {"name": "shkv_decode_kernel", "stem": "decode_attn",
+                 "sources": [_CSRC + "decode_attn.cu", _CSRC + "decode_common.cuh", _CSRC + "shkv_device.cuh"]},
+    "tcgen05": {"name": "shkv_decode_umma_kernel", "stem": "decode_umma",
+                "sources": [_CSRC + "decode_umma.cu", _CSRC + "decode_common.cuh", _CSRC + "shkv_device.cuh"]},
+}
 
 
 # ---------------------------------------------------------------------------
@@ -82,18 +90,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha() -> str:
+def kernel_sha(consumer: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNELS[consumer]["sources"]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_attn_{config}_traffic.txt")
+def profiled_traffic(consumer: str, config: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{KERNELS[consumer]['stem']}_{config}_traffic.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -101,7 +109,7 @@ def profiled_traffic(config: str):
                 if ":" in line and not line.lstrip().startswith("#"):
                     k, _, v = line.partition(":")
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha") != kernel_sha():
+        if kv.get("kernel_source_sha") != kernel_sha(consumer):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -403,7 +411,8 @@ def run_gpu(args):
                "seconds": round(secs, 2)}
 
     peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic(wl.name)
+    consumer = pool.decode_consumer(wl.N, wl.Hq)
+    traffic = profiled_traffic(consumer, wl.name)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -420,7 +429,8 @@ def run_gpu(args):
             "decoder_tokens_per_s": wl.B * wl.N * 1e3 / ms_per_step,
             "pct_of_hbm_peak": {"measured_copy": 100 * per_gpu / peak, "nominal_8tbs": 100 * per_gpu / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
-                         "frac": per_gpu / peak, "peak_kind": peak_kind, "traffic": traffic},
+                         "frac": per_gpu / peak, "peak_kind": peak_kind, "traffic": traffic,
+                         "kernel": KERNELS[consumer]["name"], "consumer": consumer},
             "unshared": {"ms_per_step": unshared_ms, "launches_per_step": wl.N,
                          "speedup_of_sharing": unshared_ms / ms_per_step},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": qbytes, "d2h_bytes_per_step": qbytes,

@@ -15,7 +15,7 @@
 // rounded to bf16 for the PV MMA; O is normalised by the sum of those same
 // rounded weights (a row dominated by one token returns that token's V
 // unchanged), and the log-sum-exp uses the fp32 sum of the unrounded ones.
-// Roles (352 threads):
+// Roles (384 threads):
 //
 //   warps 0-7  softmax: warp w owns tokens 32*(w%4) .. +31 of each stage
 //              (the TMEM lanes its sub-partition can reach) and half w/4 of
@@ -25,13 +25,15 @@
 //              longer needs.  At a segment end the same split reads O^T.
 //   warp 8     QK issuer (one lane): S^T of each stage as soon as its data
 //              has landed and an S buffer is free.
-//   warp 9     producer: TMA of each page's K and V halves (one copy per
-//              lane) into a ring of 64 KiB stages, and bulk copies of the
-//              query rows of the next segment.
+//   warp 9     K producer: TMA of each page's two K column halves (one copy
+//              per lane) into a ring of 64 KiB stages, the query rows of the
+//              next segment, and the validity word of each stage; for
+//              32-token pages also the V halves.
 //   warp 10    PV issuer (one lane): O^T of each stage as soon as its P is
 //              written; its completion frees the ring slot.  (tcgen05.commit
 //              tracks the issuing thread's MMAs, so the two issuers'
 //              commits are independent.)
+//   warp 11    V producer (16-token pages): TMA of each page's V halves.
 //
 // The running max m[r] is shared by all 128 tokens of a stage (O^T column r
 // collects all of them), and it is refreshed lazily: every stage the eight
@@ -62,7 +64,8 @@ constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kQkWarp = 8;
 constexpr int kProducerWarp = 9;
 constexpr int kPvWarp = 10;
-constexpr int kTcThreads = 352;
+constexpr int kVProducerWarp = 11;
+constexpr int kTcThreads = 384;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;               // S^T buffers at columns 0 and 64
 constexpr uint32_t kColO = 128;             // O^T
@@ -102,10 +105,10 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
     u.qbuf_bytes = align_up((uint32_t)(rows * kD * 2), 128);
     u.scr = u.qbuf + u.qbuf_bytes;
     u.rowoff = u.scr + (uint32_t)(kScrRows * 64 * 4);
-    // full[stages], empty[stages], p_full[stages], qfull, qempty, s_full[2],
-    // s_free[2], q_ready, q_tile_free, fin
+    // full_k[stages], empty[stages], p_full[stages], full_v[stages], qfull,
+    // qempty, s_full[2], s_free[2], q_ready, q_tile_free, fin
     u.bars = align_up(u.rowoff + 64u * 4u, 8);
-    u.meta = u.bars + (uint32_t)((3 * stages + 9) * 8);
+    u.meta = u.bars + (uint32_t)((4 * stages + 9) * 8);
     u.misc = u.meta + (uint32_t)(stages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
@@ -123,18 +126,20 @@ struct TcCtx {
 };
 
 __device__ __forceinline__ uint32_t bar_at(const TcCtx &c, int i) { return c.base + c.lay.bars + 8u * i; }
+// K (and the validity word) / V of the stage in ring slot s have landed.
 __device__ __forceinline__ uint32_t full_b(const TcCtx &c, int s) { return bar_at(c, s); }
+__device__ __forceinline__ uint32_t full_v_b(const TcCtx &c, int s) { return bar_at(c, 3 * c.stages + s); }
 __device__ __forceinline__ uint32_t empty_b(const TcCtx &c, int s) { return bar_at(c, c.stages + s); }
 // P of the stage in ring slot s is written (one phase per occupancy of the
 // slot: the softmax reaches the slot's next stage only after PV freed it).
 __device__ __forceinline__ uint32_t p_full_b(const TcCtx &c, int s) { return bar_at(c, 2 * c.stages + s); }
-__device__ __forceinline__ uint32_t qfull_b(const TcCtx &c) { return bar_at(c, 3 * c.stages); }
-__device__ __forceinline__ uint32_t qempty_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 1); }
-__device__ __forceinline__ uint32_t s_full_b(const TcCtx &c, int b) { return bar_at(c, 3 * c.stages + 2 + b); }
-__device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar_at(c, 3 * c.stages + 4 + b); }
-__device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 6); }
-__device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 7); }
-__device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 3 * c.stages + 8); }
+__device__ __forceinline__ uint32_t qfull_b(const TcCtx &c) { return bar_at(c, 4 * c.stages); }
+__device__ __forceinline__ uint32_t qempty_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 1); }
+__device__ __forceinline__ uint32_t s_full_b(const TcCtx &c, int b) { return bar_at(c, 4 * c.stages + 2 + b); }
+__device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar_at(c, 4 * c.stages + 4 + b); }
+__device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 6); }
+__device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 7); }
+__device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 8); }
 __device__ __forceinline__ uint32_t slot_addr(const TcCtx &c, int slot)
 {
     return c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
@@ -166,24 +171,36 @@ __device__ __forceinline__ void tmem_st_half(uint32_t taddr, int hh, const uint3
 }
 
 // ---------------------------------------------------------------------------
-// producer warp
+// producer warps
 // ---------------------------------------------------------------------------
-// Stage j of a segment is the 128 tokens from p0*P + j*128: 128/P pages,
-// each copied as 2 (K, V) x 2 (column halves) boxes of P rows x 128 bytes,
-// one box per lane.  Stage layout [K | V][half][token][128 B].
-__device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,
-                            const TcCtx &c)
+// Stage j of a segment is the 128 tokens from p0*P + j*128, i.e. 128/P
+// pages.  Each page's two column halves of K and of V are copied with 2-D
+// boxes of P rows x 128 B into [K | V][half][token][128 B] (the QK MMA reads
+// 128 tokens of one half of K at a uniform stride, the PV MMA the same of V),
+// one box per lane; K and V complete on separate full barriers, so QK starts
+// as soon as K has landed.  With split_producers (16-token pages: 16 copies
+// of each per stage) the K warp copies K, the query rows and the validity
+// word while the V warp copies V; otherwise (8 of each) the K warp issues
+// all of them, K first, and the V warp has nothing to do (measured faster).
+template <bool kIsK>
+__device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p, const TcCtx &c)
 {
     const int lane = threadIdx.x & 31;
     const int stages = c.stages;
     const int P = p.page_size;
     const int RB = kTT / P;                              // pages per stage (4 or 8)
     const int log2P = 31 - __clz(P);
-    const int my_kv = lane / (kHalves * RB);
-    const int my_h = (lane / RB) % kHalves;
-    const int my_rb = lane % RB;
-    const bool copier = lane < 2 * kHalves * RB;
-    const uint32_t page_bytes = 2u * kHalves * (uint32_t)P * 128u;   // K and V of one page
+    const bool split = p.split_producers != 0;
+    if (!kIsK && !split)
+        return;
+    // lane -> (tensor, half, page): K lanes first, then V lanes when one warp copies both
+    const int per_tensor = kHalves * RB;
+    const bool my_v = kIsK ? lane >= per_tensor : true;
+    const int cl = (my_v && kIsK) ? lane - per_tensor : lane;
+    const int my_h = cl / RB;
+    const int my_rb = cl % RB;
+    const bool copier = kIsK ? (lane < (split ? per_tensor : 2 * per_tensor)) : lane < per_tensor;
+    const uint32_t page_bytes = kHalves * (uint32_t)P * 128u;   // K or V of one page
     const uint64_t pol = l2_evict_first_policy();
     if (lane == 0) {
         prefetch_tensormap(tmK);
@@ -204,22 +221,25 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
             sn = next_segment(p, s, c.cta_end);
             pre_next = (lane < sn.p1) ? __ldg(p.block_table + (int64_t)sn.b * p.max_pages + lane) : -1;
         }
-        const int dev_len = (lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
+        const int dev_len = (kIsK && lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
         // --- query rows of this (b, g): N bulk copies of G contiguous rows
-        if (alive) {
-            bool ok = mbar_wait_bounded(qempty_b(c), (uint32_t)((seg & 1) ^ 1), c.abort_flag, p.err);
-            alive = __all_sync(0xffffffffu, ok);
+        if (kIsK) {
+            if (alive) {
+                bool ok = mbar_wait_bounded(qempty_b(c), (uint32_t)((seg & 1) ^ 1), c.abort_flag, p.err);
+                alive = __all_sync(0xffffffffu, ok);
+            }
+            if (alive && lane == 0) {
+                const uint32_t rows_bytes = (uint32_t)p.group * kD * 2u;
+                mbar_arrive_expect_tx(qfull_b(c), rows_bytes * p.n_models);
+                const __nv_bfloat16 *qsrc =
+                    p.q + ((int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group) * kD;
+                const uint32_t qdst = c.base + c.lay.qbuf;
+                for (int m = 0; m < p.n_models; ++m)
+                    bulk_load(qdst + m * rows_bytes, qsrc + (int64_t)m * p.hq * kD, rows_bytes, qfull_b(c));
+                q_issued = seg;
+            }
         }
-        if (alive && lane == 0) {
-            const uint32_t rows_bytes = (uint32_t)p.group * kD * 2u;
-            mbar_arrive_expect_tx(qfull_b(c), rows_bytes * p.n_models);
-            const __nv_bfloat16 *qsrc = p.q + ((int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group) * kD;
-            const uint32_t qdst = c.base + c.lay.qbuf;
-            for (int m = 0; m < p.n_models; ++m)
-                bulk_load(qdst + m * rows_bytes, qsrc + (int64_t)m * p.hq * kD, rows_bytes, qfull_b(c));
-            q_issued = seg;
-        }
-        // --- K/V pages of the segment
+        // --- K or V pages of the segment
         const int tok_end = s.p1 * P;
         const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
         const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
@@ -244,27 +264,32 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                 ok = mbar_wait_bounded(empty_b(c, slot), (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
             alive = alive && __all_sync(0xffffffffu, ok);
             const bool my_valid = copier && my_tok < tok_end && my_id >= 0 && my_id < p.num_pages;
-            // lanes 0..RB-1 copy the K half-0 boxes: their ballot is the page mask
+            // lanes 0..RB-1 copy page rb = lane (half 0 for K): their ballot is the page mask
             const uint32_t mask = __ballot_sync(0xffffffffu, my_valid) & ((1u << RB) - 1u);
             if (alive && lane == 0) {
-                for (int rb = 0; rb < RB; ++rb)
-                    if (!((mask >> rb) & 1u) && tok0 + rb * P < tok_end)
-                        atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
-                volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
-                meta[slot] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
-                mbar_arrive_expect_tx(full_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
+                if (kIsK) {
+                    for (int rb = 0; rb < RB; ++rb)
+                        if (!((mask >> rb) & 1u) && tok0 + rb * P < tok_end)
+                            atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
+                    volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
+                    meta[slot] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
+                    mbar_arrive_expect_tx(full_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
+                }
+                if (!kIsK || !split)
+                    mbar_arrive_expect_tx(full_v_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
             }
             __syncwarp();
             if (alive && my_valid) {
-                const uint32_t dst = slot_addr(c, slot) + (uint32_t)my_kv * (kTT * kD * 2) +
+                const uint32_t dst = slot_addr(c, slot) + (my_v ? (uint32_t)(kTT * kD * 2) : 0u) +
                                      (uint32_t)my_h * (kTT * 128) + (uint32_t)my_rb * (uint32_t)P * 128u;
-                tma_load_2d(dst, my_kv ? tmV : tmK, my_h * 64, (my_id * p.hkv + s.g) * P, full_b(c, slot), pol);
+                tma_load_2d(dst, my_v ? tmV : tmK, my_h * 64, (my_id * p.hkv + s.g) * P,
+                            my_v ? full_v_b(c, slot) : full_b(c, slot), pol);
             }
             if (alive)
                 last_issued_stage = k;
             __syncwarp();
         }
-        if (lane == 0 && dev_len != plan_len(p, s))
+        if (kIsK && lane == 0 && dev_len != plan_len(p, s))
             atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
         kbase += nst;
         ++seg;
@@ -273,12 +298,16 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
         s = sn;
         pre = pre_next;
     }
-    // After an abort, wait (bounded) for every copy still in flight so no TMA
+    // After an abort, wait (bounded) for the copies still in flight so no TMA
     // write lands after the CTA exits.
     if (!alive && lane == 0) {
         for (int k = last_issued_stage - stages + 1; k <= last_issued_stage; ++k)
-            if (k >= 0)
-                mbar_drain_bounded(full_b(c, k % stages), (uint32_t)((k / stages) & 1));
+            if (k >= 0) {
+                if (kIsK)
+                    mbar_drain_bounded(full_b(c, k % stages), (uint32_t)((k / stages) & 1));
+                if (!kIsK || !split)
+                    mbar_drain_bounded(full_v_b(c, k % stages), (uint32_t)((k / stages) & 1));
+            }
         if (q_issued >= 0)
             mbar_drain_bounded(qfull_b(c), (uint32_t)(q_issued & 1));
     }
@@ -359,6 +388,8 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             const int slot = k % stages;
             if (alive)
                 alive = mbar_wait_bounded(p_full_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
+            if (alive)
+                alive = mbar_wait_bounded(full_v_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
                 const uint32_t kst = slot_addr(c, slot);
@@ -481,6 +512,10 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             const int tok0 = s.p0 * P + j * kTT;
             const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) && (tok0 + t < lim);
             const uint32_t kst = c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+            // rows past the length inside a copied page are written by the V
+            // copy: zero them only after it has landed
+            if (__any_sync(0xffffffffu, alive && !valid))
+                wait(full_v_b(c, slot), (uint32_t)((k / stages) & 1));
             if (alive && !valid) {
                 // this token's V row (this warp's column half) may hold stale
                 // or non-finite bits: zero it
@@ -710,7 +745,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 
 }  // namespace
 
-// 11 warps at one CTA per SM: three warps share a 16K-register SM
+// 12 warps at one CTA per SM: three warps share a 16K-register SM
 // sub-partition, so at most 168 registers a thread.
 template <int NR>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -736,6 +771,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; ++s) {
             mbar_init(full_b(c, s), 1);
+            mbar_init(full_v_b(c, s), 1);
             mbar_init(empty_b(c, s), 1);                     // one tcgen05.commit per stage
             mbar_init(p_full_b(c, s), kSoftmaxWarps);
         }
@@ -772,7 +808,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.tslot);
 
     if (warp == kProducerWarp)
-        tc_producer(&tmK, &tmV, p, c);
+        tc_producer<true>(&tmK, &tmV, p, c);
+    else if (warp == kVProducerWarp)
+        tc_producer<false>(&tmK, &tmV, p, c);
     else if (warp == kQkWarp) {
         if ((threadIdx.x & 31) == 0)
             tc_qk<NR>(p, c, tmem);
@@ -815,7 +853,7 @@ static cudaError_t launch_umma_t(const CUtensorMap &tmK, const CUtensorMap &tmV,
     return cudaGetLastError();
 }
 
-// tmK/tmV: 2-D maps of the pool (128-byte swizzle, box of 64 columns x P rows).
+// tmK, tmV: 2-D maps of the pools (box of 64 columns x P rows, 128-byte swizzle).
 cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p, uint32_t smem,
                                cudaStream_t stream)
 {

@@ -78,7 +78,7 @@ constexpr int kWtMax = cmax(cmax(cmax(SHKV_WT_NT1, kNt1MultiWarps / 2), SHKV_WT_
 // consumer (up to 64 rows); below it the mma.sync consumer runs.  The
 // environment variable SHKV_DECODE_CONSUMER=mma|umma overrides the policy.
 #ifndef SHKV_UMMA_MIN_ROWS
-#define SHKV_UMMA_MIN_ROWS 65
+#define SHKV_UMMA_MIN_ROWS 25
 #endif
 constexpr int kUmmaMinRows = SHKV_UMMA_MIN_ROWS;
 constexpr int kUmmaMaxRows = 64;
@@ -108,7 +108,8 @@ struct DecodeParams {
     int32_t batch, n_models, hq, hkv, group, rows;   // rows = R = N*G per KV head
     int32_t nrg, wt, rpad, stages;                   // row groups, token warps per group
     int32_t page_size, box_rows, max_pages, num_pages;
-    int32_t num_ctas, pad0;
+    int32_t num_ctas;
+    int32_t split_producers;   // tcgen05 consumer: K and V copied by separate warps
     int64_t total_chunks;
     float scale_log2;
     float pad1;

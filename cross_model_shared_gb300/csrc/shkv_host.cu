@@ -489,6 +489,9 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     p.max_pages = c.max_pages_per_seq;
     p.num_pages = c.num_pages;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    // tcgen05 consumer: 16-token pages make 32 copies a stage, issued by two
+    // warps; the 16 copies of 32-token pages measured faster from one warp
+    p.split_producers = c.page_size < 32 ? 1 : 0;
     cudaError_t e = use_umma ? launch_decode_umma(pool->tm_k2, pool->tm_v2, p, smem_bytes, (cudaStream_t)stream)
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);

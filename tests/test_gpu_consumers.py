@@ -1,4 +1,4 @@
-"""The tcgen05 (tensor-memory) consumer against the fp64 oracle.
+"""The two decode consumers against the fp64 oracle.
 
 libshkv has two consumers for the same decode step: warp-level mma.sync
 tiles and, for head dim 128, tcgen05 tiles with tokens along the MMA's M
@@ -6,7 +6,9 @@ dimension and the accumulators in tensor memory.  SHKV_DECODE_CONSUMER
 selects one per call; these tests force the tcgen05 consumer on every row
 count class (padded N of 16, 32, 48 and 64; three- and two-stage rings;
 4 and 8 pages per 128-token stage), check that it is the one that ran, and
-compare with the oracle and with the invariants the definition fixes.
+compare with the oracle and with the invariants the definition fixes.  The
+automatic choice takes tcgen05 from 25 stacked rows up; the last tests
+force mma.sync there so both consumers stay covered at every row count.
 """
 import numpy as np
 import pytest
@@ -201,3 +203,49 @@ def test_umma_full_size_qwen14b_sampled(umma):
     picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
     for b, (ref, lref) in oracle_for_requests(wl, q, k_dev, v_dev, picks).items():
         compare(out[b], ref, lse[b], lref, what=f"umma qwen14b b={b}")
+
+
+# --------------------------------------------------------------------------
+# the mma.sync consumer where the automatic choice is tcgen05
+# --------------------------------------------------------------------------
+@pytest.fixture
+def mma(monkeypatch):
+    monkeypatch.setenv("SHKV_DECODE_CONSUMER", "mma")
+
+
+def test_automatic_choice_by_rows_and_head_dim(monkeypatch):
+    monkeypatch.delenv("SHKV_DECODE_CONSUMER", raising=False)
+    for shape, want in [("qwen14b", "tcgen05"), ("r24", "mma.sync"), ("r64", "tcgen05"), ("long", "mma.sync"),
+                        ("llama8b", "mma.sync")]:
+        sh = SHAPES[shape]
+        wl = W.custom_workload(shape, B=1, lens_prefill=[40], seed=1, **sh)
+        k, v = W.gen_pool(wl)
+        assert make_pool(wl, k, v).decode_consumer(wl.N, wl.Hq) == want, shape
+
+
+@pytest.mark.parametrize("shape", ["qwen14b", "r40_p16", "r64"])
+def test_mma_consumer_matches_oracle_for_many_rows(mma, shape):
+    lens = [1, 17, 129, 1000, 4100]
+    wl = W.custom_workload(shape, B=len(lens), lens_prefill=lens, seed=29, **SHAPES[shape])
+    q = W.gen_q(wl)
+    k, v = W.gen_pool(wl)
+    pool = make_pool(wl, k, v)
+    assert pool.decode_consumer(wl.N, wl.Hq) == "mma.sync"
+    out, lse = pool.decode_attention(bits_to_torch(q), wl.N, scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    ref, lref = oracle.decode_attention(q, k, v, wl.block_table, wl.lens_final, n_models=wl.N, hq=wl.Hq,
+                                        scale=wl.scale)
+    compare(out, ref, lse, lref, what=f"mma {shape}")
+
+
+def test_mma_long_single_request_split_and_merged(mma):
+    wl = W.custom_workload("split", B=1, N=8, Hq=40, Hkv=8, D=128, P=32, lens_prefill=[60000], seed=4)
+    q = W.gen_q(wl)
+    k, v = W.gen_pool(wl)
+    pool = make_pool(wl, k, v)
+    assert pool.decode_consumer(wl.N, wl.Hq) == "mma.sync"
+    out, lse = pool.decode_attention(bits_to_torch(q), wl.N, scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    ref, lref = oracle.decode_attention(q, k, v, wl.block_table, wl.lens_final, n_models=wl.N, hq=wl.Hq,
+                                        scale=wl.scale)
+    compare(out, ref, lse, lref, what="mma split")
