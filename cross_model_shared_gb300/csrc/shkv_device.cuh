@@ -78,7 +78,7 @@ constexpr int kWtMax = cmax(cmax(cmax(SHKV_WT_NT1, kNt1MultiWarps / 2), SHKV_WT_
 // consumer (up to 64 rows); below it the mma.sync consumer runs.  The
 // environment variable SHKV_DECODE_CONSUMER=mma|umma overrides the policy.
 #ifndef SHKV_UMMA_MIN_ROWS
-#define SHKV_UMMA_MIN_ROWS 25
+#define SHKV_UMMA_MIN_ROWS 16
 #endif
 constexpr int kUmmaMinRows = SHKV_UMMA_MIN_ROWS;
 constexpr int kUmmaMaxRows = 64;

@@ -7,7 +7,7 @@ selects one per call; these tests force the tcgen05 consumer on every row
 count class (padded N of 16, 32, 48 and 64; three- and two-stage rings;
 4 and 8 pages per 128-token stage), check that it is the one that ran, and
 compare with the oracle and with the invariants the definition fixes.  The
-automatic choice takes tcgen05 from 25 stacked rows up; the last tests
+automatic choice takes tcgen05 from 16 stacked rows up; the last tests
 force mma.sync there so both consumers stay covered at every row count.
 """
 import numpy as np
@@ -215,15 +215,15 @@ def mma(monkeypatch):
 
 def test_automatic_choice_by_rows_and_head_dim(monkeypatch):
     monkeypatch.delenv("SHKV_DECODE_CONSUMER", raising=False)
-    for shape, want in [("qwen14b", "tcgen05"), ("r24", "mma.sync"), ("r64", "tcgen05"), ("long", "mma.sync"),
-                        ("llama8b", "mma.sync")]:
+    for shape, want in [("qwen14b", "tcgen05"), ("r24", "tcgen05"), ("r64", "tcgen05"), ("long", "tcgen05"),
+                        ("llama8b", "mma.sync"), ("r1", "mma.sync")]:
         sh = SHAPES[shape]
         wl = W.custom_workload(shape, B=1, lens_prefill=[40], seed=1, **sh)
         k, v = W.gen_pool(wl)
         assert make_pool(wl, k, v).decode_consumer(wl.N, wl.Hq) == want, shape
 
 
-@pytest.mark.parametrize("shape", ["qwen14b", "r40_p16", "r64"])
+@pytest.mark.parametrize("shape", ["qwen14b", "r40_p16", "r64", "long", "r24"])
 def test_mma_consumer_matches_oracle_for_many_rows(mma, shape):
     lens = [1, 17, 129, 1000, 4100]
     wl = W.custom_workload(shape, B=len(lens), lens_prefill=lens, seed=29, **SHAPES[shape])
