@@ -73,7 +73,7 @@ constexpr float kRescaleLog2 = 10.f;
 constexpr int kTcMaxStages = 4;
 // scratch rows of 64 floats: stage maxima [token group], new max, rescale
 // factor, row-sum partials [token group] (rounded and exact), running max,
-// the two row sums
+// the reciprocal rounded-weight row sum, the exact row sum
 constexpr int kScrMax = 0, kScrNew = 4, kScrAlpha = 5, kScrLhi = 6, kScrLex = 10, kScrM = 14, kScrSumHi = 15,
               kScrSumEx = 16, kScrRows = 17;
 
@@ -169,6 +169,57 @@ __device__ __forceinline__ void tmem_st_half(uint32_t taddr, int hh, const uint3
         tmem_st8_nowait(taddr + (uint32_t)(16 * c + 8 * hh), r + 8 * c);
     tmem_wait_st();
 }
+
+// Warp reduce-scatter by recursive halving: at the butterfly step with lane
+// offset O a lane keeps half of its M values and combines it with the
+// partner's copy of that half.  Afterwards lane l holds in v[0 .. M/32 - 1]
+// (v[0] if M < 32) the warp totals of columns rs_base<M>(l) + j; for M < 32,
+// lanes that differ only in their low log2(32/M) bits hold the same column.
+// M/2 + M/4 + ... shuffles instead of 5*M for a butterfly per column.
+template <int M, int O, bool kMax>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int lane)
+    {
+        if constexpr (O > 0) {
+            if constexpr (M > 1) {
+                const bool up = (lane & O) != 0;
+#pragma unroll
+                for (int i = 0; i < M / 2; ++i) {
+                    const float send = up ? v[i] : v[i + M / 2];
+                    const float keep = up ? v[i + M / 2] : v[i];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, O);
+                    v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+                }
+                ReduceScatter<M / 2, O / 2, kMax>::run(v, lane);
+            } else {
+                const float recv = __shfl_xor_sync(0xffffffffu, v[0], O);
+                v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+                ReduceScatter<1, O / 2, kMax>::run(v, lane);
+            }
+        }
+    }
+};
+
+template <int M>
+__device__ __forceinline__ int rs_base(int lane)
+{
+    int base = 0, m = M;
+    for (int o = 16; o >= 1 && m > 1; o >>= 1) {
+        if (lane & o)
+            base += m / 2;
+        m /= 2;
+    }
+    return base;
+}
+
+// lanes that hold a distinct column after a reduce-scatter of M values
+template <int M>
+__device__ __forceinline__ bool rs_owner(int lane)
+{
+    return M >= 32 || (lane & (32 / M - 1)) == 0;
+}
+
+__host__ __device__ constexpr int pow2_at_least(int n) { return n <= 8 ? 8 : n <= 16 ? 16 : n <= 32 ? 32 : 64; }
 
 // ---------------------------------------------------------------------------
 // producer warps
@@ -534,14 +585,19 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             }
             // --- lazy max refresh: the eight warps agree on a new m[] together
             if (bar_red_or(1, kSoftmaxThreads, need)) {
+                {
+                    constexpr int M = pow2_at_least(NH);
+                    float v[M];
 #pragma unroll
-                for (int i = 0; i < NH; ++i) {
-                    float v = xs[i];
+                    for (int i = 0; i < M; ++i)
+                        v[i] = i < NH ? xs[i] : -INFINITY;
+                    ReduceScatter<M, 16, true>::run(v, lane);
+                    const int base = rs_base<M>(lane);
+                    if (rs_owner<M>(lane))
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == 0)
-                        scr[(kScrMax + tg) * 64 + half_row(hh, i)] = v;
+                        for (int j = 0; j < (M >= 32 ? M / 32 : 1); ++j)
+                            if (base + j < NH)
+                                scr[(kScrMax + tg) * 64 + half_row(hh, base + j)] = v[j];
                 }
                 named_barrier(1, kSoftmaxThreads);
                 if (threadIdx.x < NR) {
@@ -616,18 +672,23 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
         }
 
         // --- segment end: row sums across the 128 tokens, log-sum-exp
+        {
+            constexpr int M = pow2_at_least(2 * NH);
+            float v[M];
 #pragma unroll
-        for (int i = 0; i < NH; ++i) {
-            float a = lhi[i], b = lex[i];
+            for (int i = 0; i < M; ++i)
+                v[i] = i < NH ? lhi[i] : i < 2 * NH ? lex[i - NH] : 0.f;
+            ReduceScatter<M, 16, false>::run(v, lane);
+            const int base = rs_base<M>(lane);
+            if (rs_owner<M>(lane))
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, o);
-                b += __shfl_xor_sync(0xffffffffu, b, o);
-            }
-            if (lane == 0) {
-                scr[(kScrLhi + tg) * 64 + half_row(hh, i)] = a;
-                scr[(kScrLex + tg) * 64 + half_row(hh, i)] = b;
-            }
+                for (int j = 0; j < (M >= 32 ? M / 32 : 1); ++j) {
+                    const int col = base + j;
+                    if (col < NH)
+                        scr[(kScrLhi + tg) * 64 + half_row(hh, col)] = v[j];
+                    else if (col < 2 * NH)
+                        scr[(kScrLex + tg) * 64 + half_row(hh, col - NH)] = v[j];
+                }
         }
         named_barrier(1, kSoftmaxThreads);
         const bool whole = (s.seg_begin == s.unit_begin) && (s.seg_end == s.unit_end);
@@ -641,7 +702,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 a += scr[(kScrLhi + g) * 64 + r];
                 b += scr[(kScrLex + g) * 64 + r];
             }
-            scr[kScrSumHi * 64 + r] = a;
+            scr[kScrSumHi * 64 + r] = a > 0.f ? __frcp_rn(a) : 0.f;   // 1 / row sum, for O
             const float m = scr[kScrM * 64 + r];
             scr[kScrM * 64 + r] = -INFINITY;        // the next segment starts afresh
             if (alive && r < R) {
@@ -667,8 +728,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             for (int i = 0; i < NH; ++i) {
                 const int r = half_row(hh, i);
                 if (r < R) {
-                    const float l = scr[kScrSumHi * 64 + r];
-                    const float o = __uint_as_float(ov[i]) * (l > 0.f ? __frcp_rn(l) : 0.f);
+                    const float o = __uint_as_float(ov[i]) * scr[kScrSumHi * 64 + r];
                     if (whole)
                         p.out[(row0 + rowoff[r]) * kD + t] = __float2bfloat16_rn(o);
                     else
