@@ -87,7 +87,7 @@ constexpr int kMaxCtas = 256;
 // Fixed cost of one (request, head) segment in the split plan, in page
 // chunks: a CTA that crosses many short requests gets fewer chunks.
 #ifndef SHKV_SEGMENT_COST_CHUNKS
-#define SHKV_SEGMENT_COST_CHUNKS 32
+#define SHKV_SEGMENT_COST_CHUNKS 16
 #endif
 constexpr int kSegmentCostChunks = SHKV_SEGMENT_COST_CHUNKS;
 // Wall-clock limit for any single wait on an mbarrier.

@@ -50,7 +50,7 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.shkv_splitkv_merge(1, 1, 1, 6, 16, 16, 16, None, None) == N.SHKV_ERR_INVALID_ARG  # D % 4
 
 
-SEGMENT_COST = 32  # chunks charged per (request, head) segment by the planner
+SEGMENT_COST = 16  # chunks charged per (request, head) segment by the planner
 
 
 @pytest.mark.parametrize("lens,P,H,C", [
