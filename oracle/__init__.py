@@ -49,6 +49,9 @@ def _load():
                                                     ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_double, P, P, i]
             lib.oracle_decode_attention.restype = i
+            lib.oracle_decode_attention_tails.argtypes = [i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P,
+                                                          ctypes.c_double, P, P, i]
+            lib.oracle_decode_attention_tails.restype = i
             lib.oracle_splitkv_merge.argtypes = [i, i, i, i, P, P, P, P]
             lib.oracle_splitkv_merge.restype = i
             lib.oracle_append_kv.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P]
@@ -99,6 +102,39 @@ def decode_attention(q, k_pages, v_pages, block_table, seq_lens, *, n_models: in
                                          _ptr(lens), int(t_begin), int(t_end), float(scale),
                                          _ptr(out), _ptr(lse), int(nthreads))
     _check(st, "decode_attention")
+    return out, lse
+
+
+def decode_attention_tails(q, k_pages, v_pages, block_table, seq_lens, tail_table, tail_lens, *,
+                           n_models: int, hq: int, scale: float, nthreads: int = 0):
+    """Stacked decode where each decoder also attends its own unique tail.
+
+    Follows PrefillShare Sec. 3.3-4 (decode starts from the shared base cache
+    and extends it with the decoder's own Delta C_t; Eqs. 8-9 store the shared
+    prefix once and N unique tails).  Decoder m of request b attends the
+    concatenation of the shared tokens [0, L_b) and its tail tokens
+    [0, T_{b,m}).  ``tail_table`` is int32 [B, N, max_tail_pages] and
+    ``tail_lens`` int32 [B, N], into the same page pool.  Returns fp64
+    (out [B, N*Hq, D], lse [B, N*Hq]).
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    v_pages = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    tt = np.ascontiguousarray(tail_table, dtype=np.int32)
+    tl = np.ascontiguousarray(tail_lens, dtype=np.int32)
+    B, rows, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    assert D2 == D and rows == n_models * hq and bt.shape[0] >= B
+    assert tt.shape[:2] == (B, n_models) and tl.shape == (B, n_models)
+    out = np.zeros((B, rows, D), dtype=np.float64)
+    lse = np.zeros((B, rows), dtype=np.float64)
+    st = _load().oracle_decode_attention_tails(B, n_models, hq, Hkv, D, P, num_pages, bt.shape[1], tt.shape[2],
+                                               _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(bt), _ptr(lens),
+                                               _ptr(tt), _ptr(tl), float(scale), _ptr(out), _ptr(lse),
+                                               int(nthreads))
+    _check(st, "decode_attention_tails")
     return out, lse
 
 

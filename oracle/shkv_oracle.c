@@ -52,6 +52,80 @@ static double widen_bf16(uint16_t bits)
     return (double)f;
 }
 
+/* KV head of q head h (contiguous GQA); stacked row of decoder m, q head h
+ * (model-major); token slot t of (page, KV head g) in a [pages, Hkv, P, D]
+ * pool. */
+static int kv_head(int Hq, int Hkv, int h) { return h / (Hq / Hkv); }
+static long stacked_row(int N, int Hq, int m, int h)
+{
+    (void)N;
+    return (long)m * Hq + h;
+}
+static const uint16_t *page_slot(const uint16_t *pool, int Hkv, int P, int D, int32_t page, int g, int t)
+{
+    return pool + (((long)page * Hkv + g) * P + t % P) * (long)D;
+}
+
+/*
+ * Softmax attention of one query row over n tokens given by their K and V
+ * rows (the definition, two-pass, fp64):
+ *   s_i = scale * <q, K_i>,  p_i = exp(s_i - max s) / sum_j exp(s_j - max s),
+ *   o = sum_i p_i V_i,       lse = max s + ln sum_i exp(s_i - max s).
+ * n = 0 gives o = 0 and lse = -inf.  s is scratch of n doubles.
+ */
+static void softmax_attend(const uint16_t *q, int D, double scale, int n, const uint16_t *const *kt,
+                           const uint16_t *const *vt, double *s, double *o, double *lse)
+{
+    for (int k = 0; k < D; ++k)
+        o[k] = 0.0;
+    if (n <= 0) {
+        if (lse)
+            *lse = -INFINITY;
+        return;
+    }
+    double smax = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int k = 0; k < D; ++k)
+            acc += widen_bf16(q[k]) * widen_bf16(kt[i][k]);
+        s[i] = scale * acc;
+        if (s[i] > smax)
+            smax = s[i];
+    }
+    double denom = 0.0;
+    for (int i = 0; i < n; ++i)
+        denom += exp(s[i] - smax);
+    for (int i = 0; i < n; ++i) {
+        double p = exp(s[i] - smax) / denom;
+        for (int k = 0; k < D; ++k)
+            o[k] += p * widen_bf16(vt[i][k]);
+    }
+    if (lse)
+        *lse = smax + log(denom);
+}
+
+/* per-thread scratch: scores and the token list of one row */
+typedef struct {
+    double *s;
+    const uint16_t **kt, **vt;
+} row_scratch;
+
+static int scratch_alloc(row_scratch *sc, int max_len)
+{
+    size_t n = (size_t)(max_len > 0 ? max_len : 1);
+    sc->s = (double *)malloc(sizeof(double) * n);
+    sc->kt = (const uint16_t **)malloc(sizeof(uint16_t *) * n);
+    sc->vt = (const uint16_t **)malloc(sizeof(uint16_t *) * n);
+    return sc->s && sc->kt && sc->vt;
+}
+
+static void scratch_free(row_scratch *sc)
+{
+    free(sc->s);
+    free(sc->kt);
+    free(sc->vt);
+}
+
 typedef struct {
     int B, N, Hq, Hkv, D, P, num_pages, max_pages;
     const uint16_t *q, *k_pages, *v_pages;
@@ -73,7 +147,7 @@ static const uint16_t *token_ptr(const decode_job *j, const uint16_t *pool, int 
     int32_t page = j->block_table[(long)b * j->max_pages + t / j->P];
     if (page < 0 || page >= j->num_pages)
         return NULL;
-    return pool + (((long)page * j->Hkv + g) * j->P + t % j->P) * (long)j->D;
+    return page_slot(pool, j->Hkv, j->P, j->D, page, g, t);
 }
 
 /*
@@ -85,11 +159,10 @@ static const uint16_t *token_ptr(const decode_job *j, const uint16_t *pool, int 
  *   lse   = max s + ln sum_t exp(s_t - max s)
  * An empty token range gives o = 0 and lse = -inf.
  */
-static int attend_row(const decode_job *j, int b, int m, int h, double *s)
+static int attend_row(const decode_job *j, int b, int m, int h, row_scratch *sc)
 {
-    const int G = j->Hq / j->Hkv;
-    const int g = h / G;
-    const long r = (long)m * j->Hq + h;
+    const int g = kv_head(j->Hq, j->Hkv, h);
+    const long r = stacked_row(j->N, j->Hq, m, h);
     const long rows = (long)j->N * j->Hq;
     const uint16_t *q = j->q + ((long)b * rows + r) * j->D;
     double *o = j->out + ((long)b * rows + r) * j->D;
@@ -98,43 +171,14 @@ static int attend_row(const decode_job *j, int b, int m, int h, double *s)
     int L = j->seq_lens[b];
     int t0 = j->t_begin < 0 ? 0 : j->t_begin;
     int t1 = j->t_end < L ? j->t_end : L;
-    for (int k = 0; k < j->D; ++k)
-        o[k] = 0.0;
-    if (t1 <= t0) {
-        if (lse)
-            *lse = -INFINITY;
-        return ORACLE_OK;
-    }
-    int n = t1 - t0;
-
-    /* scores */
-    double smax = -INFINITY;
+    int n = t1 > t0 ? t1 - t0 : 0;
     for (int i = 0; i < n; ++i) {
-        const uint16_t *kt = token_ptr(j, j->k_pages, b, g, t0 + i);
-        if (!kt)
+        sc->kt[i] = token_ptr(j, j->k_pages, b, g, t0 + i);
+        sc->vt[i] = token_ptr(j, j->v_pages, b, g, t0 + i);
+        if (!sc->kt[i] || !sc->vt[i])
             return ORACLE_EPAGE;
-        double acc = 0.0;
-        for (int k = 0; k < j->D; ++k)
-            acc += widen_bf16(q[k]) * widen_bf16(kt[k]);
-        s[i] = j->scale * acc;
-        if (s[i] > smax)
-            smax = s[i];
     }
-    /* normaliser */
-    double denom = 0.0;
-    for (int i = 0; i < n; ++i)
-        denom += exp(s[i] - smax);
-    /* weighted values */
-    for (int i = 0; i < n; ++i) {
-        const uint16_t *vt = token_ptr(j, j->v_pages, b, g, t0 + i);
-        if (!vt)
-            return ORACLE_EPAGE;
-        double p = exp(s[i] - smax) / denom;
-        for (int k = 0; k < j->D; ++k)
-            o[k] += p * widen_bf16(vt[k]);
-    }
-    if (lse)
-        *lse = smax + log(denom);
+    softmax_attend(q, j->D, j->scale, n, sc->kt, sc->vt, sc->s, o, lse);
     return ORACLE_OK;
 }
 
@@ -145,8 +189,9 @@ static void *decode_worker(void *arg)
     for (int b = 0; b < j->B; ++b)
         if (j->seq_lens[b] > max_len)
             max_len = j->seq_lens[b];
-    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
-    if (!s) {
+    row_scratch sc;
+    if (!scratch_alloc(&sc, max_len)) {
+        scratch_free(&sc);
         pthread_mutex_lock(&j->lock);
         j->status = ORACLE_ENOMEM;
         pthread_mutex_unlock(&j->lock);
@@ -162,14 +207,14 @@ static void *decode_worker(void *arg)
             break;
         int b = (int)(idx / rows);
         int r = (int)(idx % rows);
-        int st = attend_row(j, b, r / j->Hq, r % j->Hq, s);
+        int st = attend_row(j, b, r / j->Hq, r % j->Hq, &sc);
         if (st != ORACLE_OK) {
             pthread_mutex_lock(&j->lock);
             j->status = st;
             pthread_mutex_unlock(&j->lock);
         }
     }
-    free(s);
+    scratch_free(&sc);
     return NULL;
 }
 
@@ -226,6 +271,153 @@ int oracle_decode_attention(int B, int N, int Hq, int Hkv, int D, int P, int num
         return ORACLE_ENOMEM;
     for (int i = 0; i < nt; ++i)
         pthread_create(&th[i], NULL, decode_worker, &j);
+    for (int i = 0; i < nt; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&j.lock);
+    return j.status;
+}
+
+/*
+ * Per-decoder unique tails (PrefillShare Sec. 3.3 and Sec. 4, Eqs. 8-9): a
+ * decoder starts from the shared base cache C_base and extends it with its
+ * own generated-token cache Delta C_t, so decoder m of request b attends the
+ * concatenation [shared prefix tokens 0 .. L_b) ++ [its tail tokens
+ * 0 .. T_{b,m}).  The shared prefix is stored once (L_shared); each decoder's
+ * tail is its own (N * L_unique).  Both live in the same page pool:
+ *
+ *   block_table      int32 [B, max_pages], seq_lens int32 [B]       (shared)
+ *   tail_table       int32 [B, N, max_tail_pages], tail_lens int32 [B, N]
+ *   out fp64 [B, N*Hq, D], lse fp64 [B, N*Hq] (nullable)
+ *
+ * Same definition as oracle_decode_attention over the concatenated token
+ * list: two-pass softmax in fp64.  An empty concatenation gives o = 0 and
+ * lse = -inf.
+ */
+typedef struct {
+    int B, N, Hq, Hkv, D, P, num_pages, max_pages, max_tail_pages;
+    const uint16_t *q, *k_pages, *v_pages;
+    const int32_t *block_table, *seq_lens, *tail_table, *tail_lens;
+    double scale;
+    double *out, *lse;
+    long next_row, total_rows;
+    int status;
+    pthread_mutex_t lock;
+} tails_job;
+
+/* token i of the concatenation for (b, m), KV head g; NULL for a bad page */
+static const uint16_t *concat_token(const tails_job *j, const uint16_t *pool, int b, int m, int g, int i)
+{
+    int L = j->seq_lens[b];
+    int32_t page;
+    int t;
+    if (i < L) {
+        t = i;
+        page = j->block_table[(long)b * j->max_pages + t / j->P];
+    } else {
+        t = i - L;
+        page = j->tail_table[((long)b * j->N + m) * j->max_tail_pages + t / j->P];
+    }
+    if (page < 0 || page >= j->num_pages)
+        return NULL;
+    return page_slot(pool, j->Hkv, j->P, j->D, page, g, t);
+}
+
+static int attend_row_tails(const tails_job *j, int b, int m, int h, row_scratch *sc)
+{
+    const int g = kv_head(j->Hq, j->Hkv, h);
+    const long r = stacked_row(j->N, j->Hq, m, h);
+    const long rows = (long)j->N * j->Hq;
+    const uint16_t *q = j->q + ((long)b * rows + r) * j->D;
+    double *o = j->out + ((long)b * rows + r) * j->D;
+    double *lse = j->lse ? j->lse + (long)b * rows + r : NULL;
+    const int n = j->seq_lens[b] + j->tail_lens[(long)b * j->N + m];
+    for (int i = 0; i < n; ++i) {
+        sc->kt[i] = concat_token(j, j->k_pages, b, m, g, i);
+        sc->vt[i] = concat_token(j, j->v_pages, b, m, g, i);
+        if (!sc->kt[i] || !sc->vt[i])
+            return ORACLE_EPAGE;
+    }
+    softmax_attend(q, j->D, j->scale, n, sc->kt, sc->vt, sc->s, o, lse);
+    return ORACLE_OK;
+}
+
+static void *tails_worker(void *arg)
+{
+    tails_job *j = (tails_job *)arg;
+    int max_len = 1;
+    for (int b = 0; b < j->B; ++b)
+        for (int m = 0; m < j->N; ++m) {
+            int n = j->seq_lens[b] + j->tail_lens[(long)b * j->N + m];
+            if (n > max_len)
+                max_len = n;
+        }
+    row_scratch sc;
+    if (!scratch_alloc(&sc, max_len)) {
+        scratch_free(&sc);
+        pthread_mutex_lock(&j->lock);
+        j->status = ORACLE_ENOMEM;
+        pthread_mutex_unlock(&j->lock);
+        return NULL;
+    }
+    const long rows = (long)j->N * j->Hq;
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        long idx = j->next_row++;
+        int stop = j->status != ORACLE_OK;
+        pthread_mutex_unlock(&j->lock);
+        if (stop || idx >= j->total_rows)
+            break;
+        int b = (int)(idx / rows);
+        int r = (int)(idx % rows);
+        int st = attend_row_tails(j, b, r / j->Hq, r % j->Hq, &sc);
+        if (st != ORACLE_OK) {
+            pthread_mutex_lock(&j->lock);
+            j->status = st;
+            pthread_mutex_unlock(&j->lock);
+        }
+    }
+    scratch_free(&sc);
+    return NULL;
+}
+
+int oracle_decode_attention_tails(int B, int N, int Hq, int Hkv, int D, int P, int num_pages,
+                                  int max_pages, int max_tail_pages, const uint16_t *q,
+                                  const uint16_t *k_pages, const uint16_t *v_pages,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  const int32_t *tail_table, const int32_t *tail_lens, double scale,
+                                  double *out, double *lse, int nthreads)
+{
+    if (B < 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || P <= 0 || !out)
+        return ORACLE_EARG;
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0 || seq_lens[b] > (long)max_pages * P)
+            return ORACLE_EARG;
+        for (int m = 0; m < N; ++m) {
+            int T = tail_lens[(long)b * N + m];
+            if (T < 0 || T > (long)max_tail_pages * P)
+                return ORACLE_EARG;
+        }
+    }
+    tails_job j;
+    memset(&j, 0, sizeof j);
+    j.B = B; j.N = N; j.Hq = Hq; j.Hkv = Hkv; j.D = D; j.P = P;
+    j.num_pages = num_pages; j.max_pages = max_pages; j.max_tail_pages = max_tail_pages;
+    j.q = q; j.k_pages = k_pages; j.v_pages = v_pages;
+    j.block_table = block_table; j.seq_lens = seq_lens;
+    j.tail_table = tail_table; j.tail_lens = tail_lens;
+    j.scale = scale; j.out = out; j.lse = lse;
+    j.total_rows = (long)B * N * Hq;
+    j.status = ORACLE_OK;
+    pthread_mutex_init(&j.lock, NULL);
+    int nt = resolve_threads(nthreads);
+    if (nt > j.total_rows)
+        nt = j.total_rows > 0 ? (int)j.total_rows : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!th)
+        return ORACLE_ENOMEM;
+    for (int i = 0; i < nt; ++i)
+        pthread_create(&th[i], NULL, tails_worker, &j);
     for (int i = 0; i < nt; ++i)
         pthread_join(th[i], NULL);
     free(th);

@@ -1,11 +1,13 @@
 """Planted mistakes: each mutant copy of the oracle's C source must fail at
-least one pin in test_oracle_pins.py.
+least one pin in test_oracle_pins.py or test_oracle_tails_pins.py.
 
 This checks that the pins are sharp enough to catch the plausible slips a
 hand-written attention oracle can make (wrong GQA head, swapped K/V, dropped
 scale or max, wrong row order, off-by-one mask, broken merge weight, wrong
-append slot).  Mutants are compiled on the CPU into a temporary directory;
-the real oracle is never modified.
+append slot; for per-decoder tails: another decoder's tail, the shared table
+used for the tail, a dropped tail, an un-rebased tail position).  Mutants
+are compiled on the CPU into a temporary directory; the real oracle is never
+modified.
 """
 import os
 import subprocess
@@ -14,25 +16,35 @@ import pytest
 
 import oracle
 import tests.test_oracle_pins as pins
+import tests.test_oracle_tails_pins as tail_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "shkv_oracle.c")
 
 MUTANTS = {
-    "gqa_head_modulo": ("const int g = h / G;", "const int g = h % j->Hkv;"),
+    "gqa_head_modulo": ("return h / (Hq / Hkv);", "return h % Hkv;"),
     "keys_as_values": ("token_ptr(j, j->v_pages, b, g, t0 + i)", "token_ptr(j, j->k_pages, b, g, t0 + i)"),
-    "no_scale": ("s[i] = j->scale * acc;", "s[i] = acc;"),
+    "no_scale": ("s[i] = scale * acc;", "s[i] = acc;"),
     "max_not_subtracted_in_numerator": ("double p = exp(s[i] - smax) / denom;", "double p = exp(s[i]) / denom;"),
-    "head_major_rows": ("const long r = (long)m * j->Hq + h;", "const long r = (long)h * j->N + m;"),
+    "head_major_rows": ("return (long)m * Hq + h;", "return (long)h * N + m;"),
     "mask_off_by_one": ("int t1 = j->t_end < L ? j->t_end : L;", "int t1 = j->t_end < L + 1 ? j->t_end : L + 1;"),
     "lse_without_log": ("*lse = smax + log(denom);", "*lse = smax + denom;"),
     "merge_weight_sign": ("double w = exp(l - M);", "double w = exp(M - l);"),
     "append_slot_shift": ("long dst = (((long)page * Hkv + g) * P + pos % P) * (long)D;",
                           "long dst = (((long)page * Hkv + g) * P + (pos + 1) % P) * (long)D;"),
-    "token_slot_shift": ("return pool + (((long)page * j->Hkv + g) * j->P + t % j->P) * (long)j->D;",
-                         "return pool + (((long)page * j->Hkv + g) * j->P + (t + 1) % j->P) * (long)j->D;"),
+    "token_slot_shift": ("return pool + (((long)page * Hkv + g) * P + t % P) * (long)D;",
+                         "return pool + (((long)page * Hkv + g) * P + (t + 1) % P) * (long)D;"),
+    # per-decoder unique tails
+    "tail_of_first_decoder": ("page = j->tail_table[((long)b * j->N + m) * j->max_tail_pages + t / j->P];",
+                              "page = j->tail_table[((long)b * j->N + 0) * j->max_tail_pages + t / j->P];"),
+    "tail_through_shared_table": ("page = j->tail_table[((long)b * j->N + m) * j->max_tail_pages + t / j->P];",
+                                  "page = j->block_table[(long)b * j->max_pages + t / j->P];"),
+    "tail_dropped": ("const int n = j->seq_lens[b] + j->tail_lens[(long)b * j->N + m];",
+                     "const int n = j->seq_lens[b];"),
+    "tail_position_not_rebased": ("t = i - L;", "t = i;"),
 }
 
-PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+PIN_TESTS = ([getattr(pins, n) for n in dir(pins) if n.startswith("test_")] +
+             [getattr(tail_pins, n) for n in dir(tail_pins) if n.startswith("test_")])
 
 
 @pytest.fixture(scope="module")
