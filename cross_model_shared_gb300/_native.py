@@ -32,7 +32,9 @@ EXPORTS = [
     "shkv_pool_create", "shkv_pool_destroy", "shkv_pool_set_seq_lens", "shkv_pool_get_seq_lens",
     "shkv_append_kv", "shkv_decode_workspace_size", "shkv_decode_attention", "shkv_splitkv_merge",
     "shkv_check_errors", "shkv_plan_decode", "shkv_status_string", "shkv_decode_attention_noalloc",
-    "shkv_decode_consumer",
+    "shkv_decode_consumer", "shkv_tails_create", "shkv_tails_destroy", "shkv_tails_set_lens",
+    "shkv_tails_get_lens", "shkv_tails_append", "shkv_decode_tails_workspace_size",
+    "shkv_decode_attention_tails",
 ]
 
 SHKV_CONSUMER_MMA_SYNC = 0
@@ -55,6 +57,17 @@ class shkv_pool_config(ctypes.Structure):
         ("seq_lens", ctypes.c_void_p),
         ("error_word", ctypes.c_void_p),
         ("initial_seq_lens", ctypes.c_void_p),
+    ]
+
+
+class shkv_tails_config(ctypes.Structure):
+    _fields_ = [
+        ("max_batch", ctypes.c_int32),
+        ("n_models", ctypes.c_int32),
+        ("max_tail_pages", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p),
+        ("tail_lens", ctypes.c_void_p),
+        ("initial_tail_lens", ctypes.c_void_p),
     ]
 
 
@@ -90,6 +103,13 @@ def load() -> ctypes.CDLL:
         "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
         "shkv_decode_consumer": [vp, i32, i32, ctypes.POINTER(i32)],
+        "shkv_tails_create": [vp, ctypes.POINTER(shkv_tails_config), ctypes.POINTER(vp)],
+        "shkv_tails_destroy": [vp],
+        "shkv_tails_set_lens": [vp, i32, i32p, vp],
+        "shkv_tails_get_lens": [vp, i32, i32p],
+        "shkv_tails_append": [vp, i32, i32, vp, vp, vp],
+        "shkv_decode_tails_workspace_size": [vp, vp, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
+        "shkv_decode_attention_tails": [vp, vp, i32, i32, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -187,3 +207,38 @@ def shkv_decode_consumer(pool: int, n_models: int, hq: int) -> int:
     out = ctypes.c_int32()
     _check(load().shkv_decode_consumer(pool, n_models, hq, ctypes.byref(out)), "shkv_decode_consumer")
     return out.value
+
+
+def shkv_tails_create(pool: int, cfg: shkv_tails_config) -> int:
+    h = ctypes.c_void_p()
+    _check(load().shkv_tails_create(pool, ctypes.byref(cfg), ctypes.byref(h)), "shkv_tails_create")
+    return h.value
+
+
+def shkv_tails_destroy(tails: int) -> None:
+    _check(load().shkv_tails_destroy(tails), "shkv_tails_destroy")
+
+
+def shkv_tails_set_lens(tails: int, batch: int, lens_ptr: int, stream: int) -> None:
+    _check(load().shkv_tails_set_lens(tails, batch, lens_ptr, stream), "shkv_tails_set_lens")
+
+
+def shkv_tails_get_lens(tails: int, batch: int, lens_ptr: int) -> None:
+    _check(load().shkv_tails_get_lens(tails, batch, lens_ptr), "shkv_tails_get_lens")
+
+
+def shkv_tails_append(tails: int, batch: int, n_new: int, k_new: int, v_new: int, stream: int) -> None:
+    _check(load().shkv_tails_append(tails, batch, n_new, k_new, v_new, stream), "shkv_tails_append")
+
+
+def shkv_decode_tails_workspace_size(pool: int, tails: int, batch: int, hq: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().shkv_decode_tails_workspace_size(pool, tails, batch, hq, ctypes.byref(n)),
+           "shkv_decode_tails_workspace_size")
+    return n.value
+
+
+def shkv_decode_attention_tails(pool: int, tails: int, batch: int, hq: int, q: int, scale: float, out: int,
+                                lse_out: int, workspace: int, workspace_bytes: int, stream: int) -> None:
+    _check(load().shkv_decode_attention_tails(pool, tails, batch, hq, q, scale, out, lse_out, workspace,
+                                              workspace_bytes, stream), "shkv_decode_attention_tails")

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(256)
         if (M != -INFINITY) {
             for (int s = 0; s < n_splits; ++s) {
                 const float w = ex2_approx((lse_part[(int64_t)s * nrow + row] - M) * 1.4426950408889634f);
+                if (w == 0.f)
+                    continue;     // lse = -inf: an empty split, whose o is not read
                 const float4 v = reinterpret_cast<const float4 *>(o_part + ((int64_t)s * nrow + row) * head_dim)[d4];
                 acc.x += w * v.x;
                 acc.y += w * v.y;
@@ -107,6 +109,24 @@ __global__ void __launch_bounds__(256)
     }
     if (lane == 0 && lse_out)
         lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+// dst[i] = value for i < n (grid-stride).
+__global__ void __launch_bounds__(256) shkv_fill_kernel(float *__restrict__ dst, int64_t n, float value)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = value;
+}
+
+cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream)
+{
+    if (n <= 0)
+        return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 1024)
+        blocks = 1024;
+    shkv_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dst, n, value);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,

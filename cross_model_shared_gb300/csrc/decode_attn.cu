@@ -382,10 +382,12 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                         for (int w = 0; w < kWtMax; ++w)
                             if (w < p.wt)
                                 acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * fac[nt][e & 1][w];
-                        if (whole)
-                            p.out[orow_r[nt][e & 1] * D + d] = __float2bfloat16_rn(acc);
-                        else
+                        if (!whole)
                             p.ws_part[orow_r[nt][e & 1] * D + d] = acc;
+                        else if (p.out_f32)
+                            p.out_f32[orow_r[nt][e & 1] * D + d] = acc;
+                        else
+                            p.out[orow_r[nt][e & 1] * D + d] = __float2bfloat16_rn(acc);
                     }
                     wsel = (wsel + 1 == p.wt) ? 0 : wsel + 1;
                 }
@@ -444,7 +446,10 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 #pragma unroll
                     for (int h = 0; h < (D / 128 > 0 ? D / 128 : 1); ++h) {
                         const int d4 = lane + 32 * h;
-                        if (d4 < dq) {
+                        if (d4 < dq && p.out_f32) {
+                            reinterpret_cast<float4 *>(p.out_f32 + orow * D)[d4] =
+                                make_float4(acc[h].x * inv, acc[h].y * inv, acc[h].z * inv, acc[h].w * inv);
+                        } else if (d4 < dq) {
                             __nv_bfloat162 lo = __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
                             __nv_bfloat162 hi = __floats2bfloat162_rn(acc[h].z * inv, acc[h].w * inv);
                             uint2 packed;

@@ -50,7 +50,9 @@ __device__ __forceinline__ Segment locate(const DecodeParams &p, int64_t idx, in
 }
 
 // Successor of a segment that ended at its unit's end: the next (request,
-// head) unit, from its first page, clipped to the CTA's range end.
+// head) unit, from its first page, clipped to the CTA's range end.  Requests
+// without pages (empty per-decoder tails) own no chunks and are stepped over;
+// the caller only asks while chunks remain in its range, so one exists.
 __device__ __forceinline__ Segment next_segment(const DecodeParams &p, const Segment &prev, int64_t cta_end)
 {
     Segment s;
@@ -59,6 +61,8 @@ __device__ __forceinline__ Segment next_segment(const DecodeParams &p, const Seg
     if (s.g == p.hkv) {
         s.g = 0;
         s.b = prev.b + 1;
+        while (s.b + 1 < p.batch && p.page_prefix[s.b + 1] == p.page_prefix[s.b])
+            ++s.b;
     }
     s.pages_b = p.page_prefix[s.b + 1] - p.page_prefix[s.b];
     s.unit_begin = prev.unit_end;

@@ -98,7 +98,8 @@ constexpr int kSmemLimit = 232448;
 struct DecodeParams {
     const __nv_bfloat16 *q;    // [B, N*Hq, D]
     __nv_bfloat16 *out;        // [B, N*Hq, D]
-    float *lse_out;            // [B, N*Hq] or null
+    float *out_f32;            // when set, final rows go here in fp32 instead of to out
+    float *lse_out;            // [B, N*Hq] or null (required with out_f32)
     const int32_t *block_table;
     const int32_t *seq_lens;
     uint32_t *err;

@@ -22,6 +22,7 @@ cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, c
 int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream);
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
                          const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream);
 }  // namespace shkv
@@ -37,6 +38,15 @@ struct shkv_pool {
     CUtensorMap tm_k2;     // 2-D maps: one 64-column half of a page (tcgen05 consumer)
     CUtensorMap tm_v2;
     std::vector<int32_t> lens;   // host copy of seq_lens
+    bool tails_view = false;     // a per-decoder tail table over another pool's pages: empty lengths allowed
+};
+
+// Per-decoder unique tails: a view pool over the parent's pages whose
+// "requests" are the (request, decoder) pairs, b * n_models + m.
+struct shkv_tails {
+    shkv_pool *parent;
+    shkv_pool *view;
+    int32_t max_batch, n_models, max_tail_pages;
 };
 
 namespace {
@@ -120,22 +130,24 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 //   cuts       [num_ctas + 1] first chunk of each CTA, cuts[num_ctas] = W
 shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv, int32_t max_ctas,
                        int32_t *prefix, uint8_t *last_fill, int32_t *cuts, int64_t *total_chunks,
-                       int32_t *num_ctas)
+                       int32_t *num_ctas, bool allow_empty = false)
 {
     if (batch < 1 || batch > SHKV_MAX_BATCH || !lens || page_size <= 0 || page_size > 255 || hkv <= 0 ||
         max_ctas <= 0)
         return SHKV_ERR_INVALID_ARG;
     prefix[0] = 0;
+    int64_t nonempty = 0;
     for (int b = 0; b < batch; ++b) {
-        if (lens[b] < 1)
+        if (lens[b] < (allow_empty ? 0 : 1))
             return SHKV_ERR_INVALID_ARG;
         const int64_t pages = ceil_div(lens[b], page_size);
         const int64_t next = (int64_t)prefix[b] + pages;
         if (next * hkv > INT32_MAX)
             return SHKV_ERR_UNSUPPORTED;
         prefix[b + 1] = (int32_t)next;
+        nonempty += pages > 0;
         if (last_fill)
-            last_fill[b] = (uint8_t)(lens[b] - (pages - 1) * page_size);
+            last_fill[b] = (uint8_t)(pages > 0 ? lens[b] - (pages - 1) * page_size : 0);
     }
     const int64_t W = (int64_t)hkv * prefix[batch];
     int64_t C = ceil_div(W, kMinChunksPerCta);
@@ -147,10 +159,12 @@ shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, in
         C = 1;
 
     const int64_t alpha = kSegmentCostChunks;
-    const int64_t T = W + alpha * (int64_t)batch * hkv;
+    const int64_t T = W + alpha * nonempty * hkv;
     int64_t c = 1, cw = 0, cb = 0;   // next cut, weight and chunks before the current unit
     for (int b = 0; b < batch && c < C; ++b) {
         const int64_t pg = prefix[b + 1] - prefix[b];
+        if (pg == 0)
+            continue;                // an empty request owns no chunks and costs nothing
         for (int g = 0; g < hkv && c < C; ++g) {
             const int64_t wu = pg + alpha;
             while (c < C) {
@@ -407,13 +421,22 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
     return SHKV_OK;
 }
 
-shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model,
-                                  const void *q, float scale, void *out, float *lse_out, void *workspace,
-                                  size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// One decode launch: final rows to out (bf16) or, when out_f32 is set, to
+// out_f32 (fp32; lse_out then required).  Launches nothing when the pool has
+// no chunks (every length zero, possible only for a tail view).
+shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
+                        float scale, void *out, float *out_f32, float *lse_out, void *workspace,
+                        size_t workspace_bytes, void *stream)
 {
-    if (!pool || !q || !out || !workspace || batch < 1 || n_models < 1 || hq_per_model < 1)
+    if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
+        hq_per_model < 1)
         return SHKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || ((uintptr_t)lse_out & 3u))
+    if (!aligned16(q) || !aligned16(out) || !aligned16(out_f32) || !aligned16(workspace) ||
+        ((uintptr_t)lse_out & 3u))
         return SHKV_ERR_INVALID_ARG;
     if (!isfinite(scale))
         return SHKV_ERR_INVALID_ARG;
@@ -432,9 +455,13 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     DecodeParams p;
     memset(&p, 0, sizeof p);
     shkv_status st = build_plan(batch, pool->lens.data(), c.page_size, c.num_kv_heads, pool->num_sms,
-                                p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas);
+                                p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas,
+                                pool->tails_view);
     if (st != SHKV_OK)
         return st;
+    if (p.total_chunks == 0)
+        return SHKV_OK;
+
     const bool use_umma = use_umma_consumer(rows, c.head_dim);
     const DecodeShape sh = decode_shape(rows);
     const int ncw = sh.nrg * sh.wt;
@@ -467,6 +494,7 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
     const size_t lse_bytes = align_up((uint32_t)(2 * pool->num_sms * rows * 4), 256);
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.out_f32 = out_f32;
     p.lse_out = lse_out;
     p.block_table = c.block_table;
     p.seq_lens = c.seq_lens;
@@ -496,6 +524,159 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);
     return cuda_status(e);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of a decode with tails: the shared pass's, the tail pass's, then
+// fp32 partials [2, B, rows, D] and their log-sum-exps [2, B, rows].
+struct TailsWorkspace {
+    size_t shared, tail, parts, lses, total;
+};
+
+TailsWorkspace tails_workspace(const shkv_pool *pool, int32_t batch, int32_t n_models, int32_t group)
+{
+    const shkv_pool_config &c = pool->cfg;
+    TailsWorkspace w;
+    const size_t rows_all = (size_t)batch * n_models * group * c.num_kv_heads;
+    w.shared = align256(workspace_bytes_for(batch, c.num_kv_heads, n_models * group, c.head_dim, pool->num_sms));
+    w.tail = align256(workspace_bytes_for(batch * n_models, c.num_kv_heads, group, c.head_dim, pool->num_sms));
+    w.parts = align256(2 * rows_all * c.head_dim * 4);
+    w.lses = align256(2 * rows_all * 4);
+    w.total = w.shared + w.tail + w.parts + w.lses;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model,
+                                  const void *q, float scale, void *out, float *lse_out, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    if (!out)
+        return SHKV_ERR_INVALID_ARG;
+    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, workspace,
+                       workspace_bytes, stream);
+}
+
+shkv_status shkv_tails_create(shkv_pool *pool, const shkv_tails_config *tc, shkv_tails **out)
+{
+    if (!pool || !tc || !out)
+        return SHKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (pool->tails_view || tc->max_batch < 1 || tc->n_models < 1 || tc->max_tail_pages < 1 || !tc->block_table ||
+        !tc->tail_lens || ((uintptr_t)tc->block_table & 3u) || ((uintptr_t)tc->tail_lens & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    if ((int64_t)tc->max_batch * tc->n_models > INT32_MAX / 2)
+        return SHKV_ERR_UNSUPPORTED;
+    shkv_pool_config vc = pool->cfg;
+    vc.max_batch = tc->max_batch * tc->n_models;
+    vc.max_pages_per_seq = tc->max_tail_pages;
+    vc.block_table = tc->block_table;
+    vc.seq_lens = tc->tail_lens;
+    vc.initial_seq_lens = tc->initial_tail_lens;
+    shkv_tails *t = new (std::nothrow) shkv_tails();
+    if (!t)
+        return SHKV_ERR_INVALID_ARG;
+    // the view shares the parent's pages and error word; creating it writes
+    // the tail lengths to the device and clears the (shared) error word
+    shkv_status st = shkv_pool_create(&vc, &t->view);
+    if (st != SHKV_OK) {
+        delete t;
+        return st;
+    }
+    t->view->tails_view = true;
+    t->parent = pool;
+    t->max_batch = tc->max_batch;
+    t->n_models = tc->n_models;
+    t->max_tail_pages = tc->max_tail_pages;
+    *out = t;
+    return SHKV_OK;
+}
+
+shkv_status shkv_tails_destroy(shkv_tails *tails)
+{
+    if (!tails)
+        return SHKV_ERR_INVALID_ARG;
+    shkv_pool_destroy(tails->view);
+    delete tails;
+    return SHKV_OK;
+}
+
+shkv_status shkv_tails_set_lens(shkv_tails *tails, int32_t batch, const int32_t *tail_lens, void *stream)
+{
+    if (!tails || batch < 0 || batch > tails->max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    return shkv_pool_set_seq_lens(tails->view, batch * tails->n_models, tail_lens, stream);
+}
+
+shkv_status shkv_tails_get_lens(const shkv_tails *tails, int32_t batch, int32_t *tail_lens)
+{
+    if (!tails || batch < 0 || batch > tails->max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    return shkv_pool_get_seq_lens(tails->view, batch * tails->n_models, tail_lens);
+}
+
+shkv_status shkv_tails_append(shkv_tails *tails, int32_t batch, int32_t n_new_tokens, const void *k_new,
+                              const void *v_new, void *stream)
+{
+    if (!tails || batch < 1 || batch > tails->max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    return shkv_append_kv(tails->view, batch * tails->n_models, n_new_tokens, k_new, v_new, stream);
+}
+
+shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_tails *tails, int32_t batch,
+                                             int32_t hq_per_model, size_t *bytes)
+{
+    if (!pool || !tails || !bytes || tails->parent != pool || batch < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    if (hq_per_model % pool->cfg.num_kv_heads)
+        return SHKV_ERR_UNSUPPORTED;
+    *bytes = tails_workspace(pool, batch, tails->n_models, hq_per_model / pool->cfg.num_kv_heads).total;
+    return SHKV_OK;
+}
+
+shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int32_t batch, int32_t hq_per_model,
+                                        const void *q, float scale, void *out, float *lse_out, void *workspace,
+                                        size_t workspace_bytes, void *stream)
+{
+    if (!pool || !tails || tails->parent != pool || !q || !out || !workspace || batch < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    if (batch > tails->max_batch || batch > pool->cfg.max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    if (hq_per_model % pool->cfg.num_kv_heads)
+        return SHKV_ERR_UNSUPPORTED;
+    const int32_t N = tails->n_models;
+    if ((int64_t)batch * N > SHKV_MAX_BATCH)
+        return SHKV_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || ((uintptr_t)lse_out & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    const int group = hq_per_model / pool->cfg.num_kv_heads;
+    const TailsWorkspace w = tails_workspace(pool, batch, N, group);
+    if (workspace_bytes < w.total)
+        return SHKV_ERR_INVALID_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int rows = N * hq_per_model;                    // output rows per request
+    const int64_t nrow = (int64_t)batch * rows;
+    float *o_part = reinterpret_cast<float *>(ws + w.shared + w.tail);
+    float *lse_part = reinterpret_cast<float *>(ws + w.shared + w.tail + w.parts);
+    cudaStream_t st = (cudaStream_t)stream;
+    // an empty tail writes nothing: its partial keeps lse = -inf (weight 0)
+    if (cudaError_t e = launch_fill_f32(lse_part + nrow, nrow, -INFINITY, st); e != cudaSuccess)
+        return SHKV_ERR_CUDA;
+    // tail pass: (request, decoder) pairs as requests, one decoder's G rows each
+    shkv_status s = decode_impl(tails->view, batch * N, 1, hq_per_model, q, scale, nullptr, o_part + nrow * pool->cfg.head_dim,
+                                lse_part + nrow, ws + w.shared, w.tail, stream);
+    if (s != SHKV_OK)
+        return s;
+    // shared pass: all decoders' rows stacked over the shared prefix
+    s = decode_impl(pool, batch, N, hq_per_model, q, scale, nullptr, o_part, lse_part, ws, w.shared, stream);
+    if (s != SHKV_OK)
+        return s;
+    return cuda_status(launch_merge(2, batch, rows, pool->cfg.head_dim, o_part, lse_part,
+                                    static_cast<__nv_bfloat16 *>(out), lse_out, st));
 }
 
 shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)

@@ -149,6 +149,94 @@ class SharedKVPool:
         return N.shkv_check_errors(self.handle, _stream_ptr(stream))
 
 
+class DecoderTails:
+    """Per-decoder unique tails over a SharedKVPool's pages (PrefillShare
+    Sec. 3.3-4, Eqs. 8-9: each decoder extends the shared base cache with its
+    own generated tokens; decoder m attends [shared prefix ++ its tail]).
+
+    block_table: int32 [max_batch, n_models, max_tail_pages] (fill it with
+    page indices of the shared pool; unused entries -1)
+    tail_lens: int32 [max_batch, n_models], owned by the tails after creation.
+    """
+
+    def __init__(self, pool: SharedKVPool, max_batch: int, n_models: int, max_tail_pages: int,
+                 initial_tail_lens=None):
+        self.pool = pool
+        dev = pool.k_pages.device
+        self.max_batch, self.n_models, self.max_tail_pages = max_batch, n_models, max_tail_pages
+        self.block_table = torch.full((max_batch, n_models, max_tail_pages), -1, dtype=torch.int32, device=dev)
+        self.tail_lens = torch.zeros((max_batch, n_models), dtype=torch.int32, device=dev)
+        init = None
+        if initial_tail_lens is not None:
+            init = np.zeros((max_batch, n_models), dtype=np.int32)
+            t = np.asarray(initial_tail_lens, dtype=np.int32)
+            init[: t.shape[0]] = t
+        cfg = N.shkv_tails_config(max_batch=max_batch, n_models=n_models, max_tail_pages=max_tail_pages,
+                                  block_table=self.block_table.data_ptr(), tail_lens=self.tail_lens.data_ptr(),
+                                  initial_tail_lens=init.ctypes.data if init is not None else None)
+        torch.cuda.synchronize(dev)
+        self.handle = N.shkv_tails_create(pool.handle, cfg)
+        self._workspace: Optional[torch.Tensor] = None
+
+    def close(self):
+        if getattr(self, "handle", None):
+            N.shkv_tails_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_lens(self, lens, stream=None):
+        arr = np.ascontiguousarray(lens, dtype=np.int32)
+        N.shkv_tails_set_lens(self.handle, arr.shape[0], arr.ctypes.data, _stream_ptr(stream))
+
+    def host_lens(self, batch: Optional[int] = None) -> np.ndarray:
+        batch = self.max_batch if batch is None else batch
+        out = np.zeros((batch, self.n_models), dtype=np.int32)
+        N.shkv_tails_get_lens(self.handle, batch, out.ctypes.data)
+        return out
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """Append [B, N, T, Hkv, D] bf16 K/V to every decoder's tail."""
+        _require(k_new, torch.bfloat16, "k_new")
+        _require(v_new, torch.bfloat16, "v_new")
+        B, M, T, H, D = k_new.shape
+        if tuple(v_new.shape) != (B, M, T, H, D) or M != self.n_models:
+            raise ValueError("k_new/v_new must be [B, n_models, T, num_kv_heads, head_dim]")
+        N.shkv_tails_append(self.handle, B, T, k_new.data_ptr(), v_new.data_ptr(), _stream_ptr(stream))
+
+    def workspace(self, batch: int, hq: int) -> torch.Tensor:
+        need = N.shkv_decode_tails_workspace_size(self.pool.handle, self.handle, batch, hq)
+        if self._workspace is None or self._workspace.numel() < need:
+            self._workspace = torch.zeros(need, dtype=torch.uint8, device=self.pool.k_pages.device)
+        return self._workspace
+
+    def decode_attention(self, q: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                         lse: Optional[torch.Tensor] = None, return_lse: bool = False, stream=None):
+        """Stacked decode where decoder m of request b attends the shared
+        prefix and its own tail.  q: bf16 [B, n_models * hq, head_dim]."""
+        _require(q, torch.bfloat16, "q")
+        B, rows, D = q.shape
+        if rows % self.n_models or D != self.pool.head_dim:
+            raise ValueError("q must be [B, n_models * hq, head_dim]")
+        hq = rows // self.n_models
+        if scale is None:
+            scale = 1.0 / float(np.sqrt(D))
+        if out is None:
+            out = torch.empty_like(q)
+        _require(out, torch.bfloat16, "out")
+        if return_lse and lse is None:
+            lse = torch.empty((B, rows), dtype=torch.float32, device=q.device)
+        ws = self.workspace(B, hq)
+        N.shkv_decode_attention_tails(self.pool.handle, self.handle, B, hq, q.data_ptr(), float(scale),
+                                      out.data_ptr(), lse.data_ptr() if lse is not None else None, ws.data_ptr(),
+                                      ws.numel(), _stream_ptr(stream))
+        return (out, lse) if (return_lse or lse is not None) else out
+
+
 def splitkv_merge(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,
                   lse_out: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Log-sum-exp merge of split partials: o_part fp32 [S, B, rows, D],

@@ -211,26 +211,28 @@ def custom_workload(name: str, B: int, N: int, Hq: int, Hkv: int, D: int, P: int
                     block_table=bt, num_pages=num_pages)
 
 
-def tails_spare_pages(tail_lens, P: int) -> int:
-    """Pages needed by per-decoder tails of the given lengths [B, N]."""
-    t = np.asarray(tail_lens, dtype=np.int64)
+def tails_spare_pages(tail_lens, P: int, reserve_tokens: int = 0) -> int:
+    """Pages needed by per-decoder tails of the given lengths [B, N], each
+    with room for ``reserve_tokens`` more."""
+    t = np.asarray(tail_lens, dtype=np.int64) + reserve_tokens
     return int(((t + P - 1) // P).sum())
 
 
-def make_tails(wl: Workload, tail_lens, seed: int = 0, extra_pages_per_tail: int = 0):
+def make_tails(wl: Workload, tail_lens, seed: int = 0, reserve_tokens: int = 0, extra_pages_per_tail: int = 0):
     """Per-decoder unique tails (PrefillShare Eq. 9's N * L_unique) placed in
     the pool pages the shared requests do not use, in a seeded random order.
 
-    ``tail_lens`` is [B, N] tokens.  Returns (tail_table int32 [B, N,
-    max_tail_pages] with -1 for unused entries, tail_lens int32 [B, N]).  The
-    workload must have been made with enough spare pages
-    (``tails_spare_pages``)."""
+    ``tail_lens`` is [B, N] tokens; every tail gets pages for
+    ``reserve_tokens`` more (room for appends) and the table
+    ``extra_pages_per_tail`` unused (-1) entries.  Returns (tail_table int32
+    [B, N, max_tail_pages], tail_lens int32 [B, N]).  The workload must have
+    been made with enough spare pages (``tails_spare_pages``)."""
     tl = np.asarray(tail_lens, dtype=np.int64).reshape(wl.B, wl.N)
     used = set(int(x) for x in wl.block_table[wl.block_table >= 0].ravel())
     free = np.array([pg for pg in range(wl.num_pages) if pg not in used], dtype=np.int32)
     rng = np.random.default_rng(seed)
     free = free[rng.permutation(len(free))]
-    pages = (tl + wl.P - 1) // wl.P
+    pages = (tl + reserve_tokens + wl.P - 1) // wl.P
     need = int(pages.sum())
     if need > len(free):
         raise ValueError(f"tails need {need} pages, the pool has {len(free)} spare")

@@ -173,6 +173,67 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                                   float *lse_out, void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/*
+ * Per-decoder unique tails (PrefillShare Sec. 3.3-4 and Eqs. 8-9: decode
+ * starts from the shared base cache and each decoder extends it with its own
+ * generated-token cache Delta C_t; the shared prefix is stored once, each
+ * decoder's tail N times in total).  Decoder m of request b attends the
+ * concatenation of the shared prefix (the pool's block table, L_b tokens)
+ * and its own tail (the tail table, T_{b,m} tokens, 0 allowed).  Tail pages
+ * live in the same page pool.
+ */
+typedef struct shkv_tails shkv_tails;
+
+typedef struct {
+    int32_t max_batch;                 /* requests */
+    int32_t n_models;                  /* decoders per request (N) */
+    int32_t max_tail_pages;            /* block-table width of one tail */
+    int32_t *block_table;              /* device int32 [max_batch, n_models, max_tail_pages], caller-owned */
+    int32_t *tail_lens;                /* device int32 [max_batch, n_models], caller-owned */
+    const int32_t *initial_tail_lens;  /* host int32 [max_batch * n_models] or NULL (all zero) */
+} shkv_tails_config;
+
+/*
+ * Tails over `pool`'s pages.  Writes the initial lengths to tail_lens and
+ * shares (and clears) the pool's error word.  The pool must outlive the
+ * tails.  Errors: SHKV_ERR_INVALID_ARG, SHKV_ERR_CAPACITY (an initial length
+ * above max_tail_pages * page_size), SHKV_ERR_CUDA.
+ */
+shkv_status shkv_tails_create(shkv_pool *pool, const shkv_tails_config *cfg, shkv_tails **out);
+shkv_status shkv_tails_destroy(shkv_tails *tails);
+
+/* Host-side lengths of the first `batch` requests' tails, [batch * n_models]
+ * (set: also copied to the device on `stream`, which is synchronised). */
+shkv_status shkv_tails_set_lens(shkv_tails *tails, int32_t batch, const int32_t *tail_lens, void *stream);
+shkv_status shkv_tails_get_lens(const shkv_tails *tails, int32_t batch, int32_t *tail_lens);
+
+/*
+ * Append n_new_tokens to every decoder's tail (its generated tokens' K/V):
+ * k_new / v_new device bf16 [batch, n_models, T, Hkv, d]; same rules and
+ * errors as shkv_append_kv, per (request, decoder).
+ */
+shkv_status shkv_tails_append(shkv_tails *tails, int32_t batch, int32_t n_new_tokens, const void *k_new,
+                              const void *v_new, void *stream);
+
+/* Workspace bytes for shkv_decode_attention_tails (zero-filled before the
+ * first use, kept between calls). */
+shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_tails *tails, int32_t batch,
+                                             int32_t hq_per_model, size_t *bytes);
+
+/*
+ * shkv_decode_attention where every decoder also attends its own tail:
+ * out[b, m*Hq + h] = softmax attention over [shared prefix ++ tail(b, m)].
+ * q / out / lse_out as in shkv_decode_attention with n_models = the tails'
+ * n_models.  Runs the tail pass (each (request, decoder) pair over its tail,
+ * G rows per KV head), the shared pass (all N*G rows stacked over the shared
+ * prefix), both to fp32 partials, then the log-sum-exp merge of the two.
+ * Supported: batch * n_models <= SHKV_MAX_BATCH, rest as
+ * shkv_decode_attention.  Errors as shkv_decode_attention.
+ */
+shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int32_t batch, int32_t hq_per_model,
+                                        const void *q, float scale, void *out, float *lse_out, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
 /* Consumer kernels of shkv_decode_attention. */
 #define SHKV_CONSUMER_MMA_SYNC 0
 #define SHKV_CONSUMER_TCGEN05 1

@@ -1,0 +1,138 @@
+"""Per-decoder unique tails on the GPU against the fp64 oracle.
+
+Decoder m of request b attends the shared prefix and its own tail
+(PrefillShare Sec. 3.3-4, Eqs. 8-9).  The library runs a tail pass over the
+(request, decoder) pairs, the shared pass over the stacked rows, and a
+log-sum-exp merge; these tests compare with the oracle's direct definition
+over the concatenated token list.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from cross_model_shared_gb300 import DecoderTails
+from cross_model_shared_gb300 import _native as N
+from cross_model_shared_gb300 import workloads as W
+from tests.gpu_common import bits_to_torch, compare, make_pool, torch_to_bits
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "llama8b": dict(N=2, Hq=32, Hkv=8, D=128, P=16),      # shared pass R = 8 (mma.sync)
+    "qwen14b": dict(N=8, Hq=40, Hkv=8, D=128, P=32),      # shared pass R = 40 (tcgen05)
+    "d64": dict(N=3, Hq=8, Hkv=2, D=64, P=16),            # head dim 64
+}
+
+
+def setup(shape, lens, tails, seed=5, reserve_tokens=0):
+    sh = SHAPES[shape]
+    tails = np.asarray(tails).reshape(len(lens), sh["N"])
+    spare = W.tails_spare_pages(tails, sh["P"], reserve_tokens)
+    wl = W.custom_workload(shape, B=len(lens), lens_prefill=lens, seed=seed, spare_pages=spare, **sh)
+    tt, tl = W.make_tails(wl, tails, seed=seed + 1, reserve_tokens=reserve_tokens, extra_pages_per_tail=1)
+    q = W.gen_q(wl)
+    k, v = W.gen_pool(wl)
+    pool = make_pool(wl, k, v)
+    tails_obj = DecoderTails(pool, wl.B, wl.N, tt.shape[2], initial_tail_lens=tl)
+    tails_obj.block_table.copy_(torch.from_numpy(tt))
+    torch.cuda.synchronize()
+    return wl, tt, tl, q, k, v, pool, tails_obj
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_tails_match_oracle(shape):
+    lens = [1, 17, 300, 2049, 64]
+    rng = np.random.default_rng(3)
+    tails = rng.integers(0, 400, size=(len(lens), SHAPES[shape]["N"]))
+    tails[0, 0] = 0
+    tails[1, :] = 0
+    tails[2, -1] = 1
+    wl, tt, tl, q, k, v, pool, tob = setup(shape, lens, tails)
+    out, lse = tob.decode_attention(bits_to_torch(q), scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    ref, lref = oracle.decode_attention_tails(q, k, v, wl.block_table, wl.lens_final, tt, tl, n_models=wl.N,
+                                              hq=wl.Hq, scale=wl.scale)
+    compare(out, ref, lse, lref, what=f"tails {shape}")
+
+
+@pytest.mark.parametrize("shape", ["llama8b", "qwen14b"])
+def test_empty_tails_give_the_plain_decode_bits(shape):
+    """Every tail empty: the merge has one live split with weight exactly 1,
+    so the result is the shared decode's own bits."""
+    lens = [5, 300, 2049]
+    wl, tt, tl, q, k, v, pool, tob = setup(shape, lens, np.zeros((3, SHAPES[shape]["N"]), int))
+    qt = bits_to_torch(q)
+    out_t, lse_t = tob.decode_attention(qt, scale=wl.scale, return_lse=True)
+    out_p, lse_p = pool.decode_attention(qt, wl.N, scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    assert torch.equal(out_t, out_p)
+    assert torch.equal(lse_t, lse_p)
+
+
+def test_long_tails_are_split_and_merged():
+    """Tails long enough that the tail pass itself splits across CTAs."""
+    lens = [3000]
+    wl, tt, tl, q, k, v, pool, tob = setup("qwen14b", lens, [[9000, 1, 0, 4000, 20000, 33, 7, 128]])
+    out, lse = tob.decode_attention(bits_to_torch(q), scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    ref, lref = oracle.decode_attention_tails(q, k, v, wl.block_table, wl.lens_final, tt, tl, n_models=wl.N,
+                                              hq=wl.Hq, scale=wl.scale)
+    compare(out, ref, lse, lref, what="long tails")
+
+
+def test_tail_append_then_decode():
+    """Decoders append their own generated tokens (different K/V per
+    decoder) into pre-assigned tail pages, then decode: the tails' bytes
+    match numpy indexing and the result matches the oracle."""
+    lens = [100, 40]
+    tails0 = np.array([[3, 0], [16, 15]])
+    T = 5
+    wl, tt, tl, q, k, v, pool, tob = setup("llama8b", lens, tails0, reserve_tokens=T)
+    rng = np.random.default_rng(9)
+    kn = W.bf16_bits_from_f32(rng.standard_normal((wl.B, wl.N, T, wl.Hkv, wl.D)).astype(np.float32))
+    vn = W.bf16_bits_from_f32(rng.standard_normal((wl.B, wl.N, T, wl.Hkv, wl.D)).astype(np.float32))
+    tob.append(bits_to_torch(kn), bits_to_torch(vn))
+    assert pool.check_errors() == 0
+    np.testing.assert_array_equal(tob.host_lens(wl.B), tl + T)
+    k2, v2 = torch_to_bits(pool.k_pages), torch_to_bits(pool.v_pages)
+    tl2 = tl + T
+    for b in range(wl.B):
+        for m in range(wl.N):
+            for i in range(T):
+                pos = int(tl[b, m]) + i
+                page, slot = tt[b, m, pos // wl.P], pos % wl.P
+                np.testing.assert_array_equal(k2[page, :, slot], kn[b, m, i])
+                np.testing.assert_array_equal(v2[page, :, slot], vn[b, m, i])
+    out, lse = tob.decode_attention(bits_to_torch(q), scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    ref, lref = oracle.decode_attention_tails(q, k2, v2, wl.block_table, wl.lens_final, tt, tl2.astype(np.int32),
+                                              n_models=wl.N, hq=wl.Hq, scale=wl.scale)
+    compare(out, ref, lse, lref, what="tails after append")
+
+
+def test_identical_tails_and_queries_give_matching_slices():
+    """Decoders with identical queries and identical tails get the same
+    result; each (request, decoder) tail is its own unit of the split plan,
+    so equal tails may be split differently: equal within the tolerance, not
+    bit for bit."""
+    lens = [700, 64]
+    wl, tt, tl, q, k, v, pool, tob = setup("qwen14b", lens, [[50] * 8, [200] * 8])
+    for m in range(1, wl.N):
+        q[:, m * wl.Hq:(m + 1) * wl.Hq] = q[:, :wl.Hq]
+    tt2 = tt.copy()
+    tt2[:, 1:] = tt[:, :1]
+    tob.block_table.copy_(torch.from_numpy(tt2))
+    out = tob.decode_attention(bits_to_torch(q), scale=wl.scale)
+    first = out[:, :wl.Hq].double().cpu().numpy()
+    for m in range(1, wl.N):
+        compare(out[:, m * wl.Hq:(m + 1) * wl.Hq], first, what=f"decoder {m} vs 0")
+
+
+def test_out_of_range_tail_page_sets_flag():
+    lens = [100, 100]
+    wl, tt, tl, q, k, v, pool, tob = setup("llama8b", lens, [[40, 40], [40, 40]])
+    tob.block_table[1, 1, 0] = wl.num_pages + 3
+    out = tob.decode_attention(bits_to_torch(q), scale=wl.scale)
+    assert pool.check_errors() & N.SHKV_ERRF_PAGE_OOB
+    assert bool(torch.isfinite(out.float()).all())
