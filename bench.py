@@ -62,6 +62,11 @@ def parse_args():
     ap.add_argument("--impl", default="shkv", choices=["shkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--prefix-pages", action="store_true",
+                    help="host-side page-manager run: a seeded multi-agent workflow over the prefix pool")
+    ap.add_argument("--tail-tokens", type=int, default=0,
+                    help="give every decoder its own unique tail of about this many tokens (seeded, "
+                         "uniform in [T/2, 3T/2]) and time the decode with tails")
     return ap.parse_args()
 
 
@@ -286,6 +291,207 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+def tail_lengths(wl: W.Workload, T: int) -> np.ndarray:
+    rng = np.random.default_rng(wl.seed + 4242)
+    return rng.integers(max(0, T // 2), T + T // 2 + 1, size=(wl.B, wl.N)).astype(np.int32)
+
+
+def run_gpu_tails(args):
+    """Decode where every decoder also attends its own unique tail
+    (PrefillShare Eq. 9: one shared prefix, N unique tails)."""
+    import torch
+    from cross_model_shared_gb300 import DecoderTails, SharedKVPool
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    base = load_workload(args)
+    probe = tail_lengths(base, args.tail_tokens)
+    wl = W.custom_workload(f"{base.name}+tails{args.tail_tokens}", B=base.B, N=base.N, Hq=base.Hq, Hkv=base.Hkv,
+                           D=base.D, P=base.P, lens_prefill=base.lens_prefill, n_append=base.n_append,
+                           seed=base.seed, spare_pages=W.tails_spare_pages(probe, base.P))
+    tt, tl = W.make_tails(wl, probe, seed=wl.seed + 1)
+    q_bits = W.gen_q(wl)
+    k_dev, v_dev = W.gen_pool_device(wl, device=dev)
+    pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
+                        device=dev, k_pages=k_dev, v_pages=v_dev, initial_seq_lens=wl.lens_final)
+    pool.block_table.copy_(torch.from_numpy(wl.block_table).to(dev))
+    tails = DecoderTails(pool, wl.B, wl.N, tt.shape[2], initial_tail_lens=tl)
+    tails.block_table.copy_(torch.from_numpy(tt).to(dev))
+    q = torch.from_numpy(q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.rows), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        tails.decode_attention(q, scale=wl.scale, out=out, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if pool.check_errors():
+        raise RuntimeError("device error bits during warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if pool.check_errors():
+        raise RuntimeError("device error bits in the timed region")
+    shared_kv = W.unique_kv_bytes(wl)
+    tail_kv = int(((tl.astype(np.int64) + wl.P - 1) // wl.P).sum()) * wl.P * wl.Hkv * wl.D * 4
+    nbytes = shared_kv + tail_kv + 2 * wl.B * wl.rows * wl.D * 2
+    ms_per_step = ms / args.steps
+    per_gpu = nbytes / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput_gbs(nbytes, args.steps, 1, ms * 1e-3)
+
+    # end to end through the C ABI: pinned host q in, host out back, per step
+    q_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_host.copy_(q.cpu())
+    out_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_e2e = torch.empty_like(q)
+    e_steps = max(10, min(args.steps, 1000))
+
+    def e2e_step():
+        q_e2e.copy_(q_host, non_blocking=True)
+        tails.decode_attention(q_e2e, scale=wl.scale, out=out, lse=lse)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_value = nbytes * e_steps / (time.perf_counter() - t0) / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        order = np.argsort(wl.lens_final, kind="stable")
+        kv_b, elapsed, done = 0, 0.0, []
+        i = 0
+        while elapsed < args.cpu_budget_s and i < 64 * wl.B:
+            b = int(order[(len(order) // 2 + i) % len(order)])
+            npg = int((wl.lens_final[b] + wl.P - 1) // wl.P)
+            tpg = ((tl[b].astype(np.int64) + wl.P - 1) // wl.P).astype(int)
+            ids = np.concatenate([wl.block_table[b, :npg]] + [tt[b, m, :tpg[m]] for m in range(wl.N)]).astype(np.int64)
+            idt = torch.from_numpy(ids).to(dev)
+            kb = k_dev.index_select(0, idt).view(torch.int16).cpu().numpy().view(np.uint16)
+            vb = v_dev.index_select(0, idt).view(torch.int16).cpu().numpy().view(np.uint16)
+            bt = np.arange(npg, dtype=np.int32)[None, :]
+            ttl = np.full((1, wl.N, max(1, int(tpg.max()))), -1, np.int32)
+            off = npg
+            for m in range(wl.N):
+                ttl[0, m, :tpg[m]] = np.arange(off, off + tpg[m])
+                off += tpg[m]
+            t0 = time.perf_counter()
+            oracle.decode_attention_tails(q_bits[b:b + 1], kb, vb, bt, np.array([wl.lens_final[b]], np.int32), ttl,
+                                          tl[b:b + 1], n_models=wl.N, hq=wl.Hq, scale=wl.scale)
+            elapsed += time.perf_counter() - t0
+            kv_b += len(ids) * wl.P * wl.Hkv * wl.D * 4
+            done.append(b)
+            i += 1
+        cpu = {"value": kv_b / elapsed / 1e9, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{len(done)} whole requests of {wl.name} with their {wl.N} tails, fp64, "
+                         f"{oracle.num_threads()} threads", "seconds": round(elapsed, 2)}
+
+    peak, peak_kind = measured_peaks()
+    consumer = pool.decode_consumer(wl.N, wl.Hq)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "decoders": wl.N, "hq_per_decoder": wl.Hq, "hkv": wl.Hkv,
+                   "head_dim": wl.D, "page_size": wl.P, "rows_per_kv_head": wl.R,
+                   "mean_context": float(wl.lens_final.mean()), "mean_tail": float(tl.mean()),
+                   "shared_kv_bytes": shared_kv, "tail_kv_bytes": tail_kv, "step_bytes": nbytes,
+                   "l2": "inputs larger than L2" if shared_kv + tail_kv > 2 * 129e6 else "L2-resident working set",
+                   "parallelism": "replicas x1"},
+        "steps_per_s": 1e3 / ms_per_step,
+        "pct_of_hbm_peak": {"measured_copy": 100 * per_gpu / peak, "nominal_8tbs": 100 * per_gpu / NOMINAL_HBM_GBS},
+        "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
+                     "peak_kind": peak_kind, "traffic": None, "kernel": KERNELS[consumer]["name"],
+                     "consumer": consumer, "note": "whole step: tail pass + shared pass + merge"},
+        "unshared": None,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": q.numel() * 2, "steps": e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_prefix_pages(args):
+    """Seeded agent workflow over the prefix pool (PrFaaS hybrid prefix cache
+    pool; ICaRus key design 2: prompts cached for one agent are hits for the
+    others).  Per session, every round each of the N agents sends the
+    session context plus its own instruction; its output (the next round's
+    context growth) is appended afterwards.  Compares pages held and tokens
+    prefilled with the pool against every request holding private pages."""
+    from cross_model_shared_gb300 import PrefixPages
+    wl = load_workload(args)
+    rng = np.random.default_rng(wl.seed + 99)
+    P, n_agents = wl.P, wl.N
+    sessions, rounds, instr, out_tok = 16, 4, 64, 256
+    ctx = [rng.integers(0, 32000, size=int(L)).astype(np.int32) for L in wl.lens_prefill[:sessions]]
+    max_tokens = max(len(c) for c in ctx) + rounds * (n_agents * out_tok + instr) + instr
+    num_pages = sessions * n_agents * ((max_tokens + P - 1) // P)
+    pages = PrefixPages(num_pages, P)
+    ops, t_ops = 0, 0.0
+    prefilled = total = 0
+    peak_pool = peak_private = 0
+    for r in range(rounds):
+        held = []
+        for s_ in range(sessions):
+            for a in range(n_agents):
+                prompt = np.concatenate([ctx[s_], np.full(instr, 100000 + a, np.int32)])
+                t0 = time.perf_counter()
+                pg, cached = pages.acquire(prompt)
+                pages.publish(prompt, pg)
+                t_ops += time.perf_counter() - t0
+                ops += 2
+                held.append(pg)
+                prefilled += len(prompt) - cached
+                total += len(prompt)
+        st = pages.stats()
+        peak_pool = max(peak_pool, st["referenced_pages"])
+        peak_private = max(peak_private, sum(len(h) for h in held))
+        t0 = time.perf_counter()
+        for pg in held:
+            pages.release(pg)
+        t_ops += time.perf_counter() - t0
+        ops += len(held)
+        for s_ in range(sessions):
+            for a in range(n_agents):
+                ctx[s_] = np.concatenate([ctx[s_], rng.integers(0, 32000, size=out_tok).astype(np.int32)])
+    st = pages.stats()
+    line = {
+        "metric": "prefix pool: pages held and prefill tokens saved (host page manager)",
+        "value": 1.0 - prefilled / total, "unit": "fraction of prompt tokens served from cached pages",
+        "higher_is_better": True, "data": "synthetic", "dtype": "int32",
+        "config": {"workload": f"{wl.name} sessions={sessions} agents={n_agents} rounds={rounds} "
+                               f"instruction={instr} output={out_tok}", "page_size": P},
+        "pages_held_peak": {"prefix_pool": peak_pool, "private_pages": peak_private,
+                            "ratio": peak_private / max(1, peak_pool)},
+        "prefill_tokens": {"with_pool": prefilled, "without_pool": total},
+        "block_hit_rate": st["block_hits"] / max(1, st["block_lookups"]),
+        "host_ops_per_s": ops / t_ops, "ops": ops,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -448,6 +654,12 @@ def run_gpu(args):
 
 def main():
     args = parse_args()
+    if args.prefix_pages:
+        run_prefix_pages(args)
+        return
+    if args.tail_tokens and args.impl == "shkv":
+        run_gpu_tails(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -11,11 +11,11 @@ imported without a GPU or a built library.
 """
 import importlib
 
-__all__ = ["SharedKVPool", "DecoderTails", "splitkv_merge", "native", "workloads", "build"]
+__all__ = ["SharedKVPool", "DecoderTails", "PrefixPages", "splitkv_merge", "native", "workloads", "build"]
 
 
 def __getattr__(name):
-    if name in ("SharedKVPool", "DecoderTails", "splitkv_merge"):
+    if name in ("SharedKVPool", "DecoderTails", "PrefixPages", "splitkv_merge"):
         return getattr(importlib.import_module(".pool", __name__), name)
     if name == "native":
         return importlib.import_module("._native", __name__)

@@ -34,7 +34,9 @@ EXPORTS = [
     "shkv_check_errors", "shkv_plan_decode", "shkv_status_string", "shkv_decode_attention_noalloc",
     "shkv_decode_consumer", "shkv_tails_create", "shkv_tails_destroy", "shkv_tails_set_lens",
     "shkv_tails_get_lens", "shkv_tails_append", "shkv_decode_tails_workspace_size",
-    "shkv_decode_attention_tails",
+    "shkv_decode_attention_tails", "shkv_pages_create", "shkv_pages_destroy", "shkv_pages_acquire",
+    "shkv_pages_publish", "shkv_pages_release", "shkv_pages_alloc_transfer", "shkv_pages_stats",
+    "shkv_pages_refcount",
 ]
 
 SHKV_CONSUMER_MMA_SYNC = 0
@@ -68,6 +70,19 @@ class shkv_tails_config(ctypes.Structure):
         ("block_table", ctypes.c_void_p),
         ("tail_lens", ctypes.c_void_p),
         ("initial_tail_lens", ctypes.c_void_p),
+    ]
+
+
+class shkv_pages_info(ctypes.Structure):
+    _fields_ = [
+        ("num_pages", ctypes.c_int32),
+        ("free_pages", ctypes.c_int32),
+        ("cached_idle_pages", ctypes.c_int32),
+        ("referenced_pages", ctypes.c_int32),
+        ("indexed_blocks", ctypes.c_int32),
+        ("transfer_pages", ctypes.c_int32),
+        ("block_lookups", ctypes.c_int64),
+        ("block_hits", ctypes.c_int64),
     ]
 
 
@@ -110,6 +125,14 @@ def load() -> ctypes.CDLL:
         "shkv_tails_append": [vp, i32, i32, vp, vp, vp],
         "shkv_decode_tails_workspace_size": [vp, vp, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
         "shkv_decode_attention_tails": [vp, vp, i32, i32, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
+        "shkv_pages_create": [i32, i32, ctypes.POINTER(vp)],
+        "shkv_pages_destroy": [vp],
+        "shkv_pages_acquire": [vp, i32p, i32, i32p, i32, ctypes.POINTER(i32)],
+        "shkv_pages_publish": [vp, i32p, i32, i32p],
+        "shkv_pages_release": [vp, i32p, i32],
+        "shkv_pages_alloc_transfer": [vp, i32, i32p],
+        "shkv_pages_stats": [vp, ctypes.POINTER(shkv_pages_info)],
+        "shkv_pages_refcount": [vp, i32, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -242,3 +265,13 @@ def shkv_decode_attention_tails(pool: int, tails: int, batch: int, hq: int, q: i
                                 lse_out: int, workspace: int, workspace_bytes: int, stream: int) -> None:
     _check(load().shkv_decode_attention_tails(pool, tails, batch, hq, q, scale, out, lse_out, workspace,
                                               workspace_bytes, stream), "shkv_decode_attention_tails")
+
+
+def shkv_pages_create(num_pages: int, page_size: int) -> int:
+    h = ctypes.c_void_p()
+    _check(load().shkv_pages_create(num_pages, page_size, ctypes.byref(h)), "shkv_pages_create")
+    return h.value
+
+
+def shkv_pages_destroy(pages: int) -> None:
+    _check(load().shkv_pages_destroy(pages), "shkv_pages_destroy")

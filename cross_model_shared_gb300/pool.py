@@ -237,6 +237,66 @@ class DecoderTails:
         return (out, lse) if (return_lse or lse is not None) else out
 
 
+class PrefixPages:
+    """Host-side refcounted page bookkeeping for a pool of ``num_pages``
+    pages of ``page_size`` tokens (libshkv's page manager): reusable
+    prefix-cache blocks, keyed by their token ids and shared across requests
+    and decoder models, and transfer pages for one handoff (PrFaaS hybrid
+    prefix cache pool; ICaRus key design 2)."""
+
+    def __init__(self, num_pages: int, page_size: int):
+        N.load()
+        self.page_size = page_size
+        self.handle = N.shkv_pages_create(num_pages, page_size)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            N.shkv_pages_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def acquire(self, tokens) -> Tuple[np.ndarray, int]:
+        """(pages for the prompt, tokens already cached)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        npg = (len(t) + self.page_size - 1) // self.page_size
+        out = np.zeros(max(1, npg), dtype=np.int32)
+        hit = ctypes.c_int32()
+        N._check(N.load().shkv_pages_acquire(self.handle, t.ctypes.data if len(t) else None, len(t),
+                                             out.ctypes.data, npg, ctypes.byref(hit)), "shkv_pages_acquire")
+        return out[:npg].copy(), hit.value
+
+    def publish(self, tokens, pages) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        pg = np.ascontiguousarray(pages, dtype=np.int32)
+        N._check(N.load().shkv_pages_publish(self.handle, t.ctypes.data if len(t) else None, len(t),
+                                             pg.ctypes.data if len(pg) else None), "shkv_pages_publish")
+
+    def release(self, pages) -> None:
+        pg = np.ascontiguousarray(pages, dtype=np.int32)
+        N._check(N.load().shkv_pages_release(self.handle, pg.ctypes.data if len(pg) else None, len(pg)),
+                 "shkv_pages_release")
+
+    def alloc_transfer(self, n: int) -> np.ndarray:
+        out = np.zeros(max(1, n), dtype=np.int32)
+        N._check(N.load().shkv_pages_alloc_transfer(self.handle, n, out.ctypes.data), "shkv_pages_alloc_transfer")
+        return out[:n].copy()
+
+    def stats(self) -> dict:
+        info = N.shkv_pages_info()
+        N._check(N.load().shkv_pages_stats(self.handle, ctypes.byref(info)), "shkv_pages_stats")
+        return {f: getattr(info, f) for f, _ in info._fields_}
+
+    def refcount(self, page: int) -> int:
+        c = ctypes.c_int32()
+        N._check(N.load().shkv_pages_refcount(self.handle, page, ctypes.byref(c)), "shkv_pages_refcount")
+        return c.value
+
+
 def splitkv_merge(o_part: torch.Tensor, lse_part: torch.Tensor, out: Optional[torch.Tensor] = None,
                   lse_out: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Log-sum-exp merge of split partials: o_part fp32 [S, B, rows, D],

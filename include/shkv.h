@@ -234,6 +234,73 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
                                         const void *q, float scale, void *out, float *lse_out, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
+/*
+ * Page bookkeeping for the shared pool (host only, no CUDA): refcounted
+ * prefix-cache pages and transfer pages.
+ *
+ * PrFaaS (hybrid prefix cache pool): prefix-cache blocks are reused within
+ * the cluster and must be block-aligned and completely filled; transfer-cache
+ * blocks serve one cross-cluster transfer and are dropped when it is done.
+ * ICaRus key design 2: all task models share the frozen base encoder, so a
+ * prefix cached while serving one agent is a hit for every later agent.
+ *
+ * A full block (page_size tokens) is keyed by a hash chain over token ids
+ * with the parent block's hash, and matched only if the parent and the token
+ * ids are equal.  Pages whose reference count drops to zero stay indexed
+ * (idle, least recently used first) until a new allocation needs a page.
+ * The caller fills the pages it is handed (prefill / handoff /
+ * shkv_append_kv) and writes them into block tables; several requests may
+ * reference one page.
+ */
+typedef struct shkv_pages shkv_pages;
+
+typedef struct {
+    int32_t num_pages;
+    int32_t free_pages;          /* never used, or released private/transfer pages */
+    int32_t cached_idle_pages;   /* indexed prefix pages no request references */
+    int32_t referenced_pages;    /* pages with a reference count > 0 */
+    int32_t indexed_blocks;      /* full blocks in the prefix index */
+    int32_t transfer_pages;      /* transfer pages currently allocated */
+    int64_t block_lookups;       /* full blocks looked up by acquire */
+    int64_t block_hits;          /* of which were cached */
+} shkv_pages_info;
+
+/* A manager for pages 0 .. num_pages-1 of page_size tokens. */
+shkv_status shkv_pages_create(int32_t num_pages, int32_t page_size, shkv_pages **out);
+shkv_status shkv_pages_destroy(shkv_pages *pages);
+
+/*
+ * Pages for a request whose prompt is tokens[0 .. n_tokens): the longest
+ * prefix of full blocks found in the index is reused (reference +1 each),
+ * the remaining ceil(n_tokens / page_size) - hits pages are new private
+ * pages (reference 1) taken from the free pages, else from the idle cached
+ * pages in LRU order (dropped from the index).
+ *   pages            host int32 [max_pages]: receives the request's pages
+ *   n_cached_tokens  receives hits * page_size (tokens already in the pool)
+ * Errors: SHKV_ERR_INVALID_ARG; SHKV_ERR_CAPACITY (more than max_pages
+ * blocks, or not enough pages: nothing is kept).
+ */
+shkv_status shkv_pages_acquire(shkv_pages *pages, const int32_t *tokens, int32_t n_tokens, int32_t *out_pages,
+                               int32_t max_pages, int32_t *n_cached_tokens);
+
+/*
+ * After the request's pages hold its K/V: enter its full blocks (not a
+ * partial last block) into the prefix index.  Blocks already indexed (this
+ * request's hits, or the same content published by another request) are
+ * left as they are.  Errors: SHKV_ERR_INVALID_ARG (a page not referenced,
+ * or a transfer page).
+ */
+shkv_status shkv_pages_publish(shkv_pages *pages, const int32_t *tokens, int32_t n_tokens, const int32_t *req_pages);
+
+/* Drop one reference from each page (a finished request or transfer). */
+shkv_status shkv_pages_release(shkv_pages *pages, const int32_t *req_pages, int32_t n_pages);
+
+/* n pages for one transfer (reference 1, never indexed). */
+shkv_status shkv_pages_alloc_transfer(shkv_pages *pages, int32_t n_pages, int32_t *out_pages);
+
+shkv_status shkv_pages_stats(const shkv_pages *pages, shkv_pages_info *info);
+shkv_status shkv_pages_refcount(const shkv_pages *pages, int32_t page, int32_t *count);
+
 /* Consumer kernels of shkv_decode_attention. */
 #define SHKV_CONSUMER_MMA_SYNC 0
 #define SHKV_CONSUMER_TCGEN05 1
