@@ -52,6 +52,8 @@ def _load():
             lib.oracle_decode_attention_tails.argtypes = [i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P,
                                                           ctypes.c_double, P, P, i]
             lib.oracle_decode_attention_tails.restype = i
+            lib.oracle_prefill_attention.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, ctypes.c_double, P, P, i]
+            lib.oracle_prefill_attention.restype = i
             lib.oracle_splitkv_merge.argtypes = [i, i, i, i, P, P, P, P]
             lib.oracle_splitkv_merge.restype = i
             lib.oracle_append_kv.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P]
@@ -135,6 +137,31 @@ def decode_attention_tails(q, k_pages, v_pages, block_table, seq_lens, tail_tabl
                                                _ptr(tt), _ptr(tl), float(scale), _ptr(out), _ptr(lse),
                                                int(nthreads))
     _check(st, "decode_attention_tails")
+    return out, lse
+
+
+def prefill_attention(q, k_pages, v_pages, block_table, seq_lens, *, scale: float, nthreads: int = 0):
+    """Causal attention of n_new appended tokens over the cached prefix and
+    themselves (PrefillShare Sec. 3.3, partial prefill on a cache hit).
+
+    ``q`` is bf16 bits [B, n_new, Hq, D]; ``seq_lens`` already include the
+    n_new tokens, whose K/V are in the pool.  New token i of request b is at
+    position seq_lens[b] - n_new + i and attends keys 0 .. its position.
+    Returns fp64 (out [B, n_new, Hq, D], lse [B, n_new, Hq])."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    v_pages = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, T, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    assert D2 == D and bt.shape[0] >= B
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, T, Hq), dtype=np.float64)
+    st = _load().oracle_prefill_attention(B, T, Hq, Hkv, D, P, num_pages, bt.shape[1], _ptr(q), _ptr(k_pages),
+                                          _ptr(v_pages), _ptr(bt), _ptr(lens), float(scale), _ptr(out), _ptr(lse),
+                                          int(nthreads))
+    _check(st, "prefill_attention")
     return out, lse
 
 

@@ -426,6 +426,121 @@ int oracle_decode_attention_tails(int B, int N, int Hq, int Hkv, int D, int P, i
 }
 
 /*
+ * Partial-prefill attention (PrefillShare Sec. 3.3: on a prefix-cache hit the
+ * shared prefill module runs only on the new tokens, extending the cached
+ * prefix).  The caller has appended the n_new tokens' K/V, so request b holds
+ * L_b = seq_lens[b] tokens of which the last n_new are new; new token i sits
+ * at position L_b - n_new + i and attends every key at a position <= its own
+ * (the whole cached prefix, and the new tokens causally).
+ *
+ *   q      bf16 bits [B, n_new, Hq, D]     (the prefill module's query heads)
+ *   out    fp64 [B, n_new, Hq, D];  lse fp64 [B, n_new, Hq] (nullable)
+ *
+ * Same two-pass fp64 softmax as the decode oracle, over keys 0 .. position.
+ */
+typedef struct {
+    int B, n_new, Hq, Hkv, D, P, num_pages, max_pages;
+    const uint16_t *q, *k_pages, *v_pages;
+    const int32_t *block_table, *seq_lens;
+    double scale;
+    double *out, *lse;
+    long next_row, total_rows;
+    int status;
+    pthread_mutex_t lock;
+} prefill_job;
+
+static int attend_prefill_row(const prefill_job *j, int b, int i, int h, row_scratch *sc)
+{
+    const int g = kv_head(j->Hq, j->Hkv, h);
+    const long row = ((long)b * j->n_new + i) * j->Hq + h;
+    const uint16_t *q = j->q + row * j->D;
+    double *o = j->out + row * j->D;
+    double *lse = j->lse ? j->lse + row : NULL;
+    const int L = j->seq_lens[b];
+    const int n = L - j->n_new + i + 1;                /* keys 0 .. own position */
+    for (int t = 0; t < n; ++t) {
+        int32_t page = j->block_table[(long)b * j->max_pages + t / j->P];
+        if (page < 0 || page >= j->num_pages)
+            return ORACLE_EPAGE;
+        sc->kt[t] = page_slot(j->k_pages, j->Hkv, j->P, j->D, page, g, t);
+        sc->vt[t] = page_slot(j->v_pages, j->Hkv, j->P, j->D, page, g, t);
+    }
+    softmax_attend(q, j->D, j->scale, n, sc->kt, sc->vt, sc->s, o, lse);
+    return ORACLE_OK;
+}
+
+static void *prefill_worker(void *arg)
+{
+    prefill_job *j = (prefill_job *)arg;
+    int max_len = 1;
+    for (int b = 0; b < j->B; ++b)
+        if (j->seq_lens[b] > max_len)
+            max_len = j->seq_lens[b];
+    row_scratch sc;
+    if (!scratch_alloc(&sc, max_len)) {
+        scratch_free(&sc);
+        pthread_mutex_lock(&j->lock);
+        j->status = ORACLE_ENOMEM;
+        pthread_mutex_unlock(&j->lock);
+        return NULL;
+    }
+    const long per_b = (long)j->n_new * j->Hq;
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        long idx = j->next_row++;
+        int stop = j->status != ORACLE_OK;
+        pthread_mutex_unlock(&j->lock);
+        if (stop || idx >= j->total_rows)
+            break;
+        int b = (int)(idx / per_b);
+        long rem = idx % per_b;
+        int st = attend_prefill_row(j, b, (int)(rem / j->Hq), (int)(rem % j->Hq), &sc);
+        if (st != ORACLE_OK) {
+            pthread_mutex_lock(&j->lock);
+            j->status = st;
+            pthread_mutex_unlock(&j->lock);
+        }
+    }
+    scratch_free(&sc);
+    return NULL;
+}
+
+int oracle_prefill_attention(int B, int n_new, int Hq, int Hkv, int D, int P, int num_pages, int max_pages,
+                             const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                             const int32_t *block_table, const int32_t *seq_lens, double scale, double *out,
+                             double *lse, int nthreads)
+{
+    if (B < 0 || n_new < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || P <= 0 || !out)
+        return ORACLE_EARG;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] < n_new || seq_lens[b] > (long)max_pages * P)
+            return ORACLE_EARG;
+    prefill_job j;
+    memset(&j, 0, sizeof j);
+    j.B = B; j.n_new = n_new; j.Hq = Hq; j.Hkv = Hkv; j.D = D; j.P = P;
+    j.num_pages = num_pages; j.max_pages = max_pages;
+    j.q = q; j.k_pages = k_pages; j.v_pages = v_pages;
+    j.block_table = block_table; j.seq_lens = seq_lens;
+    j.scale = scale; j.out = out; j.lse = lse;
+    j.total_rows = (long)B * n_new * Hq;
+    j.status = ORACLE_OK;
+    pthread_mutex_init(&j.lock, NULL);
+    int nt = resolve_threads(nthreads);
+    if (nt > j.total_rows)
+        nt = j.total_rows > 0 ? (int)j.total_rows : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!th)
+        return ORACLE_ENOMEM;
+    for (int i = 0; i < nt; ++i)
+        pthread_create(&th[i], NULL, prefill_worker, &j);
+    for (int i = 0; i < nt; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&j.lock);
+    return j.status;
+}
+
+/*
  * Log-sum-exp merge of S partial attentions over disjoint token ranges of
  * the same rows (the split-KV reduction named for long contexts):
  *   M   = max_s lse_s

@@ -1,5 +1,6 @@
 """Planted mistakes: each mutant copy of the oracle's C source must fail at
-least one pin in test_oracle_pins.py or test_oracle_tails_pins.py.
+least one pin in test_oracle_pins.py, test_oracle_tails_pins.py or
+test_oracle_prefill_pins.py.
 
 This checks that the pins are sharp enough to catch the plausible slips a
 hand-written attention oracle can make (wrong GQA head, swapped K/V, dropped
@@ -7,7 +8,8 @@ scale or max, wrong row order, off-by-one mask, broken merge weight, wrong
 append slot; for per-decoder tails: another decoder's tail, the shared table
 used for the tail, a dropped tail, an un-rebased tail position).  Mutants
 are compiled on the CPU into a temporary directory; the real oracle is never
-modified.
+modified.  Partial prefill: attention that is not causal, that excludes the
+token itself, or that writes rows head-major.
 """
 import os
 import subprocess
@@ -16,6 +18,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_pins as pins
+import tests.test_oracle_prefill_pins as prefill_pins
 import tests.test_oracle_tails_pins as tail_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "shkv_oracle.c")
@@ -41,10 +44,16 @@ MUTANTS = {
     "tail_dropped": ("const int n = j->seq_lens[b] + j->tail_lens[(long)b * j->N + m];",
                      "const int n = j->seq_lens[b];"),
     "tail_position_not_rebased": ("t = i - L;", "t = i;"),
+    # partial-prefill attention
+    "prefill_not_causal": ("const int n = L - j->n_new + i + 1;", "const int n = L;"),
+    "prefill_excludes_itself": ("const int n = L - j->n_new + i + 1;", "const int n = L - j->n_new + i;"),
+    "prefill_row_order": ("const long row = ((long)b * j->n_new + i) * j->Hq + h;",
+                          "const long row = ((long)b * j->Hq + h) * j->n_new + i;"),
 }
 
 PIN_TESTS = ([getattr(pins, n) for n in dir(pins) if n.startswith("test_")] +
-             [getattr(tail_pins, n) for n in dir(tail_pins) if n.startswith("test_")])
+             [getattr(tail_pins, n) for n in dir(tail_pins) if n.startswith("test_")] +
+             [getattr(prefill_pins, n) for n in dir(prefill_pins) if n.startswith("test_")])
 
 
 @pytest.fixture(scope="module")
