@@ -36,7 +36,7 @@ EXPORTS = [
     "shkv_tails_get_lens", "shkv_tails_append", "shkv_decode_tails_workspace_size",
     "shkv_decode_attention_tails", "shkv_pages_create", "shkv_pages_destroy", "shkv_pages_acquire",
     "shkv_pages_publish", "shkv_pages_release", "shkv_pages_alloc_transfer", "shkv_pages_stats",
-    "shkv_pages_refcount",
+    "shkv_pages_refcount", "shkv_prefill_attention",
 ]
 
 SHKV_CONSUMER_MMA_SYNC = 0
@@ -133,6 +133,7 @@ def load() -> ctypes.CDLL:
         "shkv_pages_alloc_transfer": [vp, i32, i32p],
         "shkv_pages_stats": [vp, ctypes.POINTER(shkv_pages_info)],
         "shkv_pages_refcount": [vp, i32, ctypes.POINTER(i32)],
+        "shkv_prefill_attention": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -275,3 +276,9 @@ def shkv_pages_create(num_pages: int, page_size: int) -> int:
 
 def shkv_pages_destroy(pages: int) -> None:
     _check(load().shkv_pages_destroy(pages), "shkv_pages_destroy")
+
+
+def shkv_prefill_attention(pool: int, batch: int, n_new: int, hq: int, q: int, scale: float, out: int,
+                           lse_out: int, stream: int) -> None:
+    _check(load().shkv_prefill_attention(pool, batch, n_new, hq, q, scale, out, lse_out, stream),
+           "shkv_prefill_attention")

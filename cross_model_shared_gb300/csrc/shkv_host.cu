@@ -23,6 +23,10 @@ int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
 cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream);
+int prefill_stages();
+uint32_t prefill_smem_bytes(int stages);
+cudaError_t launch_prefill_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const PrefillParams &p, uint32_t smem,
+                                int grid, cudaStream_t stream);
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
                          const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream);
 }  // namespace shkv
@@ -559,6 +563,53 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
         return SHKV_ERR_INVALID_ARG;
     return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, workspace,
                        workspace_bytes, stream);
+}
+
+shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new, int32_t hq_per_model,
+                                   const void *q, float scale, void *out, float *lse_out, void *stream)
+{
+    if (!pool || !q || !out || batch < 1 || n_new < 1 || hq_per_model < 1 || !isfinite(scale))
+        return SHKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || ((uintptr_t)lse_out & 3u))
+        return SHKV_ERR_INVALID_ARG;
+    const shkv_pool_config &c = pool->cfg;
+    if (batch > c.max_batch)
+        return SHKV_ERR_INVALID_ARG;
+    if (batch > SHKV_MAX_BATCH || hq_per_model % c.num_kv_heads || c.head_dim != 128 || pool->tails_view)
+        return SHKV_ERR_UNSUPPORTED;
+    const int group = hq_per_model / c.num_kv_heads;
+    if (group > 128)
+        return SHKV_ERR_UNSUPPORTED;
+    PrefillParams p;
+    memset(&p, 0, sizeof p);
+    for (int b = 0; b < batch; ++b) {
+        if (pool->lens[b] < n_new)
+            return SHKV_ERR_INVALID_ARG;        // the new tokens must already be in the pool
+        p.lens[b] = pool->lens[b];
+    }
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    p.block_table = c.block_table;
+    p.seq_lens = c.seq_lens;
+    p.err = c.error_word;
+    p.batch = batch;
+    p.n_new = n_new;
+    p.hq = hq_per_model;
+    p.hkv = c.num_kv_heads;
+    p.group = group;
+    p.tpt = 128 / group;
+    p.tiles = (n_new + p.tpt - 1) / p.tpt;
+    p.page_size = c.page_size;
+    p.max_pages = c.max_pages_per_seq;
+    p.num_pages = c.num_pages;
+    p.stages = prefill_stages();
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const int64_t grid = (int64_t)batch * c.num_kv_heads * p.tiles;
+    if (grid > INT32_MAX)
+        return SHKV_ERR_UNSUPPORTED;
+    return cuda_status(launch_prefill_umma(pool->tm_k2, pool->tm_v2, p, prefill_smem_bytes(p.stages), (int)grid,
+                                           (cudaStream_t)stream));
 }
 
 shkv_status shkv_tails_create(shkv_pool *pool, const shkv_tails_config *tc, shkv_tails **out)

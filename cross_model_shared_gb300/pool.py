@@ -144,6 +144,26 @@ class SharedKVPool:
         c = N.shkv_decode_consumer(self.handle, n_models, hq)
         return "tcgen05" if c == N.SHKV_CONSUMER_TCGEN05 else "mma.sync"
 
+    def prefill_attention(self, q: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, return_lse: bool = False, stream=None):
+        """Causal attention of the n_new tokens just appended (PrefillShare
+        Sec. 3.3 partial prefill): q bf16 [B, n_new, hq, head_dim]; new token
+        i attends the cached prefix and the new tokens up to itself."""
+        _require(q, torch.bfloat16, "q")
+        B, T, H, D = q.shape
+        if D != self.head_dim:
+            raise ValueError("q must be [B, n_new, hq, head_dim]")
+        if scale is None:
+            scale = 1.0 / float(np.sqrt(D))
+        if out is None:
+            out = torch.empty_like(q)
+        _require(out, torch.bfloat16, "out")
+        if return_lse and lse is None:
+            lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+        N.shkv_prefill_attention(self.handle, B, T, H, q.data_ptr(), float(scale), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, _stream_ptr(stream))
+        return (out, lse) if (return_lse or lse is not None) else out
+
     def check_errors(self, stream=None) -> int:
         """Synchronize and return (then clear) the device error bits."""
         return N.shkv_check_errors(self.handle, _stream_ptr(stream))

@@ -174,6 +174,28 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
                                   void *stream);
 
 /*
+ * Causal partial-prefill attention (PrefillShare Sec. 3.3: on a prefix-cache
+ * hit the shared prefill module runs only on the new tokens, extending the
+ * cached prefix).  Call after shkv_append_kv has put the n_new tokens' K/V
+ * into the pool: request b then holds L_b tokens, the last n_new of them new,
+ * and new token i (position L_b - n_new + i) attends every key at a position
+ * <= its own -- the whole cached prefix and the new tokens causally.
+ *   q        device bf16 [batch, n_new, hq_per_model, head_dim] (the prefill
+ *            module's query heads; head h uses KV head h / (Hq / Hkv))
+ *   out      device bf16, same shape;  lse_out device fp32 [batch, n_new,
+ *            hq_per_model] (natural log) or NULL
+ * Tensor-core kernel (tcgen05): one CTA per (request, KV head, tile of
+ * floor(128 / G) new tokens), the G query heads of a KV head stacked with
+ * the tokens on the MMA M dimension.
+ * Supported: head_dim 128, page size 16 or 32, G <= 128, batch <=
+ * SHKV_MAX_BATCH.  Errors: SHKV_ERR_INVALID_ARG (null / misaligned pointers,
+ * a request shorter than n_new), SHKV_ERR_UNSUPPORTED, SHKV_ERR_CUDA; page
+ * and length disagreements set the error word as in decode.
+ */
+shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new, int32_t hq_per_model,
+                                   const void *q, float scale, void *out, float *lse_out, void *stream);
+
+/*
  * Per-decoder unique tails (PrefillShare Sec. 3.3-4 and Eqs. 8-9: decode
  * starts from the shared base cache and each decoder extends it with its own
  * generated-token cache Delta C_t; the shared prefix is stored once, each

@@ -2,9 +2,14 @@
 inputs, read pages back for the oracle, and apply the stated tolerance.
 
 Tolerance (bf16 inputs, fp32 accumulation, fp64 oracle): elementwise
-max |gpu - ref| <= 1e-2, and per-row normwise max_k |gpu - ref| / max_k |ref|
-<= 2e-2 (outputs are convex combinations of V rows whose magnitude shrinks
-with context length, so an elementwise relative error is ill-posed near 0).
+|gpu - ref| <= 1e-2 beyond the rounding of the bf16 output itself, i.e.
+<= 1e-2 + half a bf16 ulp of ref (the output format is bf16, and an exact
+result of magnitude >= 2.56 cannot be stored within 1e-2: around 4.6, for
+instance, bf16 values are 2^-5 apart; for the averaged outputs of long
+contexts the extra term is below 0.005), and per-row normwise
+max_k |gpu - ref| / max_k |ref| <= 2e-2 (outputs are convex combinations of
+V rows whose magnitude shrinks with context length, so an elementwise
+relative error is ill-posed near 0).
 """
 import numpy as np
 import torch
@@ -39,15 +44,25 @@ def make_pool(wl: W.Workload, k, v, lens=None, extra_max_batch: int = 0) -> Shar
     return pool
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values at |x| (8 significant bits)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
+
+
 def compare(out_gpu: torch.Tensor, ref: np.ndarray, lse_gpu=None, lse_ref=None, what=""):
     got = out_gpu.float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
     err = np.abs(got - ref)
     abs_err = float(err.max()) if err.size else 0.0
+    beyond = err - bf16_half_ulp(ref)
+    beyond_err = float(beyond.max()) if err.size else 0.0
     denom = np.maximum(np.abs(ref).max(axis=-1), 1e-30)
     rel_err = float((err.max(axis=-1) / denom).max()) if err.size else 0.0
-    assert abs_err <= ABS_TOL, f"{what}: max abs error {abs_err:.3e} > {ABS_TOL}"
+    assert beyond_err <= ABS_TOL, (f"{what}: max abs error beyond bf16 output rounding {beyond_err:.3e} > {ABS_TOL} "
+                                   f"(raw max {abs_err:.3e})")
     assert rel_err <= REL_TOL, f"{what}: max row-relative error {rel_err:.3e} > {REL_TOL}"
     if lse_gpu is not None:
         lg = lse_gpu.cpu().numpy().astype(np.float64)
