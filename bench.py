@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--prefix-pages", action="store_true",
                     help="host-side page-manager run: a seeded multi-agent workflow over the prefix pool")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="time the causal partial prefill of this many new tokens per request "
+                         "(appended after the workload's cached prefixes)")
     ap.add_argument("--tail-tokens", type=int, default=0,
                     help="give every decoder its own unique tail of about this many tokens (seeded, "
                          "uniform in [T/2, 3T/2]) and time the decode with tails")
@@ -492,6 +495,82 @@ def run_prefix_pages(args):
     print(json.dumps(line), flush=True)
 
 
+def measured_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_gpu_prefill(args):
+    """Causal partial prefill of T new tokens over each request's cached
+    prefix (PrefillShare Sec. 3.3), on the tensor cores."""
+    import torch
+    from cross_model_shared_gb300 import SharedKVPool
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    base = load_workload(args)
+    T = args.prefill_tokens
+    wl = W.custom_workload(f"{base.name}+prefill{T}", B=base.B, N=1, Hq=base.Hq, Hkv=base.Hkv, D=base.D, P=base.P,
+                           lens_prefill=base.lens_prefill, n_append=T, seed=base.seed)
+    k_dev, v_dev = W.gen_pool_device(wl, device=dev)
+    pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
+                        device=dev, k_pages=k_dev, v_pages=v_dev, initial_seq_lens=wl.lens_final)
+    pool.block_table.copy_(torch.from_numpy(wl.block_table).to(dev))
+    g = torch.Generator(device=dev).manual_seed(wl.seed + 5)
+    q = torch.randn((wl.B, T, wl.Hq, wl.D), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, T, wl.Hq), dtype=torch.float32, device=dev)
+
+    def step():
+        pool.prefill_attention(q, scale=wl.scale, out=out, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if pool.check_errors():
+        raise RuntimeError("device error bits during warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    clocks = sampler.stop()
+    if pool.check_errors():
+        raise RuntimeError("device error bits in the timed region")
+    ms = ev0.elapsed_time(ev1) / args.steps
+    prefix = wl.lens_final.astype(np.int64) - T
+    keys = int(sum(int(pf) * T + T * (T + 1) // 2 for pf in prefix))      # sum over new tokens of keys attended
+    flops = 4.0 * keys * wl.Hq * wl.D                                        # QK and PV, 2 flops per MAC
+    kv_bytes = W.unique_kv_bytes(wl)
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, kind = measured_tensor_peak()
+    line = {
+        "metric": "partial-prefill attention: TFLOP/s (% of bf16 tensor peak)", "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "new_tokens": T, "hq": wl.Hq, "hkv": wl.Hkv,
+                   "head_dim": wl.D, "page_size": wl.P, "mean_prefix": float(prefix.mean()),
+                   "kv_bytes": kv_bytes, "flops": flops, "parallelism": "replicas x1"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": kind, "traffic": None, "kernel": "shkv_prefill_umma_kernel",
+                     "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -656,6 +735,9 @@ def main():
     args = parse_args()
     if args.prefix_pages:
         run_prefix_pages(args)
+        return
+    if args.prefill_tokens and args.impl == "shkv":
+        run_gpu_prefill(args)
         return
     if args.tail_tokens and args.impl == "shkv":
         run_gpu_tails(args)

@@ -271,26 +271,35 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
             alive = false;
         }
         const uint32_t pmask = tagged & 0xffu;
-        // keys this row may see in the stage: [key0, min(pos, ...)]; whole stage if below the diagonal
-        const int nvis = row_ok ? min(kKT, pos - key0 + 1) : 0;
-        const bool all_pages = pmask == (1u << (kKT / P)) - 1u;
-        auto visible = [&](int col) -> bool { return col < nvis && ((pmask >> (col >> log2P)) & 1u); };
-        // pass 1: the stage max of this row (base 2)
-        float mt = -INFINITY;
+        // this row's 128 scores, read once; the S buffer is free right after
+        uint32_t sv[kKT];
         if (alive) {
             tc_fence_after();
-#pragma unroll 1
-            for (int c32 = 0; c32 < kKT / 32; ++c32) {
-                uint32_t sv[32];
-                tmem_ld32(tmem + lane_base + kPColS + (uint32_t)(buf * kKT + c32 * 32), sv);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int col = c32 * 32 + e;
-                    if ((nvis == kKT && all_pages) || visible(col))
-                        mt = fmaxf(mt, __uint_as_float(sv[e]) * sl2);
-                }
+            for (int c32 = 0; c32 < kKT / 32; ++c32)
+                tmem_ld32_nowait(tmem + lane_base + kPColS + (uint32_t)(buf * kKT + c32 * 32), sv + 32 * c32);
+            tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(pf_sfree(c, buf));
+        // keys this row may see: [key0, key0 + nvis), on pages that were copied
+        const int nvis = row_ok ? min(kKT, pos - key0 + 1) : 0;
+        const bool all_pages = pmask == (1u << (kKT / P)) - 1u;
+        const bool dense = alive && nvis == kKT && all_pages;    // below the diagonal: no mask
+        if (!dense) {
+#pragma unroll
+            for (int col = 0; col < kKT; ++col) {
+                const bool vis = alive && col < nvis && ((pmask >> (col >> log2P)) & 1u);
+                sv[col] = vis ? sv[col] : __float_as_uint(-INFINITY);
             }
         }
+        float smax = -INFINITY;
+#pragma unroll
+        for (int col = 0; col < kKT; ++col)
+            smax = fmaxf(smax, __uint_as_float(sv[col]));
+        const float mt = smax * sl2;                              // sl2 > 0: max of the scaled scores
         // lazy refresh of the running max: this row's O is rescaled only when
         // the max rises by more than 2^kPRescaleLog2.  tcgen05.ld/st are
         // warp-wide, so a warp with any such row rescales all its rows (by 1
@@ -319,39 +328,23 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
         if (need)
             m_use = mt;
         const float mu = m_use == -INFINITY ? 0.f : m_use;
-        // pass 2: P row (bf16) over the consumed K tile, and the row sum
+        // P row (bf16) over the consumed K tile: keys 0..63 in half 0, 64..127 in half 1
         uint8_t *prow = c.smem + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)r * 128u;
-#pragma unroll 1
-        for (int c32 = 0; c32 < kKT / 32; ++c32) {
-            uint32_t sv[32];
+#pragma unroll
+        for (int ch = 0; ch < kKT / 8; ++ch) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = ch * 8 + 2 * e;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(sv[col]), sl2, -mu));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(sv[col + 1]), sl2, -mu));
+                lsum += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
             if (alive)
-                tmem_ld32(tmem + lane_base + kPColS + (uint32_t)(buf * kKT + c32 * 32), sv);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                const int col = c32 * 32 + e;
-                const bool v0 = (nvis == kKT && all_pages) || visible(col);
-                const bool v1 = (nvis == kKT && all_pages) || visible(col + 1);
-                const float p0 = v0 ? ex2_approx(__uint_as_float(sv[e]) * sl2 - mu) : 0.f;
-                const float p1 = v1 ? ex2_approx(__uint_as_float(sv[e + 1]) * sl2 - mu) : 0.f;
-                pk[e / 2] = pack_bf16x2(p0, p1);
-                lsum += __uint_as_float(pk[e / 2] << 16) + __uint_as_float(pk[e / 2] & 0xffff0000u);
-            }
-            if (alive) {
-                // keys c32*32 .. +31: half c32 / 2, 16-byte chunks 4*(c32 % 2) .. +3 of row r
-                uint8_t *hrow = prow + (uint32_t)(c32 >> 1) * (128u * 128u);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int gch = (c32 & 1) * 4 + ch;
-                    *reinterpret_cast<uint4 *>(hrow + ((gch ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                }
-            }
+                *reinterpret_cast<uint4 *>(prow + (uint32_t)(ch >> 3) * (128u * 128u) + (((ch & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(pf_sfree(c, buf));
         // V rows of keys that no row may use in this stage (past the request's
         // end, or on a skipped page) may hold stale or non-finite bits: zero
         // them (thread r takes key row r)
