@@ -271,80 +271,116 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
             alive = false;
         }
         const uint32_t pmask = tagged & 0xffu;
-        // this row's 128 scores, read once; the S buffer is free right after
-        uint32_t sv[kKT];
-        if (alive) {
-            tc_fence_after();
+        // keys this row may see: [key0, key0 + nvis), on pages that were copied
+        const int nvis = row_ok ? min(kKT, pos - key0 + 1) : 0;
+        const bool all_pages = pmask == (1u << (kKT / P)) - 1u;
+        const bool dense = alive && nvis == kKT && all_pages;    // below the diagonal: no mask
+        const uint32_t srow = tmem + lane_base + kPColS + (uint32_t)(buf * kKT);
+        uint8_t *prow = c.smem + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)r * 128u;
+        // 32 scores of this row from TMEM, masked (-inf where invisible)
+        auto load_chunk = [&](int c32, uint32_t (&sv)[32]) {
+            tmem_ld32(srow + (uint32_t)(c32 * 32), sv);
+            if (!dense) {
 #pragma unroll
-            for (int c32 = 0; c32 < kKT / 32; ++c32)
-                tmem_ld32_nowait(tmem + lane_base + kPColS + (uint32_t)(buf * kKT + c32 * 32), sv + 32 * c32);
-            tmem_wait_ld();
+                for (int e = 0; e < 32; ++e) {
+                    const int col = c32 * 32 + e;
+                    const bool vis = alive && col < nvis && ((pmask >> (col >> log2P)) & 1u);
+                    sv[e] = vis ? sv[e] : __float_as_uint(-INFINITY);
+                }
+            }
+        };
+        // P of 32 keys (bf16) over the consumed K tile: keys 0..63 in half 0, 64..127 in half 1
+        auto emit_chunk = [&](int c32, const uint32_t (&sv)[32], float mu, bool store) -> float {
+            float part = 0.f;
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = q8 * 8 + 2 * e;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl2, -mu));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl2, -mu));
+                    part += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                const int ch = c32 * 4 + q8;                      // 16-byte chunk of the 256-byte row
+                if (store)
+                    *reinterpret_cast<uint4 *>(prow + (uint32_t)(ch >> 3) * (128u * 128u) +
+                                               (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            return part;
+        };
+        if (alive)
+            tc_fence_after();
+        // a row with no running max yet takes this stage's max first
+        if (__any_sync(0xffffffffu, alive && m_use == -INFINITY && nvis > 0)) {
+            float cm = -INFINITY;
+#pragma unroll 1
+            for (int c32 = 0; c32 < kKT / 32; ++c32) {
+                uint32_t sv[32];
+                load_chunk(c32, sv);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    cm = fmaxf(cm, __uint_as_float(sv[e]));
+            }
+            if (m_use == -INFINITY)
+                m_use = cm * sl2;                                 // sl2 > 0; stays -inf if nothing is visible
+        }
+        // stream the row: exponents against the running max, tracking this stage's max
+        const float l_before = lsum;
+        const float mu = m_use == -INFINITY ? 0.f : m_use;
+        float cmax = -INFINITY, part = 0.f;
+#pragma unroll 1
+        for (int c32 = 0; c32 < kKT / 32; ++c32) {
+            uint32_t sv[32];
+            load_chunk(c32, sv);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                cmax = fmaxf(cmax, __uint_as_float(sv[e]));
+            part += emit_chunk(c32, sv, mu, alive);
+        }
+        lsum += part;
+        // lazy refresh: a row whose max rose by more than 2^kPRescaleLog2
+        // rescales its O (after the previous PV) and redoes this stage's P
+        // from S, still in TMEM.  tcgen05.ld/st are warp-wide, so the whole
+        // warp takes part (scale 1, no rewrite, where nothing moved).
+        const float mt = cmax * sl2;
+        const bool need = alive && m_use != -INFINITY && mt > m_use + kPRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx(m_use - mt) : 1.f;
+            if (k >= 1) {
+                const int kp = k - 1;
+                wait(pf_empty(c, kp % c.stages), (uint32_t)((kp / c.stages) & 1));
+                if (alive) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c32 = 0; c32 < kPD / 32; ++c32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
+                    }
+                }
+            }
+            if (need)
+                m_use = mt;
+            float redo = 0.f;
+#pragma unroll 1
+            for (int c32 = 0; c32 < kKT / 32; ++c32) {
+                uint32_t sv[32];
+                if (alive)
+                    load_chunk(c32, sv);
+                redo += emit_chunk(c32, sv, m_use, alive && need);
+            }
+            if (need)
+                lsum = l_before * alpha + redo;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
             mbar_arrive(pf_sfree(c, buf));
-        // keys this row may see: [key0, key0 + nvis), on pages that were copied
-        const int nvis = row_ok ? min(kKT, pos - key0 + 1) : 0;
-        const bool all_pages = pmask == (1u << (kKT / P)) - 1u;
-        const bool dense = alive && nvis == kKT && all_pages;    // below the diagonal: no mask
-        if (!dense) {
-#pragma unroll
-            for (int col = 0; col < kKT; ++col) {
-                const bool vis = alive && col < nvis && ((pmask >> (col >> log2P)) & 1u);
-                sv[col] = vis ? sv[col] : __float_as_uint(-INFINITY);
-            }
-        }
-        float smax = -INFINITY;
-#pragma unroll
-        for (int col = 0; col < kKT; ++col)
-            smax = fmaxf(smax, __uint_as_float(sv[col]));
-        const float mt = smax * sl2;                              // sl2 > 0: max of the scaled scores
-        // lazy refresh of the running max: this row's O is rescaled only when
-        // the max rises by more than 2^kPRescaleLog2.  tcgen05.ld/st are
-        // warp-wide, so a warp with any such row rescales all its rows (by 1
-        // where nothing moved), after the PV of the previous stage is done.
-        const bool need = alive && mt > m_use + kPRescaleLog2;
-        const bool have_o = m_use != -INFINITY;
-        if (__any_sync(0xffffffffu, need && have_o)) {
-            const int kp = k - 1;
-            wait(pf_empty(c, kp % c.stages), (uint32_t)((kp / c.stages) & 1));
-            if (alive) {
-                tc_fence_after();
-                const float alpha = (need && have_o) ? ex2_approx(m_use - mt) : 1.f;
-#pragma unroll 1
-                for (int c32 = 0; c32 < kPD / 32; ++c32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
-                }
-                tc_fence_before();
-                lsum *= alpha;
-            }
-        }
-        if (need)
-            m_use = mt;
-        const float mu = m_use == -INFINITY ? 0.f : m_use;
-        // P row (bf16) over the consumed K tile: keys 0..63 in half 0, 64..127 in half 1
-        uint8_t *prow = c.smem + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)r * 128u;
-#pragma unroll
-        for (int ch = 0; ch < kKT / 8; ++ch) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = ch * 8 + 2 * e;
-                const float p0 = ex2_approx(fmaf(__uint_as_float(sv[col]), sl2, -mu));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(sv[col + 1]), sl2, -mu));
-                lsum += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
-            }
-            if (alive)
-                *reinterpret_cast<uint4 *>(prow + (uint32_t)(ch >> 3) * (128u * 128u) + (((ch & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
         // V rows of keys that no row may use in this stage (past the request's
         // end, or on a skipped page) may hold stale or non-finite bits: zero
         // them (thread r takes key row r)
