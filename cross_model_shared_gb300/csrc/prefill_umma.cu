@@ -7,22 +7,28 @@
 // n_new of them new; new token i sits at position L_b - n_new + i and
 // attends every key at a position <= its own.
 //
-// One CTA per (request, KV head, tile of new tokens).  The tile's 128 MMA rows
-// are TPT = floor(128 / G) new tokens x the G query heads of the KV head
-// (row r = i * G + j), so every K/V page is read once for the whole group.
-// Per 128-key stage:
-//   S[r, key]  = sum_d Q[r, d] K[key, d]      M = 128 rows, N = 128 keys
-//   O[r, d]   += sum_key P[r, key] V[key, d]  M = 128 rows, N = 128 = D
-// S (two buffers) and O live in TMEM; a softmax thread owns one row (its TMEM
-// lane), keeps its running max and sum, and rescales its own row of O lazily
-// (only when the max rises by more than 2^kRescaleLog2).  P (bf16) is written
-// over the stage's K tile, which the QK MMA has consumed.  Key stages past
-// the tile's last position are never loaded; on the diagonal the causal mask
-// is applied per element.
+// A query tile is TPT = floor(128 / G) new tokens x the G query heads of one
+// KV head: 128 MMA rows (row r = i * G + j), so every K/V page is read once
+// for the whole group.  One CTA takes two consecutive tiles X = A, B of one
+// (request, KV head) and streams 128-key stages of K/V through shared memory
+// once for both (256 query rows per K/V byte).  Per stage and tile:
+//   S_X[r, key]  = sum_d Q_X[r, d] K[key, d]      M = 128 rows, N = 128 keys
+//   O_X[r, d]   += sum_key P_X[r, key] V[key, d]  M = 128 rows, N = 128 = D
+// TMEM holds S_A, S_B, O_A, O_B (4 x 128 columns).  A softmax thread owns one
+// row of one tile (its TMEM lane): it reads its scores twice, first for the
+// stage maximum, then to exponentiate them against its running maximum, and
+// writes P (bf16 pairs) over the first 64 columns of its S, from where the PV
+// product reads it.  The running maximum moves only when the stage maximum
+// exceeds it by more than 2^kPRescaleLog2; the thread then rescales its row
+// of O first.  The two tiles alternate on the tensor core: while one tile's
+// softmax runs, the other tile's PV and next QK execute.  Key stages past a
+// tile's last position are skipped for that tile (and never loaded past the
+// pair's last position); on the diagonal the causal mask is per element.
 //
-// Roles (224 threads): warps 0-3 softmax (row = TMEM lane), warp 4 QK issuer,
-// warp 5 PV issuer (its commit frees the ring slot), warp 6 producer (TMA of
-// K and V page halves, one box per lane).
+// Roles (384 threads): warps 0-3 softmax of tile A, warps 4-7 of tile B (row
+// = TMEM lane), warp 8 QK issuer (its commit frees the K half of a ring slot),
+// warp 9 PV issuer (frees the V half), warps 10 and 11 the K and V producers
+// (TMA of page halves, one box per lane).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,33 +45,91 @@ namespace {
 constexpr int kKT = 128;                 // keys per stage
 constexpr int kPD = 128;                 // head dim
 constexpr int kPHalves = kPD / 64;
-constexpr int kPThreads = 224;
-constexpr int kPSoftmaxWarps = 4;
-constexpr int kPQkWarp = 4;
-constexpr int kPPvWarp = 5;
-constexpr int kPProducerWarp = 6;
+constexpr int kPThreads = 384;
+constexpr int kPQkWarp = 8;
+constexpr int kPPvWarp = 9;
+constexpr int kPKWarp = 10;
+constexpr int kPVWarp = 11;
+constexpr int kPGroupWarps = 4;          // softmax warps per tile
 constexpr uint32_t kPTmemCols = 512;
-constexpr uint32_t kPColS = 0;           // S buffers at 0 and 128
-constexpr uint32_t kPColO = 256;
 constexpr float kPRescaleLog2 = 8.f;
-constexpr int kPMaxStages = 3;
+constexpr int kPStages = 2;
+constexpr int kPTilesPerCta = 2;
+
+__device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)(x * 128); }        // P over its first 64
+__device__ __forceinline__ uint32_t col_o(int x) { return (uint32_t)(256 + x * 128); }
+
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, issued by one thread: A is 128 lanes
+// (rows) x K columns of packed bf16 pairs, the lower half the lower k.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+                 "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Bounded wait that sleeps on the barrier instead of spinning: each try_wait
+// suspends the thread until the phase completes or ~20 us pass, so waiting
+// warps leave the issue slots to the softmax warps of their SM sub-partition.
+// Gives up like mbar_wait_bounded (abort flag, or SHKV_ERRF_TIMEOUT after
+// kWaitLimitNs).
+__device__ __forceinline__ bool pf_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ bool pf_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag, uint32_t *err)
+{
+    if (pf_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (pf_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1u;
+            atomicOr(err, SHKV_ERRF_TIMEOUT);
+            return false;
+        }
+    }
+}
 
 struct PfSmem {
     uint32_t ring, stage_bytes, qtile, bars, meta, misc, tslot, total;
 };
 
-// ring slots of [K | V][half][128 keys][128 B], then the Q tile
-// [half][128 rows][128 B] (both 128-byte swizzled), then the barriers:
-// full[S], empty[S], p_full[S], s_full[2], s_free[2], fin
-__host__ __device__ inline PfSmem pf_layout(int stages)
+// ring slots of [K | V][half][128 keys][128 B], then the two Q tiles
+// [tile][half][128 rows][128 B] (all 128-byte swizzled), then the barriers:
+// full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[2], p_full[2], pv_done[2], fin
+__host__ __device__ inline PfSmem pf_layout()
 {
     PfSmem u;
     u.stage_bytes = (uint32_t)(2 * kKT * kPD * 2);
     u.ring = 0;
-    u.qtile = (uint32_t)stages * u.stage_bytes;
-    u.bars = u.qtile + (uint32_t)(kPHalves * 128 * 128);
-    u.meta = u.bars + (uint32_t)((3 * stages + 5) * 8);
-    u.misc = u.meta + (uint32_t)(stages * 4);
+    u.qtile = (uint32_t)kPStages * u.stage_bytes;
+    u.bars = u.qtile + (uint32_t)(kPTilesPerCta * kPHalves * 128 * 128);
+    u.meta = u.bars + (uint32_t)((4 * kPStages + 7) * 8);
+    u.misc = u.meta + (uint32_t)(kPStages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;
     return u;
@@ -75,176 +139,211 @@ struct PfCtx {
     uint8_t *smem;
     uint32_t base;
     PfSmem lay;
-    int stages;
     volatile uint32_t *abort_flag;
 };
 
 __device__ __forceinline__ uint32_t pbar(const PfCtx &c, int i) { return c.base + c.lay.bars + 8u * i; }
-__device__ __forceinline__ uint32_t pf_full(const PfCtx &c, int s) { return pbar(c, s); }
-__device__ __forceinline__ uint32_t pf_empty(const PfCtx &c, int s) { return pbar(c, c.stages + s); }
-__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int s) { return pbar(c, 2 * c.stages + s); }
-__device__ __forceinline__ uint32_t pf_sfull(const PfCtx &c, int b) { return pbar(c, 3 * c.stages + b); }
-__device__ __forceinline__ uint32_t pf_sfree(const PfCtx &c, int b) { return pbar(c, 3 * c.stages + 2 + b); }
-__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 3 * c.stages + 4); }
+__device__ __forceinline__ uint32_t pf_full(const PfCtx &c, bool v, int s) { return pbar(c, (v ? kPStages : 0) + s); }
+__device__ __forceinline__ uint32_t pf_empty(const PfCtx &c, bool v, int s)
+{
+    return pbar(c, (v ? 3 : 2) * kPStages + s);
+}
+__device__ __forceinline__ uint32_t pf_sfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + x); }
+__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 2 + x); }
+__device__ __forceinline__ uint32_t pf_pvdone(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 4 + x); }
+__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 6); }
 __device__ __forceinline__ uint32_t pf_slot(const PfCtx &c, int s)
 {
     return c.base + c.lay.ring + (uint32_t)s * c.lay.stage_bytes;
 }
+__device__ __forceinline__ uint32_t ring_par(int k) { return (uint32_t)((k / kPStages) & 1); }
 
-// the tile this CTA owns
+// the pair of tiles this CTA owns
 struct Tile {
-    int b, g, i0, ntok;          // request, KV head, first new token, new tokens in the tile
+    int b, g;
     int L, prefix;               // request length (with the new tokens), cached tokens before them
-    int nst;                     // key stages: keys 0 .. last position
+    int i0[2], ntok[2];          // first new token and new tokens of tiles A and B (B may be empty)
+    int nst[2];                  // key stages each tile attends: keys 0 .. its last position
+    int nst_all;                 // stages loaded: the larger of the two
 };
 
 __device__ __forceinline__ Tile pf_tile(const PrefillParams &p)
 {
     Tile t;
+    const int pairs = (p.tiles + kPTilesPerCta - 1) / kPTilesPerCta;
     int idx = blockIdx.x;
-    const int qt = idx % p.tiles;
-    idx /= p.tiles;
+    const int tp = idx % pairs;
+    idx /= pairs;
     t.g = idx % p.hkv;
     t.b = idx / p.hkv;
-    t.i0 = qt * p.tpt;
-    t.ntok = min(p.tpt, p.n_new - t.i0);
     t.L = p.lens[t.b];
     t.prefix = t.L - p.n_new;
-    const int last_pos = t.prefix + t.i0 + t.ntok - 1;
-    t.nst = last_pos / kKT + 1;
+#pragma unroll
+    for (int x = 0; x < kPTilesPerCta; ++x) {
+        t.i0[x] = (kPTilesPerCta * tp + x) * p.tpt;
+        t.ntok[x] = max(0, min(p.tpt, p.n_new - t.i0[x]));
+        t.nst[x] = t.ntok[x] > 0 ? (t.prefix + t.i0[x] + t.ntok[x] - 1) / kKT + 1 : 0;
+    }
+    t.nst_all = max(t.nst[0], t.nst[1]);
     return t;
 }
 
 // ---------------------------------------------------------------------------
-// producer: stage k = keys [128k, 128k + 128), 128/P pages, K and V halves
+// producers: stage k = keys [128k, 128k + 128), 128/P pages; one warp copies
+// the K halves of the pages, another the V halves (one box per lane).  The V
+// producer records which pages it copied in the slot's word (a V half is
+// released only after both tiles' softmax of its stage have read the word).
 // ---------------------------------------------------------------------------
-__device__ void pf_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const PrefillParams &p,
-                            const PfCtx &c, const Tile &t)
+template <bool kIsV>
+__device__ void pf_producer(const CUtensorMap *tm, const PrefillParams &p, const PfCtx &c, const Tile &t)
 {
     const int lane = threadIdx.x & 31;
     const int P = p.page_size;
     const int RB = kKT / P;
-    const int per_tensor = kPHalves * RB;
-    const bool my_v = lane >= per_tensor;
-    const int cl = my_v ? lane - per_tensor : lane;
-    const int my_h = cl / RB, my_rb = cl % RB;
-    const bool copier = lane < 2 * per_tensor;
+    const int my_h = lane / RB, my_rb = lane % RB;
+    const bool copier = lane < kPHalves * RB;
     const uint32_t page_bytes = kPHalves * (uint32_t)P * 128u;
     const uint64_t pol = l2_evict_first_policy();
     if (lane == 0) {
-        prefetch_tensormap(tmK);
-        prefetch_tensormap(tmV);
-        if (__ldg(p.seq_lens + t.b) != t.L)
+        prefetch_tensormap(tm);
+        if (kIsV && __ldg(p.seq_lens + t.b) != t.L)
             atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
     }
     const int npages = (t.L + P - 1) / P;
     const int32_t *btrow = p.block_table + (int64_t)t.b * p.max_pages;
     bool alive = true;
     int last_issued = -1;
-    for (int k = 0; k < t.nst; ++k) {
-        const int slot = k % c.stages;
+    // page ids are read one stage ahead
+    int nxt_id = (copier && my_rb < npages) ? __ldg(btrow + my_rb) : -1;
+    for (int k = 0; k < t.nst_all; ++k) {
+        const int slot = k % kPStages;
         const int pg = (k * kKT) / P + my_rb;
-        const int my_id = (copier && pg < npages) ? __ldg(btrow + pg) : -1;
+        const int my_id = nxt_id;
+        {
+            const int pgn = ((k + 1) * kKT) / P + my_rb;
+            nxt_id = (k + 1 < t.nst_all && copier && pgn < npages) ? __ldg(btrow + pgn) : -1;
+        }
         bool ok = true;
         if (alive && lane == 0)
-            ok = mbar_wait_bounded(pf_empty(c, slot), (uint32_t)(((k / c.stages) & 1) ^ 1), c.abort_flag, p.err);
+            ok = pf_wait(pf_empty(c, kIsV, slot), ring_par(k) ^ 1u, c.abort_flag, p.err);
         alive = alive && __all_sync(0xffffffffu, ok);
         const bool my_valid = copier && pg < npages && my_id >= 0 && my_id < p.num_pages;
         const uint32_t mask = __ballot_sync(0xffffffffu, my_valid) & ((1u << RB) - 1u);
         if (alive && lane == 0) {
-            for (int rb = 0; rb < RB; ++rb)
-                if (!((mask >> rb) & 1u) && (k * kKT) / P + rb < npages)
-                    atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
-            reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta)[slot] = mask | ((uint32_t)k << 8);
-            mbar_arrive_expect_tx(pf_full(c, slot), (uint32_t)__popc(mask) * page_bytes * 2u);
+            if (kIsV) {
+                for (int rb = 0; rb < RB; ++rb)
+                    if (!((mask >> rb) & 1u) && (k * kKT) / P + rb < npages)
+                        atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
+                reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta)[slot] = mask | ((uint32_t)k << 8);
+            }
+            mbar_arrive_expect_tx(pf_full(c, kIsV, slot), (uint32_t)__popc(mask) * page_bytes);
         }
         __syncwarp();
         if (alive && my_valid) {
-            const uint32_t dst = pf_slot(c, slot) + (my_v ? (uint32_t)(kKT * kPD * 2) : 0u) +
+            const uint32_t dst = pf_slot(c, slot) + (kIsV ? (uint32_t)(kKT * kPD * 2) : 0u) +
                                  (uint32_t)my_h * (kKT * 128) + (uint32_t)my_rb * (uint32_t)P * 128u;
-            tma_load_2d(dst, my_v ? tmV : tmK, my_h * 64, (my_id * p.hkv + t.g) * P, pf_full(c, slot), pol);
+            tma_load_2d(dst, tm, my_h * 64, (my_id * p.hkv + t.g) * P, pf_full(c, kIsV, slot), pol);
         }
         if (alive)
             last_issued = k;
         __syncwarp();
     }
     if (!alive && lane == 0)
-        for (int k = last_issued - c.stages + 1; k <= last_issued; ++k)
+        for (int k = last_issued - kPStages + 1; k <= last_issued; ++k)
             if (k >= 0)
-                mbar_drain_bounded(pf_full(c, k % c.stages), (uint32_t)((k / c.stages) & 1));
+                mbar_drain_bounded(pf_full(c, kIsV, k % kPStages), ring_par(k));
 }
 
 // ---------------------------------------------------------------------------
 // MMA issuers
 // ---------------------------------------------------------------------------
+// S_X = Q_X K^T for each tile that attends stage k; S_X is free once PV_X(k-1)
+// has read the P written over it.
 __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
 {
     const uint32_t idesc = umma_idesc_bf16(128, kKT, false, false);
-    const uint32_t qtile = c.base + c.lay.qtile;
     bool alive = true;
-    for (int k = 0; k < t.nst; ++k) {
-        const int slot = k % c.stages, buf = k & 1;
+    for (int k = 0; k < t.nst_all; ++k) {
+        const int slot = k % kPStages;
         if (alive)
-            alive = mbar_wait_bounded(pf_full(c, slot), (uint32_t)((k / c.stages) & 1), c.abort_flag, p.err);
-        if (alive)
-            alive = mbar_wait_bounded(pf_sfree(c, buf), (uint32_t)(((k >> 1) & 1) ^ 1), c.abort_flag, p.err);
-        if (alive) {
-            tc_fence_after();
-            const uint32_t kst = pf_slot(c, slot);
+            alive = pf_wait(pf_full(c, false, slot), ring_par(k), c.abort_flag, p.err);
+#pragma unroll 1
+        for (int x = 0; x < kPTilesPerCta; ++x) {
+            if (k >= t.nst[x])
+                continue;
+            if (alive && k >= 1)
+                alive = pf_wait(pf_pvdone(c, x), (uint32_t)((k - 1) & 1), c.abort_flag, p.err);
+            if (alive) {
+                tc_fence_after();
+                const uint32_t qtile = c.base + c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
+                const uint32_t kst = pf_slot(c, slot);
 #pragma unroll
-            for (int h = 0; h < kPHalves; ++h)
+                for (int h = 0; h < kPHalves; ++h)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = umma_sdesc_sw128(qtile + (uint32_t)(h * 128 * 128 + kk * 32), 16u, 1024u);
-                    const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)(h * kKT * 128 + kk * 32), 16u, 1024u);
-                    umma_bf16(tmem + kPColS + (uint32_t)(buf * kKT), ad, bd, idesc, (h | kk) ? 1u : 0u);
-                }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad =
+                            umma_sdesc_sw128(qtile + (uint32_t)(h * 128 * 128 + kk * 32), 16u, 1024u);
+                        const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)(h * kKT * 128 + kk * 32), 16u, 1024u);
+                        umma_bf16(tmem + col_s(x), ad, bd, idesc, (h | kk) ? 1u : 0u);
+                    }
+            }
+            umma_commit(pf_sfull(c, x));
         }
-        umma_commit(pf_sfull(c, buf));
+        umma_commit(pf_empty(c, false, slot));
     }
     umma_commit(pf_fin(c));
     mbar_drain_bounded(pf_fin(c), 0u);
 }
 
-// O += P V; P over the slot's K region ([key half][row][128 B]), V MN-major
+// O_X += P_X V; P_X from TMEM (over S_X), V MN-major in the slot.  PV_A(k)
+// waits for tile A's softmax, which also cleared the stage's unusable V rows
+// for both tiles (tile B's alone once A no longer attends the stage).
 __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
 {
     const uint32_t idesc = umma_idesc_bf16(128, kPD, false, true);
     bool alive = true;
-    for (int k = 0; k < t.nst; ++k) {
-        const int slot = k % c.stages;
+    for (int k = 0; k < t.nst_all; ++k) {
+        const int slot = k % kPStages;
         if (alive)
-            alive = mbar_wait_bounded(pf_pfull(c, slot), (uint32_t)((k / c.stages) & 1), c.abort_flag, p.err);
-        if (alive) {
-            tc_fence_after();
-            const uint32_t kst = pf_slot(c, slot);
-            const uint32_t vst = kst + (uint32_t)(kKT * kPD * 2);
+            alive = pf_wait(pf_full(c, true, slot), ring_par(k), c.abort_flag, p.err);
+#pragma unroll 1
+        for (int x = 0; x < kPTilesPerCta; ++x) {
+            if (k >= t.nst[x])
+                continue;
+            if (alive)
+                alive = pf_wait(pf_pfull(c, x), (uint32_t)(k & 1), c.abort_flag, p.err);
+            if (alive) {
+                tc_fence_after();
+                const uint32_t vst = pf_slot(c, slot) + (uint32_t)(kKT * kPD * 2);
 #pragma unroll
-            for (int ks = 0; ks < kKT / 16; ++ks) {
-                const uint64_t ad =
-                    umma_sdesc_sw128(kst + (uint32_t)((ks >> 2) * (128 * 128) + (ks & 3) * 32), 16u, 1024u);
-                const uint64_t bd = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kKT * 128), 1024u);
-                umma_bf16(tmem + kPColO, ad, bd, idesc, (k == 0 && ks == 0) ? 0u : 1u);
+                for (int ks = 0; ks < kKT / 16; ++ks) {
+                    const uint64_t bd = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kKT * 128), 1024u);
+                    umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + (uint32_t)(ks * 8), bd, idesc,
+                                 (k == 0 && ks == 0) ? 0u : 1u);
+                }
             }
+            umma_commit(pf_pvdone(c, x));
         }
-        umma_commit(pf_empty(c, slot));
+        umma_commit(pf_empty(c, true, slot));
     }
     umma_commit(pf_fin(c));
     mbar_drain_bounded(pf_fin(c), 0u);
 }
 
 // ---------------------------------------------------------------------------
-// softmax warps: thread r = MMA row r = (new token i0 + r / G, head r % G)
+// softmax warps of tile x: thread r = MMA row r = (new token i0 + r / G, head r % G)
 // ---------------------------------------------------------------------------
-__device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem, float &m_out,
-                           float &l_out, bool &alive_out)
+__device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem, int x,
+                           float &m_out, float &l_out, bool &alive_out)
 {
-    const int r = threadIdx.x;
+    const int r = threadIdx.x - x * 128;
     const int lane = r & 31, warp = r >> 5;
-    const int ti = r / p.group, tj = r - (r / p.group) * p.group;
-    const bool row_ok = ti < t.ntok;
-    const int pos = t.prefix + t.i0 + ti;                // this row's position (keys 0 .. pos)
+    const int ti = r / p.group;
+    const bool row_ok = ti < t.ntok[x];
+    const int pos = t.prefix + t.i0[x] + ti;             // this row's position (keys 0 .. pos)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t srow = tmem + lane_base + col_s(x);
+    const uint32_t orow = tmem + lane_base + col_o(x);
     const int P = p.page_size;
     const int log2P = 31 - __clz(P);
     const float sl2 = p.scale_log2;
@@ -253,15 +352,15 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
     auto wait = [&](uint32_t bar, uint32_t parity) {
         bool ok = false;
         if (alive)
-            ok = mbar_wait_bounded(bar, parity, c.abort_flag, p.err);
+            ok = pf_wait(bar, parity, c.abort_flag, p.err);
         alive = __all_sync(0xffffffffu, ok) && alive;
         return alive;
     };
-    for (int k = 0; k < t.nst; ++k) {
-        const int slot = k % c.stages, buf = k & 1;
+    for (int k = 0; k < t.nst[x]; ++k) {
+        const int slot = k % kPStages;
         const int key0 = k * kKT;
-        wait(pf_sfull(c, buf), (uint32_t)((k >> 1) & 1));
-        wait(pf_full(c, slot), (uint32_t)((k / c.stages) & 1));      // (complete already: orders the word below)
+        wait(pf_sfull(c, x), (uint32_t)(k & 1));
+        wait(pf_full(c, true, slot), ring_par(k));           // V landed; orders the word below
         const uint32_t tagged = alive ? reinterpret_cast<const volatile uint32_t *>(c.smem + c.lay.meta)[slot] : 0u;
         if (alive && (tagged >> 8) != ((uint32_t)k & 0xffffffu)) {
             if (lane == 0) {
@@ -274,12 +373,11 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
         // keys this row may see: [key0, key0 + nvis), on pages that were copied
         const int nvis = row_ok ? min(kKT, pos - key0 + 1) : 0;
         const bool all_pages = pmask == (1u << (kKT / P)) - 1u;
-        const bool dense = alive && nvis == kKT && all_pages;    // below the diagonal: no mask
-        const uint32_t srow = tmem + lane_base + kPColS + (uint32_t)(buf * kKT);
-        uint8_t *prow = c.smem + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes + (uint32_t)r * 128u;
-        // 32 scores of this row from TMEM, masked (-inf where invisible)
-        auto load_chunk = [&](int c32, uint32_t (&sv)[32]) {
-            tmem_ld32(srow + (uint32_t)(c32 * 32), sv);
+        // no mask below the diagonal; padding rows (no token) need none either:
+        // their scores only reach their own row of O, which is not stored
+        const bool dense = alive && all_pages && (nvis == kKT || !row_ok);
+        // 32 scores (already loaded), masked (-inf where invisible)
+        auto mask_chunk = [&](int c32, uint32_t (&sv)[32]) {
             if (!dense) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -289,102 +387,105 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
                 }
             }
         };
-        // P of 32 keys (bf16) over the consumed K tile: keys 0..63 in half 0, 64..127 in half 1
-        auto emit_chunk = [&](int c32, const uint32_t (&sv)[32], float mu, bool store) -> float {
-            float part = 0.f;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = q8 * 8 + 2 * e;
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl2, -mu));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl2, -mu));
-                    part += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                const int ch = c32 * 4 + q8;                      // 16-byte chunk of the 256-byte row
-                if (store)
-                    *reinterpret_cast<uint4 *>(prow + (uint32_t)(ch >> 3) * (128u * 128u) +
-                                               (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            return part;
-        };
         if (alive)
             tc_fence_after();
-        // a row with no running max yet takes this stage's max first
-        if (__any_sync(0xffffffffu, alive && m_use == -INFINITY && nvis > 0)) {
-            float cm = -INFINITY;
-#pragma unroll 1
+        // pass 1: this stage's maximum (next chunk's TMEM load in flight)
+        float cm = -INFINITY;
+        {
+            uint32_t sa[32], sb[32];
+            tmem_ld32(srow, sa);
+            mask_chunk(0, sa);
+#pragma unroll
             for (int c32 = 0; c32 < kKT / 32; ++c32) {
-                uint32_t sv[32];
-                load_chunk(c32, sv);
+                uint32_t (&cur)[32] = (c32 & 1) ? sb : sa;
+                uint32_t (&nxt)[32] = (c32 & 1) ? sa : sb;
+                if (c32 + 1 < kKT / 32)
+                    tmem_ld32_nowait(srow + (uint32_t)((c32 + 1) * 32), nxt);
+                float a = cm, b = -INFINITY, d = -INFINITY, e4 = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    cm = fmaxf(cm, __uint_as_float(sv[e]));
+                for (int e = 0; e < 32; e += 8) {
+                    a = max3f(a, __uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
+                    b = max3f(b, __uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3]));
+                    d = max3f(d, __uint_as_float(cur[e + 4]), __uint_as_float(cur[e + 5]));
+                    e4 = max3f(e4, __uint_as_float(cur[e + 6]), __uint_as_float(cur[e + 7]));
+                }
+                cm = max3f(a, b, fmaxf(d, e4));
+                if (c32 + 1 < kKT / 32) {
+                    tmem_wait_ld();
+                    mask_chunk(c32 + 1, nxt);
+                }
             }
-            if (m_use == -INFINITY)
-                m_use = cm * sl2;                                 // sl2 > 0; stays -inf if nothing is visible
         }
-        // stream the row: exponents against the running max, tracking this stage's max
-        const float l_before = lsum;
-        const float mu = m_use == -INFINITY ? 0.f : m_use;
-        float cmax = -INFINITY, part = 0.f;
-#pragma unroll 1
-        for (int c32 = 0; c32 < kKT / 32; ++c32) {
-            uint32_t sv[32];
-            load_chunk(c32, sv);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                cmax = fmaxf(cmax, __uint_as_float(sv[e]));
-            part += emit_chunk(c32, sv, mu, alive);
-        }
-        lsum += part;
-        // lazy refresh: a row whose max rose by more than 2^kPRescaleLog2
-        // rescales its O (after the previous PV) and redoes this stage's P
-        // from S, still in TMEM.  tcgen05.ld/st are warp-wide, so the whole
-        // warp takes part (scale 1, no rewrite, where nothing moved).
-        const float mt = cmax * sl2;
+        // the running maximum moves only by more than 2^kPRescaleLog2 (or
+        // when it is first set; O and the sum are still zero then)
+        const float mt = cm * sl2;                                // sl2 > 0; -inf if nothing is visible
+        const bool first = m_use == -INFINITY && mt != -INFINITY;
         const bool need = alive && m_use != -INFINITY && mt > m_use + kPRescaleLog2;
+        if (first)
+            m_use = mt;
         if (__any_sync(0xffffffffu, need)) {
+            // tcgen05.ld/st are warp-wide: lanes that keep their maximum scale by 1
             const float alpha = need ? ex2_approx(m_use - mt) : 1.f;
             if (k >= 1) {
-                const int kp = k - 1;
-                wait(pf_empty(c, kp % c.stages), (uint32_t)((kp / c.stages) & 1));
+                wait(pf_pvdone(c, x), (uint32_t)((k - 1) & 1));
                 if (alive) {
                     tc_fence_after();
 #pragma unroll 1
                     for (int c32 = 0; c32 < kPD / 32; ++c32) {
                         uint32_t ov[32];
-                        tmem_ld32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
+                        tmem_ld32(orow + (uint32_t)(c32 * 32), ov);
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
+                        tmem_st32(orow + (uint32_t)(c32 * 32), ov);
                     }
                 }
             }
-            if (need)
+            if (need) {
+                lsum *= alpha;
                 m_use = mt;
-            float redo = 0.f;
-#pragma unroll 1
-            for (int c32 = 0; c32 < kKT / 32; ++c32) {
-                uint32_t sv[32];
-                if (alive)
-                    load_chunk(c32, sv);
-                redo += emit_chunk(c32, sv, m_use, alive && need);
             }
-            if (need)
-                lsum = l_before * alpha + redo;
         }
+        // pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs over columns
+        // 16 c .. 16 c + 15 of S (scores already read: chunk c covers columns
+        // 32 c .. 32 c + 31)
+        const float mu = m_use == -INFINITY ? 0.f : m_use;
+        float part = 0.f;
+        {
+            uint32_t sa[32], sb[32];
+            tmem_ld32(srow, sa);
+            mask_chunk(0, sa);
+#pragma unroll
+            for (int c32 = 0; c32 < kKT / 32; ++c32) {
+                uint32_t (&cur)[32] = (c32 & 1) ? sb : sa;
+                uint32_t (&nxt)[32] = (c32 & 1) ? sa : sb;
+                if (c32 + 1 < kKT / 32)
+                    tmem_ld32_nowait(srow + (uint32_t)((c32 + 1) * 32), nxt);
+                float pp[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * e]), sl2, -mu));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * e + 1]), sl2, -mu));
+                    pp[e & 3] += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16_nowait(srow + (uint32_t)(c32 * 16), pk);
+                part += (pp[0] + pp[1]) + (pp[2] + pp[3]);
+                if (c32 + 1 < kKT / 32) {
+                    tmem_wait_ld();
+                    mask_chunk(c32 + 1, nxt);
+                }
+            }
+        }
+        lsum += part;
+        tmem_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(pf_sfree(c, buf));
         // V rows of keys that no row may use in this stage (past the request's
         // end, or on a skipped page) may hold stale or non-finite bits: zero
-        // them (thread r takes key row r)
-        {
+        // them (thread r takes key row r).  Tile A does it while it attends the
+        // stage, tile B after that.
+        if (x == 0 || k >= t.nst[0]) {
             const int key = key0 + r;
             const bool key_ok = key < t.L && ((pmask >> (r >> log2P)) & 1u);
             if (alive && !key_ok) {
@@ -395,12 +496,11 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
                     for (int ch = 0; ch < 8; ++ch)
                         st_shared_zero16(vrow + (uint32_t)(h * kKT * 128 + ch * 16));
             }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(pf_pfull(c, slot));
+            mbar_arrive(pf_pfull(c, x));
     }
     m_out = m_use;
     l_out = lsum;
@@ -408,29 +508,30 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
 }
 
 // ---------------------------------------------------------------------------
-// epilogue: this row of O, normalised, and its log-sum-exp
+// epilogue: this row of O_x, normalised, and its log-sum-exp
 // ---------------------------------------------------------------------------
-__device__ void pf_epilogue(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem, float m_use,
-                            float lsum, bool alive)
+__device__ void pf_epilogue(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem, int x,
+                            float m_use, float lsum, bool alive)
 {
-    const int r = threadIdx.x;
+    const int r = threadIdx.x - x * 128;
     const int warp = r >> 5;
     const int ti = r / p.group, tj = r - (r / p.group) * p.group;
-    const bool row_ok = ti < t.ntok;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int last = t.nst - 1;
-    bool ok = alive && mbar_wait_bounded(pf_empty(c, last % c.stages), (uint32_t)((last / c.stages) & 1),
-                                         c.abort_flag, p.err);
+    const bool row_ok = ti < t.ntok[x];
+    const uint32_t orow = tmem + ((uint32_t)(warp * 32) << 16) + col_o(x);
+    const int last = t.nst[x] - 1;
+    if (last < 0)
+        return;                                  // tile B of an odd tile count: no rows
+    bool ok = alive && pf_wait(pf_pvdone(c, x), (uint32_t)(last & 1), c.abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok)
         return;
     tc_fence_after();
     const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
-    const int64_t row = ((int64_t)t.b * p.n_new + t.i0 + ti) * p.hq + (int64_t)t.g * p.group + tj;
+    const int64_t row = ((int64_t)t.b * p.n_new + t.i0[x] + ti) * p.hq + (int64_t)t.g * p.group + tj;
 #pragma unroll 1
     for (int c32 = 0; c32 < kPD / 32; ++c32) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + kPColO + (uint32_t)(c32 * 32), ov);
+        tmem_ld32(orow + (uint32_t)(c32 * 32), ov);
         if (row_ok) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kPD + c32 * 32);
 #pragma unroll
@@ -463,38 +564,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
         c.smem = smem_raw + pad;
         c.base = raw + pad;
     }
-    c.stages = p.stages;
-    c.lay = pf_layout(p.stages);
+    c.lay = pf_layout();
     c.abort_flag = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.misc);
     const Tile t = pf_tile(p);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < c.stages; ++s) {
-            mbar_init(pf_full(c, s), 1);
-            mbar_init(pf_empty(c, s), 1);
-            mbar_init(pf_pfull(c, s), kPSoftmaxWarps);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(pf_sfull(c, i), 1);
-            mbar_init(pf_sfree(c, i), kPSoftmaxWarps);
+        for (int s = 0; s < kPStages; ++s)
+            for (int v = 0; v < 2; ++v) {
+                mbar_init(pf_full(c, v, s), 1);
+                mbar_init(pf_empty(c, v, s), 1);
+            }
+        for (int x = 0; x < kPTilesPerCta; ++x) {
+            mbar_init(pf_sfull(c, x), 1);
+            mbar_init(pf_pfull(c, x), kPGroupWarps);
+            mbar_init(pf_pvdone(c, x), 1);
         }
         mbar_init(pf_fin(c), 2);
         *c.abort_flag = 0u;
         fence_barrier_init();
     }
-    if (warp < kPSoftmaxWarps) {
-        // this thread's query row into the swizzled K-major Q tile (padding rows zero)
-        const int r = threadIdx.x;
+    if (warp < kPTilesPerCta * kPGroupWarps) {
+        // this thread's query row into its tile's swizzled K-major Q tile (padding rows zero)
+        const int x = warp / kPGroupWarps;
+        const int r = threadIdx.x - x * 128;
         const int ti = r / p.group, tj = r - (r / p.group) * p.group;
-        const bool row_ok = ti < t.ntok;
+        const bool row_ok = ti < t.ntok[x];
         const uint4 *src = reinterpret_cast<const uint4 *>(
-            p.q + (((int64_t)t.b * p.n_new + t.i0 + ti) * p.hq + (int64_t)t.g * p.group + tj) * kPD);
+            p.q + (((int64_t)t.b * p.n_new + t.i0[x] + ti) * p.hq + (int64_t)t.g * p.group + tj) * kPD);
+        const uint32_t qtile = c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
 #pragma unroll
         for (int ch = 0; ch < kPD / 8; ++ch) {
             const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t off = (uint32_t)(ch >> 3) * (128u * 128u) + (uint32_t)r * 128u +
                                  (uint32_t)(((ch & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4 *>(c.smem + c.lay.qtile + off) = v;
+            *reinterpret_cast<uint4 *>(c.smem + qtile + off) = v;
         }
         fence_proxy_async_smem();
     }
@@ -505,19 +608,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.tslot);
 
-    if (warp == kPProducerWarp)
-        pf_producer(&tmK, &tmV, p, c, t);
+    if (warp == kPKWarp)
+        pf_producer<false>(&tmK, p, c, t);
+    else if (warp == kPVWarp)
+        pf_producer<true>(&tmV, p, c, t);
     else if (warp == kPQkWarp) {
         if ((threadIdx.x & 31) == 0)
             pf_qk(p, c, t, tmem);
     } else if (warp == kPPvWarp) {
         if ((threadIdx.x & 31) == 0)
             pf_pv(p, c, t, tmem);
-    } else if (warp < kPSoftmaxWarps) {
+    } else {
+        const int x = warp / kPGroupWarps;
         float m_use, lsum;
         bool alive;
-        pf_softmax(p, c, t, tmem, m_use, lsum, alive);
-        pf_epilogue(p, c, t, tmem, m_use, lsum, alive);
+        pf_softmax(p, c, t, tmem, x, m_use, lsum, alive);
+        pf_epilogue(p, c, t, tmem, x, m_use, lsum, alive);
     }
 
     tc_fence_before();
@@ -530,15 +636,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int prefill_stages()
-{
-    int st = kPMaxStages;
-    while (st >= 2 && pf_layout(st).total > (uint32_t)kSmemLimit)
-        --st;
-    return st;
-}
+int prefill_tiles_per_cta() { return kPTilesPerCta; }
 
-uint32_t prefill_smem_bytes(int stages) { return pf_layout(stages).total; }
+uint32_t prefill_smem_bytes() { return pf_layout().total; }
 
 // tmK, tmV: 2-D maps of the pools (box of 64 columns x P rows, 128-byte swizzle).
 cudaError_t launch_prefill_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const PrefillParams &p, uint32_t smem,

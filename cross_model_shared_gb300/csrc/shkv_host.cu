@@ -23,8 +23,8 @@ int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
 cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream);
-int prefill_stages();
-uint32_t prefill_smem_bytes(int stages);
+int prefill_tiles_per_cta();
+uint32_t prefill_smem_bytes();
 cudaError_t launch_prefill_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const PrefillParams &p, uint32_t smem,
                                 int grid, cudaStream_t stream);
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
@@ -603,12 +603,13 @@ shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new
     p.page_size = c.page_size;
     p.max_pages = c.max_pages_per_seq;
     p.num_pages = c.num_pages;
-    p.stages = prefill_stages();
+    p.stages = 0;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    const int64_t grid = (int64_t)batch * c.num_kv_heads * p.tiles;
+    const int per_cta = prefill_tiles_per_cta();
+    const int64_t grid = (int64_t)batch * c.num_kv_heads * ((p.tiles + per_cta - 1) / per_cta);
     if (grid > INT32_MAX)
         return SHKV_ERR_UNSUPPORTED;
-    return cuda_status(launch_prefill_umma(pool->tm_k2, pool->tm_v2, p, prefill_smem_bytes(p.stages), (int)grid,
+    return cuda_status(launch_prefill_umma(pool->tm_k2, pool->tm_v2, p, prefill_smem_bytes(), (int)grid,
                                            (cudaStream_t)stream));
 }
 
