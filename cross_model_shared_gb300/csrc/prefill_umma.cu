@@ -10,20 +10,20 @@
 // A query tile is TPT = floor(128 / G) new tokens x the G query heads of one
 // KV head: 128 MMA rows (row r = i * G + j), so every K/V page is read once
 // for the whole group.  One CTA takes two consecutive tiles X = A, B of one
-// (request, KV head) and streams 128-key stages of K/V through shared memory
+// (request, KV head) and streams 64-key stages of K/V through shared memory
 // once for both (256 query rows per K/V byte).  Per stage and tile:
-//   S_X[r, key]  = sum_d Q_X[r, d] K[key, d]      M = 128 rows, N = 128 keys
+//   S_X[r, key]  = sum_d Q_X[r, d] K[key, d]      M = 128 rows, N = 64 keys
 //   O_X[r, d]   += sum_key P_X[r, key] V[key, d]  M = 128 rows, N = 128 = D
-// TMEM holds S_A, S_B, O_A, O_B (4 x 128 columns).  A softmax thread owns one
-// row of one tile (its TMEM lane): it reads its scores twice, first for the
-// stage maximum, then to exponentiate them against its running maximum, and
-// writes P (bf16 pairs) over the first 64 columns of its S, from where the PV
-// product reads it.  The running maximum moves only when the stage maximum
-// exceeds it by more than 2^kPRescaleLog2; the thread then rescales its row
-// of O first.  The two tiles alternate on the tensor core: while one tile's
-// softmax runs, the other tile's PV and next QK execute.  Key stages past a
-// tile's last position are skipped for that tile (and never loaded past the
-// pair's last position); on the diagonal the causal mask is per element.
+// TMEM holds two S buffers per tile (64 columns each) and O_A, O_B (128
+// each), so QK of the next stage runs while the softmax works on this one.  A
+// softmax thread owns one row of one tile (its TMEM lane): it loads its 64
+// scores into registers, takes their maximum, exponentiates them against its
+// running maximum and writes P (bf16 pairs) over the first 32 columns of the
+// S buffer, from where the PV product reads it.  The running maximum moves
+// only when the stage maximum exceeds it by more than 2^kPRescaleLog2; the
+// thread then rescales its row of O first.  Key stages past a tile's last
+// position are skipped for that tile (and never loaded past the pair's last
+// position); on the diagonal the causal mask is per element.
 //
 // Roles (384 threads): warps 0-3 softmax of tile A, warps 4-7 of tile B (row
 // = TMEM lane), warp 8 QK issuer (its commit frees the K half of a ring slot),
@@ -42,7 +42,7 @@ namespace shkv {
 
 namespace {
 
-constexpr int kKT = 128;                 // keys per stage
+constexpr int kKT = 64;                  // keys per stage
 constexpr int kPD = 128;                 // head dim
 constexpr int kPHalves = kPD / 64;
 constexpr int kPThreads = 384;
@@ -53,10 +53,11 @@ constexpr int kPVWarp = 11;
 constexpr int kPGroupWarps = 4;          // softmax warps per tile
 constexpr uint32_t kPTmemCols = 512;
 constexpr float kPRescaleLog2 = 8.f;
-constexpr int kPStages = 2;
+constexpr int kPStages = 4;
 constexpr int kPTilesPerCta = 2;
 
-__device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)(x * 128); }        // P over its first 64
+// S buffer b of tile x (P over its first 32 columns), and O of tile x
+__device__ __forceinline__ uint32_t col_s(int x, int b) { return (uint32_t)(x * 128 + b * 64); }
 __device__ __forceinline__ uint32_t col_o(int x) { return (uint32_t)(256 + x * 128); }
 
 // max of three (one instruction on sm_100 and later)
@@ -118,9 +119,10 @@ struct PfSmem {
     uint32_t ring, stage_bytes, qtile, bars, meta, misc, tslot, total;
 };
 
-// ring slots of [K | V][half][128 keys][128 B], then the two Q tiles
+// ring slots of [K | V][half][64 keys][128 B], then the two Q tiles
 // [tile][half][128 rows][128 B] (all 128-byte swizzled), then the barriers:
-// full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[2], p_full[2], pv_done[2], fin
+// full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[tile][buf], p_full[tile],
+// pv_done[tile][buf], fin
 __host__ __device__ inline PfSmem pf_layout()
 {
     PfSmem u;
@@ -128,7 +130,7 @@ __host__ __device__ inline PfSmem pf_layout()
     u.ring = 0;
     u.qtile = (uint32_t)kPStages * u.stage_bytes;
     u.bars = u.qtile + (uint32_t)(kPTilesPerCta * kPHalves * 128 * 128);
-    u.meta = u.bars + (uint32_t)((4 * kPStages + 7) * 8);
+    u.meta = u.bars + (uint32_t)((4 * kPStages + 11) * 8);
     u.misc = u.meta + (uint32_t)(kPStages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;
@@ -148,10 +150,13 @@ __device__ __forceinline__ uint32_t pf_empty(const PfCtx &c, bool v, int s)
 {
     return pbar(c, (v ? 3 : 2) * kPStages + s);
 }
-__device__ __forceinline__ uint32_t pf_sfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + x); }
-__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 2 + x); }
-__device__ __forceinline__ uint32_t pf_pvdone(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 4 + x); }
-__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 6); }
+__device__ __forceinline__ uint32_t pf_sfull(const PfCtx &c, int x, int b) { return pbar(c, 4 * kPStages + 2 * x + b); }
+__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 4 + x); }
+__device__ __forceinline__ uint32_t pf_pvdone(const PfCtx &c, int x, int b)
+{
+    return pbar(c, 4 * kPStages + 6 + 2 * x + b);
+}
+__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 10); }
 __device__ __forceinline__ uint32_t pf_slot(const PfCtx &c, int s)
 {
     return c.base + c.lay.ring + (uint32_t)s * c.lay.stage_bytes;
@@ -189,7 +194,7 @@ __device__ __forceinline__ Tile pf_tile(const PrefillParams &p)
 }
 
 // ---------------------------------------------------------------------------
-// producers: stage k = keys [128k, 128k + 128), 128/P pages; one warp copies
+// producers: stage k = keys [64k, 64k + 64), 64/P pages; one warp copies
 // the K halves of the pages, another the V halves (one box per lane).  The V
 // producer records which pages it copied in the slot's word (a V half is
 // released only after both tiles' softmax of its stage have read the word).
@@ -257,8 +262,8 @@ __device__ void pf_producer(const CUtensorMap *tm, const PrefillParams &p, const
 // ---------------------------------------------------------------------------
 // MMA issuers
 // ---------------------------------------------------------------------------
-// S_X = Q_X K^T for each tile that attends stage k; S_X is free once PV_X(k-1)
-// has read the P written over it.
+// S_X = Q_X K^T for each tile that attends stage k, into S buffer k & 1, which
+// is free once PV_X(k-2) has read the P written over it.
 __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
 {
     const uint32_t idesc = umma_idesc_bf16(128, kKT, false, false);
@@ -271,8 +276,8 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
         for (int x = 0; x < kPTilesPerCta; ++x) {
             if (k >= t.nst[x])
                 continue;
-            if (alive && k >= 1)
-                alive = pf_wait(pf_pvdone(c, x), (uint32_t)((k - 1) & 1), c.abort_flag, p.err);
+            if (alive && k >= 2)
+                alive = pf_wait(pf_pvdone(c, x, k & 1), (uint32_t)(((k - 2) >> 1) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
                 const uint32_t qtile = c.base + c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
@@ -284,10 +289,10 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
                         const uint64_t ad =
                             umma_sdesc_sw128(qtile + (uint32_t)(h * 128 * 128 + kk * 32), 16u, 1024u);
                         const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)(h * kKT * 128 + kk * 32), 16u, 1024u);
-                        umma_bf16(tmem + col_s(x), ad, bd, idesc, (h | kk) ? 1u : 0u);
+                        umma_bf16(tmem + col_s(x, k & 1), ad, bd, idesc, (h | kk) ? 1u : 0u);
                     }
             }
-            umma_commit(pf_sfull(c, x));
+            umma_commit(pf_sfull(c, x, k & 1));
         }
         umma_commit(pf_empty(c, false, slot));
     }
@@ -295,7 +300,7 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
     mbar_drain_bounded(pf_fin(c), 0u);
 }
 
-// O_X += P_X V; P_X from TMEM (over S_X), V MN-major in the slot.  PV_A(k)
+// O_X += P_X V; P_X from TMEM (over S buffer k & 1), V MN-major in the slot.  PV_A(k)
 // waits for tile A's softmax, which also cleared the stage's unusable V rows
 // for both tiles (tile B's alone once A no longer attends the stage).
 __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
@@ -318,11 +323,11 @@ __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
 #pragma unroll
                 for (int ks = 0; ks < kKT / 16; ++ks) {
                     const uint64_t bd = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kKT * 128), 1024u);
-                    umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + (uint32_t)(ks * 8), bd, idesc,
+                    umma_bf16_ts(tmem + col_o(x), tmem + col_s(x, k & 1) + (uint32_t)(ks * 8), bd, idesc,
                                  (k == 0 && ks == 0) ? 0u : 1u);
                 }
             }
-            umma_commit(pf_pvdone(c, x));
+            umma_commit(pf_pvdone(c, x, k & 1));
         }
         umma_commit(pf_empty(c, true, slot));
     }
@@ -342,7 +347,6 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
     const bool row_ok = ti < t.ntok[x];
     const int pos = t.prefix + t.i0[x] + ti;             // this row's position (keys 0 .. pos)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t srow = tmem + lane_base + col_s(x);
     const uint32_t orow = tmem + lane_base + col_o(x);
     const int P = p.page_size;
     const int log2P = 31 - __clz(P);
@@ -359,7 +363,9 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
     for (int k = 0; k < t.nst[x]; ++k) {
         const int slot = k % kPStages;
         const int key0 = k * kKT;
-        wait(pf_sfull(c, x), (uint32_t)(k & 1));
+        const int buf = k & 1;
+        const uint32_t srow = tmem + lane_base + col_s(x, buf);
+        wait(pf_sfull(c, x, buf), (uint32_t)((k >> 1) & 1));
         wait(pf_full(c, true, slot), ring_par(k));           // V landed; orders the word below
         const uint32_t tagged = alive ? reinterpret_cast<const volatile uint32_t *>(c.smem + c.lay.meta)[slot] : 0u;
         if (alive && (tagged >> 8) != ((uint32_t)k & 0xffffffu)) {
@@ -389,32 +395,26 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
         };
         if (alive)
             tc_fence_after();
-        // pass 1: this stage's maximum (next chunk's TMEM load in flight)
-        float cm = -INFINITY;
+        // this row's 64 scores into registers
+        uint32_t sv[2][32];
+        tmem_ld32_nowait(srow, sv[0]);
+        tmem_ld32_nowait(srow + 32u, sv[1]);
+        tmem_wait_ld();
+        mask_chunk(0, sv[0]);
+        mask_chunk(1, sv[1]);
+        float cm;
         {
-            uint32_t sa[32], sb[32];
-            tmem_ld32(srow, sa);
-            mask_chunk(0, sa);
+            float a = -INFINITY, b = -INFINITY, d = -INFINITY, e4 = -INFINITY;
 #pragma unroll
-            for (int c32 = 0; c32 < kKT / 32; ++c32) {
-                uint32_t (&cur)[32] = (c32 & 1) ? sb : sa;
-                uint32_t (&nxt)[32] = (c32 & 1) ? sa : sb;
-                if (c32 + 1 < kKT / 32)
-                    tmem_ld32_nowait(srow + (uint32_t)((c32 + 1) * 32), nxt);
-                float a = cm, b = -INFINITY, d = -INFINITY, e4 = -INFINITY;
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
-                    a = max3f(a, __uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
-                    b = max3f(b, __uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3]));
-                    d = max3f(d, __uint_as_float(cur[e + 4]), __uint_as_float(cur[e + 5]));
-                    e4 = max3f(e4, __uint_as_float(cur[e + 6]), __uint_as_float(cur[e + 7]));
+                    a = max3f(a, __uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1]));
+                    b = max3f(b, __uint_as_float(sv[h][e + 2]), __uint_as_float(sv[h][e + 3]));
+                    d = max3f(d, __uint_as_float(sv[h][e + 4]), __uint_as_float(sv[h][e + 5]));
+                    e4 = max3f(e4, __uint_as_float(sv[h][e + 6]), __uint_as_float(sv[h][e + 7]));
                 }
-                cm = max3f(a, b, fmaxf(d, e4));
-                if (c32 + 1 < kKT / 32) {
-                    tmem_wait_ld();
-                    mask_chunk(c32 + 1, nxt);
-                }
-            }
+            cm = max3f(a, b, fmaxf(d, e4));
         }
         // the running maximum moves only by more than 2^kPRescaleLog2 (or
         // when it is first set; O and the sum are still zero then)
@@ -427,7 +427,7 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
             // tcgen05.ld/st are warp-wide: lanes that keep their maximum scale by 1
             const float alpha = need ? ex2_approx(m_use - mt) : 1.f;
             if (k >= 1) {
-                wait(pf_pvdone(c, x), (uint32_t)((k - 1) & 1));
+                wait(pf_pvdone(c, x, (k - 1) & 1), (uint32_t)(((k - 1) >> 1) & 1));
                 if (alive) {
                     tc_fence_after();
 #pragma unroll 1
@@ -446,37 +446,23 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
                 m_use = mt;
             }
         }
-        // pass 2: P = 2^(s * scale_log2 - m) as bf16 pairs over columns
-        // 16 c .. 16 c + 15 of S (scores already read: chunk c covers columns
-        // 32 c .. 32 c + 31)
+        // P = 2^(s * scale_log2 - m) as bf16 pairs over columns 0 .. 31 of
+        // the S buffer (the scores are in registers)
         const float mu = m_use == -INFINITY ? 0.f : m_use;
         float part = 0.f;
-        {
-            uint32_t sa[32], sb[32];
-            tmem_ld32(srow, sa);
-            mask_chunk(0, sa);
 #pragma unroll
-            for (int c32 = 0; c32 < kKT / 32; ++c32) {
-                uint32_t (&cur)[32] = (c32 & 1) ? sb : sa;
-                uint32_t (&nxt)[32] = (c32 & 1) ? sa : sb;
-                if (c32 + 1 < kKT / 32)
-                    tmem_ld32_nowait(srow + (uint32_t)((c32 + 1) * 32), nxt);
-                float pp[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[16];
+        for (int h = 0; h < 2; ++h) {
+            float pp[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * e]), sl2, -mu));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * e + 1]), sl2, -mu));
-                    pp[e & 3] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16_nowait(srow + (uint32_t)(c32 * 16), pk);
-                part += (pp[0] + pp[1]) + (pp[2] + pp[3]);
-                if (c32 + 1 < kKT / 32) {
-                    tmem_wait_ld();
-                    mask_chunk(c32 + 1, nxt);
-                }
+            for (int e = 0; e < 16; ++e) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][2 * e]), sl2, -mu));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][2 * e + 1]), sl2, -mu));
+                pp[e & 3] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
             }
+            tmem_st16_nowait(srow + (uint32_t)(h * 16), pk);
+            part += (pp[0] + pp[1]) + (pp[2] + pp[3]);
         }
         lsum += part;
         tmem_wait_st();
@@ -487,16 +473,18 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
         // stage, tile B after that.
         if (x == 0 || k >= t.nst[0]) {
             const int key = key0 + r;
-            const bool key_ok = key < t.L && ((pmask >> (r >> log2P)) & 1u);
-            if (alive && !key_ok) {
-                const uint32_t vrow = pf_slot(c, slot) + (uint32_t)(kKT * kPD * 2) + (uint32_t)r * 128u;
+            const bool zero_mine = alive && r < kKT && !(key < t.L && ((pmask >> (r >> log2P)) & 1u));
+            if (__any_sync(0xffffffffu, zero_mine)) {
+                if (zero_mine) {
+                    const uint32_t vrow = pf_slot(c, slot) + (uint32_t)(kKT * kPD * 2) + (uint32_t)r * 128u;
 #pragma unroll
-                for (int h = 0; h < kPHalves; ++h)
+                    for (int h = 0; h < kPHalves; ++h)
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_zero16(vrow + (uint32_t)(h * kKT * 128 + ch * 16));
+                        for (int ch = 0; ch < 8; ++ch)
+                            st_shared_zero16(vrow + (uint32_t)(h * kKT * 128 + ch * 16));
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0)
@@ -521,7 +509,7 @@ __device__ void pf_epilogue(const PrefillParams &p, const PfCtx &c, const Tile &
     const int last = t.nst[x] - 1;
     if (last < 0)
         return;                                  // tile B of an odd tile count: no rows
-    bool ok = alive && pf_wait(pf_pvdone(c, x), (uint32_t)(last & 1), c.abort_flag, p.err);
+    bool ok = alive && pf_wait(pf_pvdone(c, x, last & 1), (uint32_t)((last >> 1) & 1), c.abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok)
         return;
@@ -575,9 +563,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 mbar_init(pf_empty(c, v, s), 1);
             }
         for (int x = 0; x < kPTilesPerCta; ++x) {
-            mbar_init(pf_sfull(c, x), 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(pf_sfull(c, x, b), 1);
+                mbar_init(pf_pvdone(c, x, b), 1);
+            }
             mbar_init(pf_pfull(c, x), kPGroupWarps);
-            mbar_init(pf_pvdone(c, x), 1);
         }
         mbar_init(pf_fin(c), 2);
         *c.abort_flag = 0u;
