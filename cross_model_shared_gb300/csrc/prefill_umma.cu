@@ -121,8 +121,10 @@ struct PfSmem {
 
 // ring slots of [K | V][half][64 keys][128 B], then the two Q tiles
 // [tile][half][128 rows][128 B] (all 128-byte swizzled), then the barriers:
-// full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[tile][buf], p_full[tile],
-// pv_done[tile][buf], fin
+// full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[tile][buf], p_full[tile][buf],
+// pv_done[tile][buf], fin.  Everything a tile's softmax hands to the MMA
+// issuers is per S buffer: a softmax group may finish stage k+1 before the
+// PV issuer has waited for stage k, but not stage k+2 (its scores need PV(k)).
 __host__ __device__ inline PfSmem pf_layout()
 {
     PfSmem u;
@@ -130,7 +132,7 @@ __host__ __device__ inline PfSmem pf_layout()
     u.ring = 0;
     u.qtile = (uint32_t)kPStages * u.stage_bytes;
     u.bars = u.qtile + (uint32_t)(kPTilesPerCta * kPHalves * 128 * 128);
-    u.meta = u.bars + (uint32_t)((4 * kPStages + 11) * 8);
+    u.meta = u.bars + (uint32_t)((4 * kPStages + 13) * 8);
     u.misc = u.meta + (uint32_t)(kPStages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;
@@ -151,12 +153,12 @@ __device__ __forceinline__ uint32_t pf_empty(const PfCtx &c, bool v, int s)
     return pbar(c, (v ? 3 : 2) * kPStages + s);
 }
 __device__ __forceinline__ uint32_t pf_sfull(const PfCtx &c, int x, int b) { return pbar(c, 4 * kPStages + 2 * x + b); }
-__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int x) { return pbar(c, 4 * kPStages + 4 + x); }
+__device__ __forceinline__ uint32_t pf_pfull(const PfCtx &c, int x, int b) { return pbar(c, 4 * kPStages + 4 + 2 * x + b); }
 __device__ __forceinline__ uint32_t pf_pvdone(const PfCtx &c, int x, int b)
 {
-    return pbar(c, 4 * kPStages + 6 + 2 * x + b);
+    return pbar(c, 4 * kPStages + 8 + 2 * x + b);
 }
-__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 10); }
+__device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 12); }
 __device__ __forceinline__ uint32_t pf_slot(const PfCtx &c, int s)
 {
     return c.base + c.lay.ring + (uint32_t)s * c.lay.stage_bytes;
@@ -316,7 +318,7 @@ __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
             if (k >= t.nst[x])
                 continue;
             if (alive)
-                alive = pf_wait(pf_pfull(c, x), (uint32_t)(k & 1), c.abort_flag, p.err);
+                alive = pf_wait(pf_pfull(c, x, k & 1), (uint32_t)((k >> 1) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
                 const uint32_t vst = pf_slot(c, slot) + (uint32_t)(kKT * kPD * 2);
@@ -488,7 +490,7 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(pf_pfull(c, x));
+            mbar_arrive(pf_pfull(c, x, buf));
     }
     m_out = m_use;
     l_out = lsum;
@@ -565,9 +567,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int x = 0; x < kPTilesPerCta; ++x) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(pf_sfull(c, x, b), 1);
+                mbar_init(pf_pfull(c, x, b), kPGroupWarps);
                 mbar_init(pf_pvdone(c, x, b), 1);
             }
-            mbar_init(pf_pfull(c, x), kPGroupWarps);
         }
         mbar_init(pf_fin(c), 2);
         *c.abort_flag = 0u;
