@@ -36,6 +36,7 @@
 #include <stdint.h>
 
 #include "shkv_device.cuh"
+#include "prefill.cuh"
 
 namespace shkv {
 
@@ -53,7 +54,7 @@ constexpr int kPVWarp = 11;
 constexpr int kPGroupWarps = 4;          // softmax warps per tile
 constexpr uint32_t kPTmemCols = 512;
 constexpr float kPRescaleLog2 = 8.f;
-constexpr int kPStages = 4;
+constexpr int kPStages = 4;              // ring slots of 32 KB
 constexpr int kPTilesPerCta = 2;
 
 // S buffer b of tile x (P over its first 32 columns), and O of tile x

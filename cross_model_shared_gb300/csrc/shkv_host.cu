@@ -13,6 +13,7 @@
 
 #include "shkv.h"
 #include "shkv_device.cuh"
+#include "prefill.cuh"
 
 namespace shkv {
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
