@@ -41,6 +41,7 @@
 #include <stdint.h>
 
 #include "decode_common.cuh"
+#include "launch.cuh"
 
 namespace shkv {
 
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
                        const __grid_constant__ DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();
     Ctx c;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -523,6 +525,7 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
     }
     fence_proxy_async_smem();
     __syncthreads();
+    pdl_wait_prior();                       // global memory only from here on
 
     const int warp = threadIdx.x >> 5;
     if (warp == ncw)
@@ -547,8 +550,7 @@ static cudaError_t launch_decode_t(const CUtensorMap &tmK, const CUtensorMap &tm
         configured = smem;
     }
     const int threads = (p.nrg * p.wt + 1) * 32;
-    kern<<<p.num_ctas, threads, smem, stream>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, p.num_ctas, threads, smem, stream, tmK, tmV, p);
 }
 
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,

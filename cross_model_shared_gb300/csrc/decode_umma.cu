@@ -48,6 +48,7 @@
 #include <stdint.h>
 
 #include "decode_common.cuh"
+#include "launch.cuh"
 
 namespace shkv {
 
@@ -818,6 +819,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const __grid_constant__ DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();
     TcCtx c;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -871,6 +873,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.tslot);
+    pdl_wait_prior();                       // global memory only from here on
 
     if (warp == kProducerWarp)
         tc_producer<true>(&tmK, &tmV, p, c);
@@ -914,8 +917,7 @@ static cudaError_t launch_umma_t(const CUtensorMap &tmK, const CUtensorMap &tmV,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<p.num_ctas, kTcThreads, smem, stream>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, p.num_ctas, kTcThreads, smem, stream, tmK, tmV, p);
 }
 
 // tmK, tmV: 2-D maps of the pools (box of 64 columns x P rows, 128-byte swizzle).
