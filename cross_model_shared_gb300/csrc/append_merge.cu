@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "launch.cuh"
 #include "shkv_device.cuh"
 
 namespace shkv {
@@ -17,6 +18,8 @@ namespace shkv {
 // reads seq_lens after that store).
 __global__ void __launch_bounds__(256) shkv_append_kernel(const __grid_constant__ AppendParams p)
 {
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int hv = p.head_vecs;                      // 16-byte vectors per head row
     const int64_t rows = (int64_t)p.batch * p.n_new * p.hkv;
     const int64_t total = rows * hv;
@@ -56,8 +59,7 @@ cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t strea
         blocks = (int64_t)num_sms * 8;
     if (blocks < 1)
         blocks = 1;
-    shkv_append_kernel<<<(int)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(shkv_append_kernel, (int)blocks, 256, 0u, stream, p);
 }
 
 // Log-sum-exp merge of split-KV partials.  One warp per (request, row); the
@@ -68,6 +70,8 @@ __global__ void __launch_bounds__(256)
                       const float *__restrict__ lse_part, __nv_bfloat16 *__restrict__ out,
                       float *__restrict__ lse_out)
 {
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int lane = threadIdx.x & 31;
     const int64_t nrow = (int64_t)batch * rows;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -114,6 +118,8 @@ __global__ void __launch_bounds__(256)
 // dst[i] = value for i < n (grid-stride).
 __global__ void __launch_bounds__(256) shkv_fill_kernel(float *__restrict__ dst, int64_t n, float value)
 {
+    pdl_launch_dependents();
+    pdl_wait_prior();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         dst[i] = value;
 }
@@ -125,8 +131,7 @@ cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t str
     int64_t blocks = (n + 255) / 256;
     if (blocks > 1024)
         blocks = 1024;
-    shkv_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dst, n, value);
-    return cudaGetLastError();
+    return launch_pdl(shkv_fill_kernel, (int)blocks, 256, 0u, stream, dst, n, value);
 }
 
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
@@ -134,10 +139,10 @@ cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const 
 {
     const int64_t nrow = (int64_t)batch * rows;
     const int64_t blocks = (nrow + 7) / 8;
-    if (blocks > 0)
-        shkv_merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n_splits, batch, rows, head_dim, o_part,
-                                                                lse_part, out, lse_out);
-    return cudaGetLastError();
+    if (blocks <= 0)
+        return cudaSuccess;
+    return launch_pdl(shkv_merge_kernel, (int)blocks, 256, 0u, stream, n_splits, batch, rows, head_dim, o_part,
+                      lse_part, out, lse_out);
 }
 
 }  // namespace shkv
