@@ -6,6 +6,7 @@
 
 #include "launch.cuh"
 #include "shkv_device.cuh"
+#include "tails.cuh"
 
 namespace shkv {
 
@@ -113,6 +114,49 @@ __global__ void __launch_bounds__(256)
     }
     if (lane == 0 && lse_out)
         lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+// One block per request: its unit of shared pages then each decoder's tail
+// pages, with each page's valid tokens and attending decoder.
+__global__ void __launch_bounds__(256) shkv_tails_unit_kernel(const __grid_constant__ TailsUnitParams p)
+{
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    const int b = blockIdx.x;
+    const int P = p.page_size;
+    const int L = p.shared_len[b];
+    const int S = (L + P - 1) / P;
+    int U = S;
+    for (int m = 0; m < p.n_models; ++m)
+        U += (p.tail_len[b * p.n_models + m] + P - 1) / P;
+    for (int j = threadIdx.x; j < U; j += blockDim.x) {
+        int id, cnt;
+        uint32_t dec = kAllDecoders;
+        if (j < S) {
+            id = __ldg(p.block_table + (int64_t)b * p.bt_stride + j);
+            cnt = j == S - 1 ? L - j * P : P;
+        } else {
+            int jt = j - S, m = 0;
+            for (;; ++m) {
+                const int pages = (p.tail_len[b * p.n_models + m] + P - 1) / P;
+                if (jt < pages)
+                    break;
+                jt -= pages;
+            }
+            const int T = p.tail_len[b * p.n_models + m];
+            const int pages = (T + P - 1) / P;
+            id = __ldg(p.tail_table + ((int64_t)b * p.n_models + m) * p.tt_stride + jt);
+            cnt = jt == pages - 1 ? T - jt * P : P;
+            dec = (uint32_t)m;
+        }
+        p.unit_table[(int64_t)b * p.ustride + j] = id;
+        p.unit_info[(int64_t)b * p.ustride + j] = (uint32_t)cnt | (dec << 8);
+    }
+}
+
+cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream)
+{
+    return launch_pdl(shkv_tails_unit_kernel, p.batch, 256, 0u, stream, p);
 }
 
 // dst[i] = value for i < n (grid-stride).

@@ -52,7 +52,7 @@ using namespace detail;
 // ---------------------------------------------------------------------------
 // consumer warps
 // ---------------------------------------------------------------------------
-template <int D, int NT>
+template <int D, int NT, bool FUSED>
 __device__ void consumer(const DecodeParams &p, const Ctx &c)
 {
     constexpr int KSTEPS = D / 16;
@@ -121,8 +121,10 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 mbar_arrive(qempty_bar(c, qb, stages));
         }
 
-        // --- cached length, from the plan (the producer checks the device copy)
-        const int L = plan_len(p, s);
+        // --- cached length, from the plan (the producer checks the device copy);
+        // fused tails take each page's valid tokens from page_info instead
+        constexpr bool fused = FUSED;
+        const int L = fused ? tok_end : plan_len(p, s);
         const int lim = L < tok_end ? L : tok_end;     // tokens of this segment that count
 
         float o[KSTEPS][NT][4];
@@ -146,7 +148,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 alive = ok;
             }
             bool tag_ok = true;
-            if (ok && (meta[slot] >> 8) != ((uint32_t)k & 0xffffffu)) {
+            if (ok && (meta[slot * kMetaWords] >> 8) != ((uint32_t)k & 0xffffffu)) {
                 // The slot holds another stage: report it, stop this CTA
                 // (bounded) and do not arrive, so no copy is re-armed over it.
                 tag_ok = false;
@@ -160,12 +162,29 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
             if (ok) {
                 const uint32_t kst = c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
                 const uint32_t vst = kst + (uint32_t)(TT * D * 2);
-                const uint32_t mask = meta[slot] & 0xffu;
+                const uint32_t mask = meta[slot * kMetaWords] & 0xffu;
                 const int tok0 = s.p0 * P + j * TT;       // logical token of slot row 0
                 const uint32_t full_mask = (1u << (TT / BR)) - 1u;
-                const bool all_valid = (mask == full_mask) && (tok0 + TT <= lim);
+                // fused tails: per row-block (one page) its valid tokens and
+                // the decoder whose rows attend it
+                const uint32_t whole = kAllDecoders << 8 | (uint32_t)BR;
+                uint32_t inf0 = whole, inf1 = whole;
+                if (fused) {
+                    inf0 = meta[slot * kMetaWords + 1];
+                    inf1 = TT / BR > 1 ? meta[slot * kMetaWords + 2] : inf0;
+                }
+                const bool all_valid = (mask == full_mask) &&
+                                       (fused ? (inf0 == whole && inf1 == whole) : (tok0 + TT <= lim));
                 auto tok_valid = [&](int t) -> bool {
-                    return ((mask >> (t >> log2BR)) & 1u) && (tok0 + t < lim);
+                    if (!fused)
+                        return ((mask >> (t >> log2BR)) & 1u) && (tok0 + t < lim);
+                    const int rb = t >> log2BR;
+                    return ((mask >> rb) & 1u) && (uint32_t)(t & (BR - 1)) < ((rb ? inf1 : inf0) & 0xffu);
+                };
+                // (fused tails) row r of the N*G stacked rows attends token t
+                auto row_attends = [&](int t, int r) -> bool {
+                    const uint32_t dec = (((t >> log2BR) ? inf1 : inf0) >> 8) & 0xffu;
+                    return dec == kAllDecoders || (uint32_t)(r - (int)dec * p.group) < (uint32_t)p.group;
                 };
                 if (!all_valid) {
                     // Rows that are masked may hold stale or non-finite bits:
@@ -213,8 +232,12 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float x = (sc[mt][nt][e] + sc2[mt][nt][e]) * sl2;
-                            if (!all_valid && !tok_valid(mt * 16 + (lane >> 2) + (e >> 1) * 8))
-                                x = -INFINITY;
+                            if (!all_valid) {
+                                const int tt = mt * 16 + (lane >> 2) + (e >> 1) * 8;
+                                if (!tok_valid(tt) ||
+                                    (fused && !row_attends(tt, row0 + nt * 8 + (lane & 3) * 2 + (e & 1))))
+                                    x = -INFINITY;
+                            }
                             sc[mt][nt][e] = x;
                         }
                 uint32_t pb[MTS][NT][2];
@@ -478,7 +501,8 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 
 }  // namespace
 
-template <int D, int NT>
+// FUSED: the units are fused per-decoder tails (DecodeParams::page_info).
+template <int D, int NT, bool FUSED>
 __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
     shkv_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ DecodeParams p)
@@ -529,19 +553,19 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
 
     const int warp = threadIdx.x >> 5;
     if (warp == ncw)
-        producer<D>(&tmK, &tmV, p, c);
+        producer<D, FUSED>(&tmK, &tmV, p, c);
     else if (warp < ncw)
-        consumer<D, NT>(p, c);
+        consumer<D, NT, FUSED>(p, c);
 }
 
 // ---------------------------------------------------------------------------
 // host-side launcher (internal to the library)
 // ---------------------------------------------------------------------------
-template <int D, int NT>
-static cudaError_t launch_decode_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+template <int D, int NT, bool FUSED>
+static cudaError_t launch_decode_f(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                                    uint32_t smem, cudaStream_t stream)
 {
-    auto kern = shkv_decode_kernel<D, NT>;
+    auto kern = shkv_decode_kernel<D, NT, FUSED>;
     static uint32_t configured = 0;
     if (smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -551,6 +575,14 @@ static cudaError_t launch_decode_t(const CUtensorMap &tmK, const CUtensorMap &tm
     }
     const int threads = (p.nrg * p.wt + 1) * 32;
     return launch_pdl(kern, p.num_ctas, threads, smem, stream, tmK, tmV, p);
+}
+
+template <int D, int NT>
+static cudaError_t launch_decode_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+                                   uint32_t smem, cudaStream_t stream)
+{
+    return p.fused ? launch_decode_f<D, NT, true>(tmK, tmV, p, smem, stream)
+                   : launch_decode_f<D, NT, false>(tmK, tmV, p, smem, stream);
 }
 
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,

@@ -90,6 +90,13 @@ __device__ __forceinline__ int cta_of(const DecodeParams &p, int64_t idx)
     return lo;
 }
 
+// Window load of the unit table (page ids) or of page_info: entry j of
+// request b's row, -1 past the segment.
+__device__ __forceinline__ int unit_entry(const int32_t *table, const DecodeParams &p, int b, int j, int jend)
+{
+    return j < jend ? __ldg(table + (int64_t)b * p.max_pages + j) : -1;
+}
+
 // Cached length of request b, from the split plan (the host's copy).
 __device__ __forceinline__ int plan_len(const DecodeParams &p, const Segment &s)
 {
@@ -139,7 +146,8 @@ __device__ __forceinline__ uint32_t qempty_bar(const Ctx &c, int i, int stages)
 // Stage j of a segment holds the kStageTokens logical tokens starting at
 // p0*P + j*kStageTokens, as one or two row-blocks of BR = min(P, kStageTokens)
 // rows, each row-block inside one page.
-template <int D>
+// FUSED: the units are fused per-decoder tails (DecodeParams::page_info).
+template <int D, bool FUSED>
 __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,
                          const Ctx &c)
 {
@@ -164,17 +172,23 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
     Segment s = locate(p, c.cta_begin, c.cta_end);
     // first block-table window of the current segment, prefetched one
     // segment ahead
-    int pre = (lane < s.p1 - s.p0) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
+    const int32_t *info_tab = reinterpret_cast<const int32_t *>(p.page_info);
+    constexpr bool fused = FUSED;
+    int pre = unit_entry(p.block_table, p, s.b, s.p0 + lane, s.p1);
+    int pre_i = fused ? unit_entry(info_tab, p, s.b, s.p0 + lane, s.p1) : -1;
     for (;;) {
         const bool has_next = s.seg_end < c.cta_end;
         Segment sn;
-        int pre_next = -1;
+        int pre_next = -1, pre_next_i = -1;
         if (has_next) {
             sn = next_segment(p, s, c.cta_end);
-            pre_next = (lane < sn.p1) ? __ldg(p.block_table + (int64_t)sn.b * p.max_pages + lane) : -1;
+            pre_next = unit_entry(p.block_table, p, sn.b, lane, sn.p1);
+            if (fused)
+                pre_next_i = unit_entry(info_tab, p, sn.b, lane, sn.p1);
         }
         // device copy of the length, checked at the end of the segment
-        const int dev_len = (lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
+        // (a unit of fused tails is not one sequence: nothing to check)
+        const int dev_len = (lane == 0 && !fused) ? __ldg(p.seq_lens + s.b) : 0;
         // --- query rows of this (b, g): N bulk copies of G contiguous rows
         const int qb = seg & 1;
         if (alive) {
@@ -196,8 +210,9 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
         const int nst = (tok_end - s.p0 * P + TT - 1) / TT;
         const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
         int w0 = s.p0;                                   // block-table window [w0, w0+32)
-        int cur = pre;
+        int cur = pre, cur_i = pre_i;
         int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+        int nxt_i = fused ? unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1) : -1;
         // Lane 4*sub + 2*rb + kv copies row-block rb of K (kv = 0) or V
         // (kv = 1) for stage j + sub of this iteration.
         const int sub = lane >> 2;
@@ -215,10 +230,19 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
                 w0 += 32;
                 cur = nxt;
                 nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+                if (fused) {
+                    cur_i = nxt_i;
+                    nxt_i = unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1);
+                }
             }
             const int my_tok = tok0 + my_rb * BR;
             const int my_pg = my_tok >> log2P;
             const int my_id = __shfl_sync(0xffffffffu, cur, (my_pg - w0) & 31);
+            int my_info = 0, rb1_info = 0;
+            if (fused) {
+                my_info = __shfl_sync(0xffffffffu, cur_i, (my_pg - w0) & 31);
+                rb1_info = __shfl_sync(0xffffffffu, my_info, (lane + 2) & 31);   // row-block 1, seen by lane 4*sub
+            }
             bool ok = true;
             if (alive && in_iter && (lane & 3) == 0)
                 ok = mbar_wait_bounded(empty_bar(c, slot, stages), ((k / stages) & 1) ^ 1, c.abort_flag, p.err);
@@ -234,8 +258,12 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
                     else if (tok0 + rb * BR < tok_end)
                         atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
                 }
-                volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
-                meta[slot] = mask | ((uint32_t)k << 8);   // valid row-blocks + stage tag
+                volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta) + slot * kMetaWords;
+                if (fused) {
+                    meta[1] = (uint32_t)my_info;
+                    meta[2] = (uint32_t)rb1_info;
+                }
+                meta[0] = mask | ((uint32_t)k << 8);   // valid row-blocks + stage tag
                 mbar_arrive_expect_tx(full_bar(c, slot), (uint32_t)__popc(mask) * rb_bytes_kv);
             }
             __syncwarp();
@@ -251,7 +279,7 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
             }
             __syncwarp();
         }
-        if (lane == 0 && dev_len != plan_len(p, s))
+        if (lane == 0 && !fused && dev_len != plan_len(p, s))
             atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
         kbase += nst;
         ++seg;
@@ -259,6 +287,7 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
             break;
         s = sn;
         pre = pre_next;
+        pre_i = pre_next_i;
     }
     // After an abort, wait (bounded) for every copy this CTA still has in
     // flight so no TMA write lands after the CTA exits.

@@ -110,7 +110,7 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
     // qempty, s_full[2], s_free[2], q_ready, q_tile_free, fin
     u.bars = align_up(u.rowoff + 64u * 4u, 8);
     u.meta = u.bars + (uint32_t)((4 * stages + 9) * 8);
-    u.misc = u.meta + (uint32_t)(stages * 4);
+    u.misc = u.meta + (uint32_t)(stages * kMetaWords * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
     return u;
@@ -264,16 +264,22 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
     int last_issued_stage = -1;
     int q_issued = -1;
     Segment s = locate(p, c.cta_begin, c.cta_end);
-    int pre = (lane < s.p1 - s.p0) ? __ldg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane) : -1;
+    const int32_t *info_tab = reinterpret_cast<const int32_t *>(p.page_info);
+    const bool fused = kIsK && p.fused != 0;          // the K warp publishes page_info
+    int pre = unit_entry(p.block_table, p, s.b, s.p0 + lane, s.p1);
+    int pre_i = fused ? unit_entry(info_tab, p, s.b, s.p0 + lane, s.p1) : -1;
     for (;;) {
         const bool has_next = s.seg_end < c.cta_end;
         Segment sn;
-        int pre_next = -1;
+        int pre_next = -1, pre_next_i = -1;
         if (has_next) {
             sn = next_segment(p, s, c.cta_end);
-            pre_next = (lane < sn.p1) ? __ldg(p.block_table + (int64_t)sn.b * p.max_pages + lane) : -1;
+            pre_next = unit_entry(p.block_table, p, sn.b, lane, sn.p1);
+            if (fused)
+                pre_next_i = unit_entry(info_tab, p, sn.b, lane, sn.p1);
         }
-        const int dev_len = (kIsK && lane == 0) ? __ldg(p.seq_lens + s.b) : 0;
+        // (a unit of fused tails is not one sequence: no length to check)
+        const int dev_len = (kIsK && lane == 0 && p.fused == 0) ? __ldg(p.seq_lens + s.b) : 0;
         // --- query rows of this (b, g): N bulk copies of G contiguous rows
         if (kIsK) {
             if (alive) {
@@ -296,8 +302,9 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
         const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
         const int32_t *btrow = p.block_table + (int64_t)s.b * p.max_pages;
         int w0 = s.p0;                                   // block-table window [w0, w0+32)
-        int cur = pre;
+        int cur = pre, cur_i = pre_i;
         int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+        int nxt_i = fused ? unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1) : -1;
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int slot = k % stages;
@@ -308,9 +315,21 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                 w0 += 32;
                 cur = nxt;
                 nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
+                if (fused) {
+                    cur_i = nxt_i;
+                    nxt_i = unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1);
+                }
             }
             const int my_tok = tok0 + my_rb * P;
             const int my_id = __shfl_sync(0xffffffffu, cur, ((my_tok >> log2P) - w0) & 31);
+            // page_info of page rb of the stage, gathered to lane 0 (lane rb < RB holds page rb)
+            uint32_t pinfo[8];
+            if (fused) {
+                const int my_info = __shfl_sync(0xffffffffu, cur_i, ((my_tok >> log2P) - w0) & 31);
+#pragma unroll
+                for (int rb = 0; rb < 8; ++rb)
+                    pinfo[rb] = (uint32_t)__shfl_sync(0xffffffffu, my_info, rb);
+            }
             bool ok = true;
             if (alive && lane == 0)
                 ok = mbar_wait_bounded(empty_b(c, slot), (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
@@ -323,8 +342,15 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                     for (int rb = 0; rb < RB; ++rb)
                         if (!((mask >> rb) & 1u) && tok0 + rb * P < tok_end)
                             atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
-                    volatile uint32_t *meta = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta);
-                    meta[slot] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
+                    volatile uint32_t *meta =
+                        reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta) + slot * kMetaWords;
+                    if (fused) {
+#pragma unroll
+                        for (int rb = 0; rb < 8; ++rb)
+                            if (rb < RB)
+                                meta[1 + rb] = pinfo[rb];
+                    }
+                    meta[0] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
                     mbar_arrive_expect_tx(full_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
                 }
                 if (!kIsK || !split)
@@ -341,7 +367,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                 last_issued_stage = k;
             __syncwarp();
         }
-        if (kIsK && lane == 0 && dev_len != plan_len(p, s))
+        if (kIsK && lane == 0 && p.fused == 0 && dev_len != plan_len(p, s))
             atomicOr(p.err, SHKV_ERRF_SEQ_LEN);
         kbase += nst;
         ++seg;
@@ -349,6 +375,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
             break;
         s = sn;
         pre = pre_next;
+        pre_i = pre_next_i;
     }
     // After an abort, wait (bounded) for the copies still in flight so no TMA
     // write lands after the CTA exits.
@@ -523,7 +550,8 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     for (;;) {
         const int tok_end = s.p1 * P;
         const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
-        const int L = plan_len(p, s);
+        const bool fused = p.fused != 0;
+        const int L = fused ? tok_end : plan_len(p, s);   // fused tails: valid tokens per page from page_info
         const int lim = L < tok_end ? L : tok_end;
         float m_use[NH], lhi[NH], lex[NH];
 #pragma unroll
@@ -553,7 +581,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 mbar_arrive(s_free_b(c, buf));
             // the slot's validity word (the QK MMA has already consumed the data)
             wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
-            const uint32_t tagged = alive ? meta[slot] : 0u;
+            const uint32_t tagged = alive ? meta[slot * kMetaWords] : 0u;
             if (alive && (tagged >> 8) != ((uint32_t)k & 0xffffffu)) {
                 if (lane == 0) {
                     atomicOr(p.err, SHKV_ERRF_PIPELINE);
@@ -562,7 +590,11 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 alive = false;
             }
             const int tok0 = s.p0 * P + j * kTT;
-            const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) && (tok0 + t < lim);
+            // fused tails: this token's page holds info (valid tokens, decoder)
+            const uint32_t tinfo = fused && alive ? meta[slot * kMetaWords + 1 + (t >> log2P)] : (kAllDecoders << 8);
+            const uint32_t tdec = (tinfo >> 8) & 0xffu;
+            const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) &&
+                               (fused ? (uint32_t)(t & (P - 1)) < (tinfo & 0xffu) : (tok0 + t < lim));
             const uint32_t kst = c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
             // rows past the length inside a copied page are written by the V
             // copy: zero them only after it has landed
@@ -581,7 +613,10 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             bool need = false;
 #pragma unroll
             for (int i = 0; i < NH; ++i) {
-                xs[i] = valid ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
+                // a tail page is attended by its decoder's rows only
+                const bool attends =
+                    tdec == kAllDecoders || (uint32_t)(half_row(hh, i) - (int)tdec * p.group) < (uint32_t)p.group;
+                xs[i] = valid && attends ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
                 need = need || (xs[i] > m_use[i] + kRescaleLog2);
             }
             // --- lazy max refresh: the eight warps agree on a new m[] together

@@ -92,6 +92,10 @@ constexpr int kMaxCtas = 256;
 constexpr int kSegmentCostChunks = SHKV_SEGMENT_COST_CHUNKS;
 // Wall-clock limit for any single wait on an mbarrier.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Per ring slot, the producer publishes a word of valid pages + stage tag and,
+// for fused tails, one page_info word per page of the stage (up to 8).
+constexpr int kMetaWords = 16;
+constexpr uint32_t kAllDecoders = 0xffu;
 // Dynamic shared memory a CTA may use on sm_100-family parts.
 constexpr int kSmemLimit = 232448;
 
@@ -101,6 +105,12 @@ struct DecodeParams {
     float *out_f32;            // when set, final rows go here in fp32 instead of to out
     float *lse_out;            // [B, N*Hq] or null (required with out_f32)
     const int32_t *block_table;
+    // Per-decoder tails in one pass: when set, a request's unit of pages is
+    // its shared pages followed by each decoder's tail pages (block_table is
+    // that unit table), and page_info[b * max_pages + j] describes page j:
+    // valid tokens (bits 0-7) and the decoder whose rows attend it (bits
+    // 8-15, kAllDecoders for a shared page).
+    const uint32_t *page_info;
     const int32_t *seq_lens;
     uint32_t *err;
     uint32_t *ws_count;        // [B*Hkv] arrival counters, zero between calls
@@ -113,7 +123,7 @@ struct DecodeParams {
     int32_t split_producers;   // tcgen05 consumer: K and V copied by separate warps
     int64_t total_chunks;
     float scale_log2;
-    float pad1;
+    int32_t fused;             // page_info is set (see above)
     int32_t cta_cut[kMaxCtas + 1];             // first chunk of each CTA; [num_ctas] = total
     int32_t page_prefix[SHKV_MAX_BATCH + 1];   // pages before each request
     uint8_t last_fill[SHKV_MAX_BATCH];         // tokens in each request's last page (1..P)
@@ -152,7 +162,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int rows_w, int 
     s.comb_l = s.comb_m + (uint32_t)(ncw * rows_w * 4);
     s.bars = align_up(s.comb_l + (uint32_t)(ncw * rows_w * 4), 8);
     s.meta = s.bars + (uint32_t)((2 * stages + 4) * 8);
-    s.misc = s.meta + (uint32_t)(stages * 4);
+    s.misc = s.meta + (uint32_t)(stages * kMetaWords * 4);
     s.total = s.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
     return s;
 }

@@ -14,6 +14,7 @@
 #include "shkv.h"
 #include "shkv_device.cuh"
 #include "prefill.cuh"
+#include "tails.cuh"
 
 namespace shkv {
 cudaError_t launch_decode(int D, int NT, const CUtensorMap &tmK, const CUtensorMap &tmV,
@@ -24,6 +25,7 @@ int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
 cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream);
+cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream);
 int prefill_tiles_per_cta();
 uint32_t prefill_smem_bytes();
 cudaError_t launch_prefill_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, const PrefillParams &p, uint32_t smem,
@@ -430,12 +432,23 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
 
 namespace {
 
+// Units of a decode with per-decoder tails in one pass: the unit table and
+// page info built on the device, their row stride, and each request's unit
+// length in tokens (whole pages), which the split plan is built from.
+struct FusedUnits {
+    const int32_t *table;
+    const uint32_t *info;
+    int32_t stride;
+    const int32_t *unit_tokens;
+};
+
 // One decode launch: final rows to out (bf16) or, when out_f32 is set, to
 // out_f32 (fp32; lse_out then required).  Launches nothing when the pool has
-// no chunks (every length zero, possible only for a tail view).
+// no chunks (every length zero, possible only for a tail view).  With fu,
+// request b's unit is fu's row b instead of the pool's block table.
 shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
                         float scale, void *out, float *out_f32, float *lse_out, void *workspace,
-                        size_t workspace_bytes, void *stream)
+                        size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr)
 {
     if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
         hq_per_model < 1)
@@ -459,8 +472,8 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
 
     DecodeParams p;
     memset(&p, 0, sizeof p);
-    shkv_status st = build_plan(batch, pool->lens.data(), c.page_size, c.num_kv_heads, pool->num_sms,
-                                p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas,
+    shkv_status st = build_plan(batch, fu ? fu->unit_tokens : pool->lens.data(), c.page_size, c.num_kv_heads,
+                                pool->num_sms, p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas,
                                 pool->tails_view);
     if (st != SHKV_OK)
         return st;
@@ -501,7 +514,9 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.out_f32 = out_f32;
     p.lse_out = lse_out;
-    p.block_table = c.block_table;
+    p.block_table = fu ? fu->table : c.block_table;
+    p.page_info = fu ? fu->info : nullptr;
+    p.fused = fu ? 1 : 0;
     p.seq_lens = c.seq_lens;
     p.err = c.error_word;
     p.ws_count = reinterpret_cast<uint32_t *>(ws);
@@ -519,7 +534,7 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     p.stages = stages;
     p.page_size = c.page_size;
     p.box_rows = c.page_size < kStageTokens ? c.page_size : kStageTokens;
-    p.max_pages = c.max_pages_per_seq;
+    p.max_pages = fu ? fu->stride : c.max_pages_per_seq;
     p.num_pages = c.num_pages;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     // tcgen05 consumer: 16-token pages make 32 copies a stage, issued by two
@@ -533,22 +548,21 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace of a decode with tails: the shared pass's, the tail pass's, then
-// fp32 partials [2, B, rows, D] and their log-sum-exps [2, B, rows].
+// Workspace of a decode with tails: the decode's own, then the unit table
+// and page info [B, stride] with stride = max_pages_per_seq + N * max_tail_pages.
 struct TailsWorkspace {
-    size_t shared, tail, parts, lses, total;
+    size_t decode, table, stride, total;
 };
 
-TailsWorkspace tails_workspace(const shkv_pool *pool, int32_t batch, int32_t n_models, int32_t group)
+TailsWorkspace tails_workspace(const shkv_pool *pool, const shkv_tails *tails, int32_t batch, int32_t group)
 {
     const shkv_pool_config &c = pool->cfg;
     TailsWorkspace w;
-    const size_t rows_all = (size_t)batch * n_models * group * c.num_kv_heads;
-    w.shared = align256(workspace_bytes_for(batch, c.num_kv_heads, n_models * group, c.head_dim, pool->num_sms));
-    w.tail = align256(workspace_bytes_for(batch * n_models, c.num_kv_heads, group, c.head_dim, pool->num_sms));
-    w.parts = align256(2 * rows_all * c.head_dim * 4);
-    w.lses = align256(2 * rows_all * 4);
-    w.total = w.shared + w.tail + w.parts + w.lses;
+    w.decode = align256(workspace_bytes_for(batch, c.num_kv_heads, tails->n_models * group, c.head_dim,
+                                            pool->num_sms));
+    w.stride = (size_t)c.max_pages_per_seq + (size_t)tails->n_models * tails->max_tail_pages;
+    w.table = align256((size_t)batch * w.stride * 4);
+    w.total = w.decode + 2 * w.table;
     return w;
 }
 
@@ -687,7 +701,7 @@ shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_t
         return SHKV_ERR_INVALID_ARG;
     if (hq_per_model % pool->cfg.num_kv_heads)
         return SHKV_ERR_UNSUPPORTED;
-    *bytes = tails_workspace(pool, batch, tails->n_models, hq_per_model / pool->cfg.num_kv_heads).total;
+    *bytes = tails_workspace(pool, tails, batch, hq_per_model / pool->cfg.num_kv_heads).total;
     return SHKV_OK;
 }
 
@@ -706,30 +720,47 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
         return SHKV_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || ((uintptr_t)lse_out & 3u))
         return SHKV_ERR_INVALID_ARG;
+    if (N > 254 ||
+        ((int64_t)pool->cfg.max_pages_per_seq + (int64_t)N * tails->max_tail_pages) * pool->cfg.page_size > INT32_MAX)
+        return SHKV_ERR_UNSUPPORTED;
     const int group = hq_per_model / pool->cfg.num_kv_heads;
-    const TailsWorkspace w = tails_workspace(pool, batch, N, group);
+    const TailsWorkspace w = tails_workspace(pool, tails, batch, group);
     if (workspace_bytes < w.total)
         return SHKV_ERR_INVALID_ARG;
+    // One pass: request b's unit is its shared pages then each decoder's tail
+    // pages; a tail page is attended by its decoder's rows only.
+    const int32_t P = pool->cfg.page_size;
+    TailsUnitParams up;
+    memset(&up, 0, sizeof up);
+    std::vector<int32_t> unit_tokens((size_t)batch);
+    for (int b = 0; b < batch; ++b) {
+        const int32_t L = pool->lens[b];
+        if (L < 1)
+            return SHKV_ERR_INVALID_ARG;
+        up.shared_len[b] = L;
+        int64_t pages = (L + P - 1) / P;
+        for (int m = 0; m < N; ++m) {
+            const int32_t T = tails->view->lens[(size_t)b * N + m];
+            up.tail_len[b * N + m] = T;
+            pages += (T + P - 1) / P;
+        }
+        unit_tokens[b] = (int32_t)(pages * P);
+    }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int rows = N * hq_per_model;                    // output rows per request
-    const int64_t nrow = (int64_t)batch * rows;
-    float *o_part = reinterpret_cast<float *>(ws + w.shared + w.tail);
-    float *lse_part = reinterpret_cast<float *>(ws + w.shared + w.tail + w.parts);
-    cudaStream_t st = (cudaStream_t)stream;
-    // an empty tail writes nothing: its partial keeps lse = -inf (weight 0)
-    if (cudaError_t e = launch_fill_f32(lse_part + nrow, nrow, -INFINITY, st); e != cudaSuccess)
+    up.block_table = pool->cfg.block_table;
+    up.tail_table = tails->view->cfg.block_table;
+    up.unit_table = reinterpret_cast<int32_t *>(ws + w.decode);
+    up.unit_info = reinterpret_cast<uint32_t *>(ws + w.decode + w.table);
+    up.bt_stride = pool->cfg.max_pages_per_seq;
+    up.tt_stride = tails->max_tail_pages;
+    up.ustride = (int32_t)w.stride;
+    up.batch = batch;
+    up.n_models = N;
+    up.page_size = P;
+    if (cudaError_t e = launch_tails_units(up, (cudaStream_t)stream); e != cudaSuccess)
         return SHKV_ERR_CUDA;
-    // tail pass: (request, decoder) pairs as requests, one decoder's G rows each
-    shkv_status s = decode_impl(tails->view, batch * N, 1, hq_per_model, q, scale, nullptr, o_part + nrow * pool->cfg.head_dim,
-                                lse_part + nrow, ws + w.shared, w.tail, stream);
-    if (s != SHKV_OK)
-        return s;
-    // shared pass: all decoders' rows stacked over the shared prefix
-    s = decode_impl(pool, batch, N, hq_per_model, q, scale, nullptr, o_part, lse_part, ws, w.shared, stream);
-    if (s != SHKV_OK)
-        return s;
-    return cuda_status(launch_merge(2, batch, rows, pool->cfg.head_dim, o_part, lse_part,
-                                    static_cast<__nv_bfloat16 *>(out), lse_out, st));
+    const FusedUnits fu{up.unit_table, up.unit_info, up.ustride, unit_tokens.data()};
+    return decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu);
 }
 
 shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)

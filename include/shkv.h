@@ -246,11 +246,14 @@ shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_t
  * shkv_decode_attention where every decoder also attends its own tail:
  * out[b, m*Hq + h] = softmax attention over [shared prefix ++ tail(b, m)].
  * q / out / lse_out as in shkv_decode_attention with n_models = the tails'
- * n_models.  Runs the tail pass (each (request, decoder) pair over its tail,
- * G rows per KV head), the shared pass (all N*G rows stacked over the shared
- * prefix), both to fp32 partials, then the log-sum-exp merge of the two.
- * Supported: batch * n_models <= SHKV_MAX_BATCH, rest as
- * shkv_decode_attention.  Errors as shkv_decode_attention.
+ * n_models.  One pass over the pages: a small kernel lays out each request's
+ * unit (its shared pages, then each decoder's tail pages, read from the
+ * device block and tail tables with the host copies of the lengths), then
+ * the decode kernel streams every unit once for all N*G stacked rows, a tail
+ * page being attended by its own decoder's G rows only.  Supported:
+ * batch * n_models <= SHKV_MAX_BATCH, n_models <= 254, rest as
+ * shkv_decode_attention.  Errors as shkv_decode_attention (the device copies
+ * of the lengths are not compared: SHKV_ERRF_SEQ_LEN is not raised here).
  */
 shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int32_t batch, int32_t hq_per_model,
                                         const void *q, float scale, void *out, float *lse_out, void *workspace,
