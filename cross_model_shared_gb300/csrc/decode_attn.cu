@@ -173,8 +173,12 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     inf0 = meta[slot * kMetaWords + 1];
                     inf1 = TT / BR > 1 ? meta[slot * kMetaWords + 2] : inf0;
                 }
-                const bool all_valid = (mask == full_mask) &&
-                                       (fused ? (inf0 == whole && inf1 == whole) : (tok0 + TT <= lim));
+                // every token of the stage is a real key (no V row to clear) ...
+                const bool toks_valid =
+                    (mask == full_mask) &&
+                    (fused ? ((inf0 & 0xffu) == (uint32_t)BR && (inf1 & 0xffu) == (uint32_t)BR) : (tok0 + TT <= lim));
+                // ... and every row attends every token (no score to mask)
+                const bool all_valid = toks_valid && (!fused || (inf0 == whole && inf1 == whole));
                 auto tok_valid = [&](int t) -> bool {
                     if (!fused)
                         return ((mask >> (t >> log2BR)) & 1u) && (tok0 + t < lim);
@@ -186,7 +190,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     const uint32_t dec = (((t >> log2BR) ? inf1 : inf0) >> 8) & 0xffu;
                     return dec == kAllDecoders || (uint32_t)(r - (int)dec * p.group) < (uint32_t)p.group;
                 };
-                if (!all_valid) {
+                if (!toks_valid) {
                     // Rows that are masked may hold stale or non-finite bits:
                     // zero their V so 0 * V stays 0 in the PV product.
                     for (int e = lane; e < TT * (D / 8); e += 32) {
@@ -307,7 +311,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                             mma_bf16(o[mt][nt], a0, a1, a2, a3, pb[kt][nt][0], pb[kt][nt][1]);
                     }
                 }
-                if (!all_valid)
+                if (!toks_valid)
                     fence_proxy_async_smem();   // generic zero-writes before the next TMA into this slot
             }
             __syncwarp();
