@@ -1,10 +1,10 @@
 """Per-decoder unique tails on the GPU against the fp64 oracle.
 
 Decoder m of request b attends the shared prefix and its own tail
-(PrefillShare Sec. 3.3-4, Eqs. 8-9).  The library runs a tail pass over the
-(request, decoder) pairs, the shared pass over the stacked rows, and a
-log-sum-exp merge; these tests compare with the oracle's direct definition
-over the concatenated token list.
+(PrefillShare Sec. 3.3-4, Eqs. 8-9).  The library streams each request's
+shared pages and then every decoder's tail pages in one pass, a tail page
+attended by its own decoder's rows only; these tests compare with the
+oracle's direct definition over the concatenated token list.
 """
 import numpy as np
 import pytest
@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 SHAPES = {
     "llama8b": dict(N=2, Hq=32, Hkv=8, D=128, P=16),      # shared pass R = 8 (mma.sync)
     "qwen14b": dict(N=8, Hq=40, Hkv=8, D=128, P=32),      # shared pass R = 40 (tcgen05)
+    "qwen8b": dict(N=4, Hq=32, Hkv=8, D=128, P=16),       # R = 16: tcgen05 with 16-token pages (two producers)
     "d64": dict(N=3, Hq=8, Hkv=2, D=64, P=16),            # head dim 64
 }
 
@@ -136,3 +137,42 @@ def test_out_of_range_tail_page_sets_flag():
     out = tob.decode_attention(bits_to_torch(q), scale=wl.scale)
     assert pool.check_errors() & N.SHKV_ERRF_PAGE_OOB
     assert bool(torch.isfinite(out.float()).all())
+
+
+@pytest.mark.parametrize("name", ["llama8b", "qwen8b"])
+def test_full_size_tails_sampled_requests(name):
+    """A full-size workload with 128-384-token tails per decoder (pools on the
+    device); the shortest, median and longest requests are recomputed by the
+    oracle from their shared and tail pages read back."""
+    base = W.make_workload(name)
+    rng = np.random.default_rng(base.seed + 4242)
+    tails = rng.integers(128, 385, size=(base.B, base.N)).astype(np.int32)
+    wl = W.custom_workload(f"{name}+tails", B=base.B, N=base.N, Hq=base.Hq, Hkv=base.Hkv, D=base.D, P=base.P,
+                           lens_prefill=base.lens_prefill, n_append=base.n_append, seed=base.seed,
+                           spare_pages=W.tails_spare_pages(tails, base.P))
+    tt, tl = W.make_tails(wl, tails, seed=wl.seed + 1)
+    q = W.gen_q(wl)
+    k_dev, v_dev = W.gen_pool_device(wl)
+    pool = make_pool(wl, k_dev, v_dev)
+    tob = DecoderTails(pool, wl.B, wl.N, tt.shape[2], initial_tail_lens=tl)
+    tob.block_table.copy_(torch.from_numpy(tt))
+    out, lse = tob.decode_attention(bits_to_torch(q), scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    assert bool(torch.isfinite(out.float()).all())
+    order = np.argsort(wl.lens_final)
+    for b in sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])}):
+        npg = int((wl.lens_final[b] + wl.P - 1) // wl.P)
+        tpg = [int((tl[b, m] + wl.P - 1) // wl.P) for m in range(wl.N)]
+        ids = np.concatenate([wl.block_table[b, :npg]] + [tt[b, m, :tpg[m]] for m in range(wl.N)]).astype(np.int64)
+        sel = torch.from_numpy(ids).to(k_dev.device)
+        kb, vb = torch_to_bits(k_dev.index_select(0, sel)), torch_to_bits(v_dev.index_select(0, sel))
+        # the request's pages renumbered 0.. in the order gathered: shared, then each tail
+        bt = np.arange(npg, dtype=np.int32)[None, :]
+        ttb = np.full((1, wl.N, max(1, max(tpg))), -1, np.int32)
+        off = npg
+        for m in range(wl.N):
+            ttb[0, m, :tpg[m]] = np.arange(off, off + tpg[m], dtype=np.int32)
+            off += tpg[m]
+        ref, lref = oracle.decode_attention_tails(q[b:b + 1], kb, vb, bt, np.array([wl.lens_final[b]], np.int32),
+                                                  ttb, tl[b:b + 1], n_models=wl.N, hq=wl.Hq, scale=wl.scale)
+        compare(out[b], ref[0], lse[b], lref[0], what=f"{name}+tails[b={b}, L={wl.lens_final[b]}]")
