@@ -74,9 +74,9 @@ constexpr float kRescaleLog2 = 10.f;
 constexpr int kTcMaxStages = 4;
 // scratch rows of 64 floats: stage maxima [token group], new max, rescale
 // factor, row-sum partials [token group] (rounded and exact), running max,
-// the reciprocal rounded-weight row sum, the exact row sum
+// the reciprocal rounded-weight row sum (one spare row keeps the layout)
 constexpr int kScrMax = 0, kScrNew = 4, kScrAlpha = 5, kScrLhi = 6, kScrLex = 10, kScrM = 14, kScrSumHi = 15,
-              kScrSumEx = 16, kScrRows = 17;
+              kScrRows = 17;
 
 static_assert(kTT == 32 * kTokenGroups, "one softmax thread per token of a stage and row half");
 static_assert(kD == 32 * kTokenGroups, "one softmax thread per column of O^T and row half");
