@@ -553,13 +553,17 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
     }
     fence_proxy_async_smem();
     __syncthreads();
-    pdl_wait_prior();                       // global memory only from here on
 
     const int warp = threadIdx.x >> 5;
-    if (warp == ncw)
+    if (warp == ncw) {
+        warm_l2<D>(&tmK, &tmV, p, c);
+        pdl_wait_prior();                   // global memory only from here on
         producer<D, FUSED>(&tmK, &tmV, p, c);
-    else if (warp < ncw)
-        consumer<D, NT, FUSED>(p, c);
+    } else {
+        pdl_wait_prior();
+        if (warp < ncw)
+            consumer<D, NT, FUSED>(p, c);
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -146,6 +146,32 @@ __device__ __forceinline__ uint32_t qempty_bar(const Ctx &c, int i, int stages)
 // Stage j of a segment holds the kStageTokens logical tokens starting at
 // p0*P + j*kStageTokens, as one or two row-blocks of BR = min(P, kStageTokens)
 // rows, each row-block inside one page.
+// Run by the producer warp before it waits for the previous grid: prefetch
+// into L2 the K/V row-blocks of this CTA's first ring-full of stages (up to
+// 32 pages of its first segment), so that its first copies after the wait
+// hit L2 instead of waiting on DRAM.  The block-table entries are read
+// through L2 only and may be stale (a preceding kernel may still be writing
+// them): they are used for nothing but these prefetches, and an id outside
+// the pool is skipped.
+template <int D>
+__device__ void warm_l2(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p, const Ctx &c)
+{
+    const int lane = threadIdx.x & 31;
+    const Segment s = locate(p, c.cta_begin, c.cta_end);
+    const int P = p.page_size;
+    const int ring_pages = p.stages * kStageTokens / P;
+    const int pages = s.p1 - s.p0 < ring_pages ? s.p1 - s.p0 : ring_pages;
+    if (lane < pages) {
+        const int id = __ldcg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane);
+        if (id >= 0 && id < p.num_pages)
+            for (int rb = 0; rb < P; rb += p.box_rows) {
+                const int y = (id * p.hkv + s.g) * P + rb;
+                tma_prefetch_3d_row(tmK, y);
+                tma_prefetch_3d_row(tmV, y);
+            }
+    }
+}
+
 // FUSED: the units are fused per-decoder tails (DecodeParams::page_info).
 template <int D, bool FUSED>
 __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p,

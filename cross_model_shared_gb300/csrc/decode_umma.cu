@@ -392,6 +392,39 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
     }
 }
 
+// Run by the producer warps before they wait for the previous grid: prefetch
+// into L2 the page halves of this CTA's first ring-full of stages (up to 32
+// pages of its first segment; K from the K warp, V from the warp that will
+// copy it), so that the first copies after the wait hit L2 instead of waiting
+// on DRAM.  The block-table entries are read through L2 only and may be
+// stale (a preceding kernel may still be writing them): they are used for
+// nothing but these prefetches, and an id outside the pool is skipped.
+template <bool kIsK>
+__device__ void tc_warm_l2(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p, const TcCtx &c)
+{
+    const int lane = threadIdx.x & 31;
+    const bool split = p.split_producers != 0;
+    if (!kIsK && !split)
+        return;
+    const Segment s = locate(p, c.cta_begin, c.cta_end);
+    const int P = p.page_size;
+    const int ring_pages = c.stages * kTT / P;
+    const int pages = s.p1 - s.p0 < ring_pages ? s.p1 - s.p0 : ring_pages;
+    if (lane < pages) {
+        const int id = __ldcg(p.block_table + (int64_t)s.b * p.max_pages + s.p0 + lane);
+        if (id >= 0 && id < p.num_pages) {
+            const int y = (id * p.hkv + s.g) * P;
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h) {
+                if (kIsK)
+                    tma_prefetch_2d(tmK, h * 64, y);
+                if (!kIsK || !split)
+                    tma_prefetch_2d(tmV, h * 64, y);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // MMA issuers (one lane each)
 // ---------------------------------------------------------------------------
@@ -908,6 +941,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.tslot);
+    if (warp == kProducerWarp)
+        tc_warm_l2<true>(&tmK, &tmV, p, c);
+    else if (warp == kVProducerWarp)
+        tc_warm_l2<false>(&tmK, &tmV, p, c);
     pdl_wait_prior();                       // global memory only from here on
 
     if (warp == kProducerWarp)

@@ -295,6 +295,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// L2 prefetch of the box a tma_load_3d_row / tma_load_2d at the same
+// coordinates would copy (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d_row(const CUtensorMap *tm, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(0), "r"(y), "r"(0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
