@@ -21,6 +21,7 @@ struct PrefillParams {
     int32_t page_size, max_pages, num_pages, stages;
     float scale_log2;
     int32_t lens[SHKV_MAX_BATCH];    // host copy of the lengths (with the new tokens)
+    int32_t order[SHKV_MAX_BATCH];   // requests by length, longest first (CTA dispatch order)
 };
 
 }  // namespace shkv

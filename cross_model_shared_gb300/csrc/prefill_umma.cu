@@ -175,15 +175,18 @@ struct Tile {
     int nst_all;                 // stages loaded: the larger of the two
 };
 
+// CTAs are dispatched roughly in index order, so the index runs over the
+// longest work first (requests by length, then each request's tile pairs from
+// the last, which attends the most keys): the short pairs fill the last wave.
 __device__ __forceinline__ Tile pf_tile(const PrefillParams &p)
 {
     Tile t;
     const int pairs = (p.tiles + kPTilesPerCta - 1) / kPTilesPerCta;
     int idx = blockIdx.x;
-    const int tp = idx % pairs;
+    const int tp = pairs - 1 - idx % pairs;
     idx /= pairs;
     t.g = idx % p.hkv;
-    t.b = idx / p.hkv;
+    t.b = p.order[idx / p.hkv];
     t.L = p.lens[t.b];
     t.prefix = t.L - p.n_new;
 #pragma unroll

@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -601,7 +602,9 @@ shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new
         if (pool->lens[b] < n_new)
             return SHKV_ERR_INVALID_ARG;        // the new tokens must already be in the pool
         p.lens[b] = pool->lens[b];
+        p.order[b] = b;
     }
+    std::stable_sort(p.order, p.order + batch, [&](int32_t a, int32_t b) { return p.lens[a] > p.lens[b]; });
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.lse_out = lse_out;
