@@ -269,16 +269,35 @@ __device__ void pf_producer(const CUtensorMap *tm, const PrefillParams &p, const
 // MMA issuers
 // ---------------------------------------------------------------------------
 // S_X = Q_X K^T for each tile that attends stage k, into S buffer k & 1, which
-// is free once PV_X(k-2) has read the P written over it.
+// is free once PV_X(k-2) has read the P written over it.  One thread issues
+// every MMA of the CTA while two softmax warps share its SM sub-partition, so
+// the descriptors of a stage are ready before its waits end: the issue itself
+// is only the MMA instructions.
 __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
 {
     const uint32_t idesc = umma_idesc_bf16(128, kKT, false, false);
+    // A (Q tile x) and B (K of a slot): one base descriptor each; the others
+    // add (byte offset >> 4) to its 14-bit address field, which shared
+    // addresses below 256 KB never carry out of
+    uint64_t ad[kPTilesPerCta][kPHalves * 4];
+#pragma unroll
+    for (int x = 0; x < kPTilesPerCta; ++x)
+#pragma unroll
+        for (int i = 0; i < kPHalves * 4; ++i)
+            ad[x][i] = umma_sdesc_sw128(c.base + c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128) +
+                                            (uint32_t)((i >> 2) * 128 * 128 + (i & 3) * 32),
+                                        16u, 1024u);
+    const uint64_t kd0 = umma_sdesc_sw128(pf_slot(c, 0), 16u, 1024u);
     bool alive = true;
     for (int k = 0; k < t.nst_all; ++k) {
         const int slot = k % kPStages;
+        uint64_t bd[kPHalves * 4];
+#pragma unroll
+        for (int i = 0; i < kPHalves * 4; ++i)
+            bd[i] = kd0 + (((uint32_t)slot * c.lay.stage_bytes + (uint32_t)((i >> 2) * kKT * 128 + (i & 3) * 32)) >> 4);
         if (alive)
             alive = pf_wait(pf_full(c, false, slot), ring_par(k), c.abort_flag, p.err);
-#pragma unroll 1
+#pragma unroll
         for (int x = 0; x < kPTilesPerCta; ++x) {
             if (k >= t.nst[x])
                 continue;
@@ -286,17 +305,10 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
                 alive = pf_wait(pf_pvdone(c, x, k & 1), (uint32_t)(((k - 2) >> 1) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
-                const uint32_t qtile = c.base + c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
-                const uint32_t kst = pf_slot(c, slot);
+                const uint32_t d = tmem + col_s(x, k & 1);
 #pragma unroll
-                for (int h = 0; h < kPHalves; ++h)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad =
-                            umma_sdesc_sw128(qtile + (uint32_t)(h * 128 * 128 + kk * 32), 16u, 1024u);
-                        const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)(h * kKT * 128 + kk * 32), 16u, 1024u);
-                        umma_bf16(tmem + col_s(x, k & 1), ad, bd, idesc, (h | kk) ? 1u : 0u);
-                    }
+                for (int i = 0; i < kPHalves * 4; ++i)
+                    umma_bf16(d, ad[x][i], bd[i], idesc, i ? 1u : 0u);
             }
             umma_commit(pf_sfull(c, x, k & 1));
         }
@@ -312,12 +324,17 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
 __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uint32_t tmem)
 {
     const uint32_t idesc = umma_idesc_bf16(128, kPD, false, true);
+    const uint64_t vd0 = umma_sdesc_sw128(pf_slot(c, 0) + (uint32_t)(kKT * kPD * 2), (uint32_t)(kKT * 128), 1024u);
     bool alive = true;
     for (int k = 0; k < t.nst_all; ++k) {
         const int slot = k % kPStages;
+        uint64_t bd[kKT / 16];
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks)
+            bd[ks] = vd0 + (((uint32_t)slot * c.lay.stage_bytes + (uint32_t)ks * 2048u) >> 4);
         if (alive)
             alive = pf_wait(pf_full(c, true, slot), ring_par(k), c.abort_flag, p.err);
-#pragma unroll 1
+#pragma unroll
         for (int x = 0; x < kPTilesPerCta; ++x) {
             if (k >= t.nst[x])
                 continue;
@@ -325,13 +342,11 @@ __device__ void pf_pv(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
                 alive = pf_wait(pf_pfull(c, x, k & 1), (uint32_t)((k >> 1) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
-                const uint32_t vst = pf_slot(c, slot) + (uint32_t)(kKT * kPD * 2);
+                const uint32_t d = tmem + col_o(x);
+                const uint32_t a = tmem + col_s(x, k & 1);
 #pragma unroll
-                for (int ks = 0; ks < kKT / 16; ++ks) {
-                    const uint64_t bd = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kKT * 128), 1024u);
-                    umma_bf16_ts(tmem + col_o(x), tmem + col_s(x, k & 1) + (uint32_t)(ks * 8), bd, idesc,
-                                 (k == 0 && ks == 0) ? 0u : 1u);
-                }
+                for (int ks = 0; ks < kKT / 16; ++ks)
+                    umma_bf16_ts(d, a + (uint32_t)(ks * 8), bd[ks], idesc, (k == 0 && ks == 0) ? 0u : 1u);
             }
             umma_commit(pf_pvdone(c, x, k & 1));
         }
