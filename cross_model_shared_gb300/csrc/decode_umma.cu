@@ -428,13 +428,23 @@ __device__ void tc_warm_l2(const CUtensorMap *tmK, const CUtensorMap *tmV, const
 // ---------------------------------------------------------------------------
 // MMA issuers (one lane each)
 // ---------------------------------------------------------------------------
+// The descriptors of a stage are built before its waits end, so that once
+// the data is there the issue is only the MMA instructions (the issuing
+// thread shares its SM sub-partition with two softmax warps).  Each operand
+// has one base descriptor; the others add (byte offset >> 4) to its 14-bit
+// address field, which shared addresses below 256 KB never carry out of.
 template <int NR>
 __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_qk = umma_idesc_bf16(128, NR, false, false);
-    const uint32_t qtile = c.base + c.lay.qtile;
+    uint64_t bq[kHalves * 4];                 // the Q tile (B), K-major
+#pragma unroll
+    for (int i = 0; i < kHalves * 4; ++i)
+        bq[i] = umma_sdesc_sw128(c.base + c.lay.qtile + (uint32_t)(i >> 2) * c.lay.qhalf + (uint32_t)((i & 3) * 32),
+                                 16u, 1024u);
+    const uint64_t kd0 = umma_sdesc_sw128(slot_addr(c, 0), 16u, 1024u);
     bool alive = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (alive)
@@ -451,21 +461,18 @@ __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             const int k = kbase + j;
             const int buf = k & 1;
             const int slot = k % stages;
+            uint64_t ak[kHalves * 4];         // this stage's K tile (A), K-major
+#pragma unroll
+            for (int i = 0; i < kHalves * 4; ++i)
+                ak[i] = kd0 + (((uint32_t)slot * c.lay.stage_bytes + (uint32_t)((i >> 2) * kTT * 128 + (i & 3) * 32)) >> 4);
             wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
             wait(s_free_b(c, buf), (uint32_t)(((k >> 1) & 1) ^ 1));
             if (alive) {
                 tc_fence_after();
-                const uint32_t kst = slot_addr(c, slot);
+                const uint32_t d = tmem + kColS + (uint32_t)(buf * 64);
 #pragma unroll
-                for (int h = 0; h < kHalves; ++h)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad =
-                            umma_sdesc_sw128(kst + (uint32_t)(h * kTT * 128 + kk * 32), 16u, 1024u);
-                        const uint64_t bd =
-                            umma_sdesc_sw128(qtile + (uint32_t)h * c.lay.qhalf + (uint32_t)(kk * 32), 16u, 1024u);
-                        umma_bf16(tmem + kColS + (uint32_t)(buf * 64), ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
-                    }
+                for (int i = 0; i < kHalves * 4; ++i)
+                    umma_bf16(d, ak[i], bq[i], idesc_qk, i ? 1u : 0u);
             }
             umma_commit(s_full_b(c, buf));
             if (j == nst - 1)
@@ -490,6 +497,9 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
+    // V^T (A) and P^T (B, over the K tile's first half), both MN-major
+    const uint64_t vd0 = umma_sdesc_sw128(slot_addr(c, 0) + (uint32_t)(kTT * kD * 2), (uint32_t)(kTT * 128), 1024u);
+    const uint64_t pd0 = umma_sdesc_sw128(slot_addr(c, 0), (uint32_t)(kTT * 128), 1024u);
     bool alive = true;
     int kbase = 0;
     Segment s = locate(p, c.cta_begin, c.cta_end);
@@ -498,20 +508,22 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int slot = k % stages;
+            uint64_t av[kTT / 16], bp[kTT / 16];
+#pragma unroll
+            for (int ks = 0; ks < kTT / 16; ++ks) {
+                const uint32_t off = ((uint32_t)slot * c.lay.stage_bytes + (uint32_t)ks * 2048u) >> 4;
+                av[ks] = vd0 + off;
+                bp[ks] = pd0 + off;
+            }
             if (alive)
                 alive = mbar_wait_bounded(p_full_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
             if (alive)
                 alive = mbar_wait_bounded(full_v_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
             if (alive) {
                 tc_fence_after();
-                const uint32_t kst = slot_addr(c, slot);
-                const uint32_t vst = kst + (uint32_t)(kTT * kD * 2);
 #pragma unroll
-                for (int ks = 0; ks < kTT / 16; ++ks) {
-                    const uint64_t ad = umma_sdesc_sw128(vst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                    const uint64_t bd = umma_sdesc_sw128(kst + (uint32_t)ks * 2048u, (uint32_t)(kTT * 128), 1024u);
-                    umma_bf16(tmem + kColO, ad, bd, idesc_pv, (j == 0 && ks == 0) ? 0u : 1u);
-                }
+                for (int ks = 0; ks < kTT / 16; ++ks)
+                    umma_bf16(tmem + kColO, av[ks], bp[ks], idesc_pv, (j == 0 && ks == 0) ? 0u : 1u);
             }
             umma_commit(empty_b(c, slot));
         }
