@@ -592,11 +592,48 @@ def run_gpu_prefill(args):
         raise RuntimeError("device error bits in the timed region")
     ms = ev0.elapsed_time(ev1) / args.steps
     prefix = wl.lens_final.astype(np.int64) - T
-    keys = int(sum(int(pf) * T + T * (T + 1) // 2 for pf in prefix))      # sum over new tokens of keys attended
-    flops = 4.0 * keys * wl.Hq * wl.D                                        # QK and PV, 2 flops per MAC
+    keys_b = prefix * T + T * (T + 1) // 2                                   # per request: keys attended, summed
+    flops_b = 4.0 * keys_b * wl.Hq * wl.D                                    # QK and PV, 2 flops per MAC
+    flops = float(flops_b.sum())
     kv_bytes = W.unique_kv_bytes(wl)
     tflops = flops / (ms * 1e-3) / 1e12
     peak, kind = measured_tensor_peak()
+
+    # end to end through the C ABI: pinned host q in, host out back, per step
+    e_steps = max(10, min(args.steps, 200))
+    pipe = E2EPipeline(q, lambda qd, od: pool.prefill_attention(qd, scale=wl.scale, out=od, lse=lse))
+    for _ in range(3):
+        pipe.step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        pipe.step()
+    torch.cuda.synchronize()
+    e2e_value = flops * e_steps / (time.perf_counter() - t0) / 1e12
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        order = np.argsort(wl.lens_final, kind="stable")
+        q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+        fl, elapsed, done = 0.0, 0.0, []
+        i = 0
+        while elapsed < args.cpu_budget_s and i < wl.B:
+            b = int(order[(len(order) // 2 + i) % len(order)])
+            npg = int((wl.lens_final[b] + wl.P - 1) // wl.P)
+            idt = torch.from_numpy(wl.block_table[b, :npg].astype(np.int64)).to(dev)
+            kb = k_dev.index_select(0, idt).view(torch.int16).cpu().numpy().view(np.uint16)
+            vb = v_dev.index_select(0, idt).view(torch.int16).cpu().numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            oracle.prefill_attention(q_bits[b:b + 1], kb, vb, np.arange(npg, dtype=np.int32)[None, :],
+                                     np.array([wl.lens_final[b]], np.int32), scale=wl.scale)
+            elapsed += time.perf_counter() - t0
+            fl += float(flops_b[b])
+            done.append(b)
+            i += 1
+        cpu = {"value": fl / elapsed / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{len(done)} whole requests of {wl.name} ({T} new tokens each), fp64, "
+                         f"{oracle.num_threads()} threads", "seconds": round(elapsed, 2)}
     line = {
         "metric": "partial-prefill attention: TFLOP/s (% of bf16 tensor peak)", "value": tflops, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -607,8 +644,12 @@ def run_gpu_prefill(args):
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": kind, "traffic": None, "kernel": "shkv_prefill_umma_kernel",
                      "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": q.numel() * 2, "steps": e_steps,
+                "copies": "own streams, two buffers: overlap the neighbouring steps' kernels"},
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
 
