@@ -392,33 +392,37 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                     }
                 }
             }
-        // element (mt, nt, e) is register reg = (mt*NT + nt)*4 + e; warp wtid
-        // of the group takes the registers with reg % wt == wtid
-        int wsel = 0;
+        // element (mt, nt, e) is register reg = (mt*NT + nt)*4 + e of the row
+        // group's O; warp wtid of the group takes the registers with
+        // reg % wt == wtid.  A loop over just those, unrolled, so the shared
+        // memory loads of several elements are in flight together (this runs
+        // once per segment on one warp per SM sub-partition: latency-bound).
+#pragma unroll 8
+        for (int reg = wtid; reg < NREG; reg += p.wt) {
+            const int e = reg & 3, i = e & 1;
+            const int nt = NT > 1 ? (reg >> 2) % NT : 0;
+            const int mt = (reg >> 2) / NT;
+            float acc = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < KSTEPS; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int reg = (mt * NT + nt) * 4 + e;
-                    const int r = row0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-                    if (wsel == wtid && r < p.rows) {
-                        const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int w = 0; w < kWtMax; ++w)
-                            if (w < p.wt)
-                                acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * fac[nt][e & 1][w];
-                        if (!whole)
-                            p.ws_part[orow_r[nt][e & 1] * D + d] = acc;
-                        else if (p.out_f32)
-                            p.out_f32[orow_r[nt][e & 1] * D + d] = acc;
-                        else
-                            p.out[orow_r[nt][e & 1] * D + d] = __float2bfloat16_rn(acc);
-                    }
-                    wsel = (wsel + 1 == p.wt) ? 0 : wsel + 1;
+            for (int w = 0; w < kWtMax; ++w)
+                if (w < p.wt) {
+                    const float f = (NT > 1 && nt) ? (i ? fac[NT - 1][1][w] : fac[NT - 1][0][w])
+                                                   : (i ? fac[0][1][w] : fac[0][0][w]);
+                    acc += comb_o[((size_t)(w_first + w) * NREG + reg) * 32 + lane] * f;
                 }
+            const int r = row0 + nt * 8 + 2 * (lane & 3) + i;
+            if (r < p.rows) {
+                const int64_t orow = (NT > 1 && nt) ? (i ? orow_r[NT - 1][1] : orow_r[NT - 1][0])
+                                                    : (i ? orow_r[0][1] : orow_r[0][0]);
+                const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
+                if (!whole)
+                    p.ws_part[orow * D + d] = acc;
+                else if (p.out_f32)
+                    p.out_f32[orow * D + d] = acc;
+                else
+                    p.out[orow * D + d] = __float2bfloat16_rn(acc);
+            }
+        }
         named_barrier(1, (uint32_t)ncw * 32u);
 
         // --- split unit: the last piece to arrive merges all pieces
