@@ -87,6 +87,17 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
     const int v_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // V: token within a 16-token tile
     const int v_col = ((lane >> 3) & 1) * 8;                  // V: column offset within 16
 
+    // output row of this lane's rows (nt, i) without the KV head's term g*G:
+    // fixed for the whole launch
+    int qoff[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = row0 + nt * 8 + 2 * (lane & 3) + i;
+            qoff[nt][i] = q_row(p, 0, r < p.rows ? r : 0);
+        }
+
     bool alive = true;
     int kbase = 0, seg = 0;
     Segment s = locate(p, c.cta_begin, c.cta_end);
@@ -356,23 +367,32 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
         const int w_first = rg * p.wt;
         float fac[NT][2][kWtMax];
         int64_t orow_r[NT][2];
+        const int64_t rbase = whole ? (int64_t)s.b * p.n_models * p.hq + (int64_t)s.g * p.group
+                                    : (int64_t)slot_id * p.rows;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int rl = nt * 8 + 2 * (lane & 3) + i;
+                // every warp's (m, l) of this row first, so the loads issue together
+                float mw[kWtMax], lw[kWtMax];
+#pragma unroll
+                for (int w = 0; w < kWtMax; ++w) {
+                    mw[w] = w < p.wt ? comb_m[(w_first + w) * ROWS_W + rl] : -INFINITY;
+                    lw[w] = w < p.wt ? comb_l[(w_first + w) * ROWS_W + rl] : 0.f;
+                }
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kWtMax; ++w)
                     if (w < p.wt)
-                        M = fmaxf(M, comb_m[(w_first + w) * ROWS_W + rl]);
+                        M = fmaxf(M, mw[w]);
                 float lsum = 0.f;
 #pragma unroll
                 for (int w = 0; w < kWtMax; ++w) {
                     fac[nt][i][w] = 0.f;
                     if (w < p.wt && M != -INFINITY) {
-                        fac[nt][i][w] = ex2_approx(comb_m[(w_first + w) * ROWS_W + rl] - M);
-                        lsum += comb_l[(w_first + w) * ROWS_W + rl] * fac[nt][i][w];
+                        fac[nt][i][w] = ex2_approx(mw[w] - M);
+                        lsum += lw[w] * fac[nt][i][w];
                     }
                 }
                 const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
@@ -380,8 +400,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 for (int w = 0; w < kWtMax; ++w)
                     fac[nt][i][w] *= inv;
                 const int r = row0 + rl;
-                orow_r[nt][i] = whole ? (int64_t)s.b * p.n_models * p.hq + q_row(p, s.g, r < p.rows ? r : 0)
-                                      : (int64_t)slot_id * p.rows + r;
+                orow_r[nt][i] = rbase + (whole ? (int64_t)qoff[nt][i] : (int64_t)r);
                 if (wtid == 0 && (lane >> 2) == 0 && r < p.rows) {     // one writer per row
                     const float lse = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
                     if (whole) {
