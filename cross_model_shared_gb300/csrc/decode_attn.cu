@@ -330,6 +330,13 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 mbar_arrive(empty_bar(c, slot, stages));
         }
 
+        // A split piece's unit count, read now so that its latency hides behind
+        // the epilogue: when every other piece has arrived already, this one
+        // merges without arriving (see below).
+        uint32_t pre_count = 0xffffffffu;
+        if (threadIdx.x == 0 && !(s.seg_begin == s.unit_begin && s.seg_end == s.unit_end))
+            pre_count = ld_acquire_gpu(p.ws_count + (int64_t)s.b * p.hkv + s.g);
+
         // --- merge the row group's warps: publish (m, l, O) ...
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -450,9 +457,15 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
             const int c1 = cta_of(p, s.unit_end - 1);
             uint32_t *counter = p.ws_count + (int64_t)s.b * p.hkv + s.g;
             if (threadIdx.x == 0) {
-                __threadfence();     // this CTA's partial (ordered by the barrier above) before the count
-                const uint32_t prev = atomicAdd(counter, 1u);
-                *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
+                if (pre_count == (uint32_t)(c1 - c0)) {
+                    // every other piece had arrived (acquire read above): this is
+                    // the last one, so it merges without arriving
+                    *c.bcast = 1u;
+                } else {
+                    __threadfence();     // this CTA's partial (ordered by the barrier above) before the count
+                    const uint32_t prev = atomicAdd(counter, 1u);
+                    *c.bcast = (prev == (uint32_t)(c1 - c0)) ? 1u : 0u;
+                }
             }
             named_barrier(1, (uint32_t)ncw * 32u);
             if (*c.bcast) {
