@@ -49,6 +49,18 @@ def test_reduced_shapes_match_oracle(shape):
     run_full(wl, W.gen_q(wl), *W.gen_pool(wl))
 
 
+@pytest.mark.parametrize("shape", ["llama8b", "qwen8b"])
+def test_max_batch_matches_oracle(shape):
+    """The largest batch one call takes (SHKV_MAX_BATCH = 1024 requests) with
+    ragged short lengths: every entry of the plan's per-request tables is used
+    and each CTA crosses many (request, head) units.  llama8b heads run the
+    mma.sync consumer, qwen8b heads the tcgen05 one."""
+    rng = np.random.default_rng(23)
+    lens = rng.integers(1, 97, size=1024).tolist()
+    wl = W.custom_workload(f"maxbatch_{shape}", B=len(lens), lens_prefill=lens, seed=29, **SHAPES[shape])
+    run_full(wl, W.gen_q(wl), *W.gen_pool(wl))
+
+
 def test_single_long_request_is_split_and_merged():
     """One request, one KV head: the whole grid works on it, so it is cut
     into many pieces that the last arriving CTA merges."""
