@@ -123,7 +123,7 @@ struct PfSmem {
 // ring slots of [K | V][half][64 keys][128 B], then the two Q tiles
 // [tile][half][128 rows][128 B] (all 128-byte swizzled), then the barriers:
 // full_k[S], full_v[S], empty_k[S], empty_v[S], s_full[tile][buf], p_full[tile][buf],
-// pv_done[tile][buf], fin.  Everything a tile's softmax hands to the MMA
+// pv_done[tile][buf], fin, q_ready.  Everything a tile's softmax hands to the MMA
 // issuers is per S buffer: a softmax group may finish stage k+1 before the
 // PV issuer has waited for stage k, but not stage k+2 (its scores need PV(k)).
 __host__ __device__ inline PfSmem pf_layout()
@@ -133,7 +133,7 @@ __host__ __device__ inline PfSmem pf_layout()
     u.ring = 0;
     u.qtile = (uint32_t)kPStages * u.stage_bytes;
     u.bars = u.qtile + (uint32_t)(kPTilesPerCta * kPHalves * 128 * 128);
-    u.meta = u.bars + (uint32_t)((4 * kPStages + 13) * 8);
+    u.meta = u.bars + (uint32_t)((4 * kPStages + 14) * 8);
     u.misc = u.meta + (uint32_t)(kPStages * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;
@@ -160,6 +160,8 @@ __device__ __forceinline__ uint32_t pf_pvdone(const PfCtx &c, int x, int b)
     return pbar(c, 4 * kPStages + 8 + 2 * x + b);
 }
 __device__ __forceinline__ uint32_t pf_fin(const PfCtx &c) { return pbar(c, 4 * kPStages + 12); }
+// both query tiles are in shared memory (one arrival per softmax warp)
+__device__ __forceinline__ uint32_t pf_qready(const PfCtx &c) { return pbar(c, 4 * kPStages + 13); }
 __device__ __forceinline__ uint32_t pf_slot(const PfCtx &c, int s)
 {
     return c.base + c.lay.ring + (uint32_t)s * c.lay.stage_bytes;
@@ -288,7 +290,7 @@ __device__ void pf_qk(const PrefillParams &p, const PfCtx &c, const Tile &t, uin
                                             (uint32_t)((i >> 2) * 128 * 128 + (i & 3) * 32),
                                         16u, 1024u);
     const uint64_t kd0 = umma_sdesc_sw128(pf_slot(c, 0), 16u, 1024u);
-    bool alive = true;
+    bool alive = pf_wait(pf_qready(c), 0u, c.abort_flag, p.err);
     for (int k = 0; k < t.nst_all; ++k) {
         const int slot = k % kPStages;
         uint64_t bd[kPHalves * 4];
@@ -591,26 +593,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
         }
         mbar_init(pf_fin(c), 2);
+        mbar_init(pf_qready(c), kPTilesPerCta * kPGroupWarps);
         *c.abort_flag = 0u;
         fence_barrier_init();
-    }
-    if (warp < kPTilesPerCta * kPGroupWarps) {
-        // this thread's query row into its tile's swizzled K-major Q tile (padding rows zero)
-        const int x = warp / kPGroupWarps;
-        const int r = threadIdx.x - x * 128;
-        const int ti = r / p.group, tj = r - (r / p.group) * p.group;
-        const bool row_ok = ti < t.ntok[x];
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            p.q + (((int64_t)t.b * p.n_new + t.i0[x] + ti) * p.hq + (int64_t)t.g * p.group + tj) * kPD);
-        const uint32_t qtile = c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
-#pragma unroll
-        for (int ch = 0; ch < kPD / 8; ++ch) {
-            const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t off = (uint32_t)(ch >> 3) * (128u * 128u) + (uint32_t)r * 128u +
-                                 (uint32_t)(((ch & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4 *>(c.smem + qtile + off) = v;
-        }
-        fence_proxy_async_smem();
     }
     if (warp == 0)
         tmem_alloc(c.base + c.lay.tslot, kPTmemCols);
@@ -630,7 +615,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if ((threadIdx.x & 31) == 0)
             pf_pv(p, c, t, tmem);
     } else {
+        // this thread's query row into its tile's swizzled K-major Q tile
+        // (padding rows zero), after the CTA barrier so that the producers'
+        // first copies are already on their way
         const int x = warp / kPGroupWarps;
+        {
+            const int r = threadIdx.x - x * 128;
+            const int ti = r / p.group, tj = r - (r / p.group) * p.group;
+            const bool row_ok = ti < t.ntok[x];
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + (((int64_t)t.b * p.n_new + t.i0[x] + ti) * p.hq + (int64_t)t.g * p.group + tj) * kPD);
+            const uint32_t qtile = c.lay.qtile + (uint32_t)(x * kPHalves * 128 * 128);
+#pragma unroll
+            for (int ch = 0; ch < kPD / 8; ++ch) {
+                const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t off = (uint32_t)(ch >> 3) * (128u * 128u) + (uint32_t)r * 128u +
+                                     (uint32_t)(((ch & 7) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(c.smem + qtile + off) = v;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0)
+                mbar_arrive(pf_qready(c));
+        }
         float m_use, lsum;
         bool alive;
         pf_softmax(p, c, t, tmem, x, m_use, lsum, alive);
