@@ -16,7 +16,13 @@
 //   range as a sequence of segments (one segment per (b, g) it touches).  A
 //   (b, g) that straddles a cut is split: each piece writes a normalised
 //   partial and its log-sum-exp, and the last piece to finish (an atomic
-//   arrival counter, no waiting) merges them.  No CTA ever waits for another.
+//   arrival counter, no waiting) merges them; a piece that reads, early in
+//   its epilogue, that every other piece has arrived merges without
+//   arriving.  No CTA ever waits for another.
+//
+// Launches are chained by programmatic dependent launch; before waiting for
+// the previous launch the producer prefetches its first ring-full of pages
+// into L2 (prefetches only: nothing read before the wait is used after it).
 //
 // Inside a CTA:
 //   * one producer warp streams K and V into an mbarrier ring of
@@ -33,7 +39,8 @@
 //     an MMA exactly; an online softmax in base 2 follows; P^T is transposed in
 //     registers (movmatrix) and O^T += V^T P^T accumulates in fp32;
 //   * at the end of a segment the warps of a row group merge their
-//     (max, sum, O) states through shared memory.
+//     (max, sum, O) states through shared memory; each warp then combines
+//     and writes its own share of the accumulator registers.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
