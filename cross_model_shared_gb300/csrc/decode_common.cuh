@@ -270,7 +270,7 @@ __device__ void producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const D
                 rb1_info = __shfl_sync(0xffffffffu, my_info, (lane + 2) & 31);   // row-block 1, seen by lane 4*sub
             }
             bool ok = true;
-            if (alive && in_iter && (lane & 3) == 0)
+            if (alive && in_iter)           // the 4 lanes of each stage poll its slot together
                 ok = mbar_wait_bounded(empty_bar(c, slot, stages), ((k / stages) & 1) ^ 1, c.abort_flag, p.err);
             alive = alive && __all_sync(0xffffffffu, ok);
             const bool my_valid = in_iter && my_rb < RB && my_tok < tok_end && my_id >= 0 && my_id < p.num_pages;
