@@ -60,6 +60,8 @@ SEGMENT_COST = 16  # chunks charged per (request, head) segment by the planner
     (list(range(1, 300)), 32, 8, 152),
     ([5], 16, 1, 152),                         # fewer chunks than CTAs
     ([512] * 40 + [32768] * 3, 16, 8, 152),    # many short requests next to long ones
+    ([1 + (37 * i) % 96 for i in range(1024)], 16, 8, 152),   # the largest batch, ragged
+    ([1] * 1024, 32, 2, 152),                  # the largest batch, one token each
 ])
 def test_plan_covers_every_chunk_with_balanced_cost(lib, lens, P, H, C):
     begin, nc, ns = N.shkv_plan_decode(lens, P, H, C)
