@@ -9,7 +9,7 @@ import torch
 import oracle
 from cross_model_shared_gb300 import _native as N
 from cross_model_shared_gb300 import workloads as W
-from tests.gpu_common import bits_to_torch, compare, make_pool, oracle_for_requests, torch_to_bits
+from tests.gpu_common import bits_to_torch, compare, make_pool, torch_to_bits
 
 pytestmark = pytest.mark.gpu
 

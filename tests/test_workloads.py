@@ -1,5 +1,4 @@
 """Seeded synthetic inputs: determinism, shapes and the length mixes."""
-import math
 
 import numpy as np
 import pytest

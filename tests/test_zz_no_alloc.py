@@ -9,7 +9,6 @@ failure has already run every other test.  It must pass both alone in a
 fresh process and after the rest of the suite (the static scratch keeps the
 previous call's contents; each call clears what must start at zero).
 """
-import numpy as np
 import pytest
 import torch
 
