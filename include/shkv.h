@@ -184,9 +184,10 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
  *            module's query heads; head h uses KV head h / (Hq / Hkv))
  *   out      device bf16, same shape;  lse_out device fp32 [batch, n_new,
  *            hq_per_model] (natural log) or NULL
- * Tensor-core kernel (tcgen05): one CTA per (request, KV head, tile of
- * floor(128 / G) new tokens), the G query heads of a KV head stacked with
- * the tokens on the MMA M dimension.
+ * Tensor-core kernel (tcgen05): a tile is floor(128 / G) new tokens x the G
+ * query heads of one KV head, stacked on the MMA M dimension; one CTA takes
+ * two consecutive tiles of a (request, KV head) and streams its pages once
+ * for both, the CTAs ordered longest first.
  * Supported: head_dim 128, page size 16 or 32, G <= 128, batch <=
  * SHKV_MAX_BATCH.  Errors: SHKV_ERR_INVALID_ARG (null / misaligned pointers,
  * a request shorter than n_new), SHKV_ERR_UNSUPPORTED, SHKV_ERR_CUDA; page
