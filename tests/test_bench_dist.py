@@ -52,3 +52,27 @@ def test_single_rank_is_identity_and_throughput_counts_every_rank():
     one = bench.job_throughput_gbs(10**9, 10, 1, 2.0)
     assert one == pytest.approx(5.0)
     assert bench.job_throughput_gbs(10**9, 10, 4, 2.0) == pytest.approx(4 * one)   # weak scaling
+
+
+def test_reference_arm_prints_one_contract_line():
+    """The reference arm (the fp64 oracle on the host cores) needs no GPU: one
+    JSON line with the main line's metric and unit, `impl: reference`, and the
+    cpu_baseline and e2e objects that describe it."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
