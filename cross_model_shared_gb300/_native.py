@@ -36,9 +36,11 @@ EXPORTS = [
     "shkv_tails_get_lens", "shkv_tails_append", "shkv_decode_tails_workspace_size",
     "shkv_decode_attention_tails", "shkv_pages_create", "shkv_pages_destroy", "shkv_pages_acquire",
     "shkv_pages_publish", "shkv_pages_release", "shkv_pages_alloc_transfer", "shkv_pages_stats",
-    "shkv_pages_refcount", "shkv_prefill_attention",
+    "shkv_pages_refcount", "shkv_prefill_attention", "shkv_pool_set_decode_consumer",
+    "shkv_partition_requests",
 ]
 
+SHKV_CONSUMER_AUTO = -1
 SHKV_CONSUMER_MMA_SYNC = 0
 SHKV_CONSUMER_TCGEN05 = 1
 
@@ -118,6 +120,8 @@ def load() -> ctypes.CDLL:
         "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
         "shkv_decode_consumer": [vp, i32, i32, ctypes.POINTER(i32)],
+        "shkv_pool_set_decode_consumer": [vp, i32],
+        "shkv_partition_requests": [i32, i32p, i32, i32, i32p, vp],
         "shkv_tails_create": [vp, ctypes.POINTER(shkv_tails_config), ctypes.POINTER(vp)],
         "shkv_tails_destroy": [vp],
         "shkv_tails_set_lens": [vp, i32, i32p, vp],
@@ -225,9 +229,25 @@ def shkv_decode_attention_noalloc(pool: int, batch: int, n_models: int, hq: int,
            "shkv_decode_attention_noalloc")
 
 
+def shkv_partition_requests(lens, page_size: int, world_size: int):
+    """Host-only division of a batch among replicas: (owner int32 [batch],
+    pages per replica int64 [world_size])."""
+    import numpy as np
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    owner = np.zeros(len(lens), dtype=np.int32)
+    rank_pages = np.zeros(world_size, dtype=np.int64)
+    _check(load().shkv_partition_requests(len(lens), lens.ctypes.data, page_size, world_size, owner.ctypes.data,
+                                          rank_pages.ctypes.data), "shkv_partition_requests")
+    return owner, rank_pages
+
+
+def shkv_pool_set_decode_consumer(pool: int, consumer: int) -> None:
+    _check(load().shkv_pool_set_decode_consumer(pool, consumer), "shkv_pool_set_decode_consumer")
+
+
 def shkv_decode_consumer(pool: int, n_models: int, hq: int) -> int:
     """SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05: the consumer a decode
-    call with this shape would run now."""
+    call with this shape would run on this pool."""
     out = ctypes.c_int32()
     _check(load().shkv_decode_consumer(pool, n_models, hq, ctypes.byref(out)), "shkv_decode_consumer")
     return out.value

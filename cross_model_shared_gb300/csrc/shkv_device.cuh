@@ -75,8 +75,8 @@ constexpr int kMaxThreadsNT2 =
 constexpr int kWtMax = cmax(cmax(cmax(SHKV_WT_NT1, kNt1MultiWarps / 2), SHKV_WT_NRG1),
                             cmax(cmax(SHKV_WT_NRG2, SHKV_WT_NRG3), SHKV_WT_NRG4));
 // Stacked rows per KV head from which the automatic policy picks the tcgen05
-// consumer (up to 64 rows); below it the mma.sync consumer runs.  The
-// environment variable SHKV_DECODE_CONSUMER=mma|umma overrides the policy.
+// consumer (up to 64 rows); below it the mma.sync consumer runs.  A pool
+// can name one consumer instead (shkv_pool_set_decode_consumer).
 #ifndef SHKV_UMMA_MIN_ROWS
 #define SHKV_UMMA_MIN_ROWS 16
 #endif

@@ -47,6 +47,7 @@ struct shkv_pool {
     CUtensorMap tm_v2;
     std::vector<int32_t> lens;   // host copy of seq_lens
     bool tails_view = false;     // a per-decoder tail table over another pool's pages: empty lengths allowed
+    int32_t consumer = SHKV_CONSUMER_AUTO;   // decode consumer the caller asked for
 };
 
 // Per-decoder unique tails: a view pool over the parent's pages whose
@@ -253,17 +254,17 @@ DecodeShape decode_shape(int rows)
     return s;
 }
 
-// Which consumer runs for R stacked rows of head dim D: the automatic
-// policy, or the one named by SHKV_DECODE_CONSUMER ("mma" or "umma"; read on
-// every call).  The tcgen05 consumer covers D = 128 and R <= 64 only.
-bool use_umma_consumer(int rows, int head_dim)
+// Which consumer runs for R stacked rows of head dim D: the one the pool
+// names (shkv_pool_set_decode_consumer), else the automatic policy.  The
+// tcgen05 consumer covers D = 128 and R <= 64 only; outside that the
+// mma.sync consumer runs whatever the pool names.
+bool use_umma_consumer(int rows, int head_dim, int32_t choice)
 {
     if (head_dim != 128 || rows > kUmmaMaxRows || umma_stages(rows) == 0)
         return false;
-    const char *env = getenv("SHKV_DECODE_CONSUMER");
-    if (env && strcmp(env, "umma") == 0)
+    if (choice == SHKV_CONSUMER_TCGEN05)
         return true;
-    if (env && strcmp(env, "mma") == 0)
+    if (choice == SHKV_CONSUMER_MMA_SYNC)
         return false;
     return rows >= kUmmaMinRows;
 }
@@ -446,10 +447,14 @@ struct FusedUnits {
 // One decode launch: final rows to out (bf16) or, when out_f32 is set, to
 // out_f32 (fp32; lse_out then required).  Launches nothing when the pool has
 // no chunks (every length zero, possible only for a tail view).  With fu,
-// request b's unit is fu's row b instead of the pool's block table.
+// request b's unit is fu's row b instead of the pool's block table.  With
+// clear_counters, once every check has passed, the workspace's arrival
+// counters are zeroed on the stream before the launch (for a workspace whose
+// previous contents are unknown).
 shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
                         float scale, void *out, float *out_f32, float *lse_out, void *workspace,
-                        size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr)
+                        size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr,
+                        bool clear_counters = false)
 {
     if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
         hq_per_model < 1)
@@ -481,7 +486,7 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     if (p.total_chunks == 0)
         return SHKV_OK;
 
-    const bool use_umma = use_umma_consumer(rows, c.head_dim);
+    const bool use_umma = use_umma_consumer(rows, c.head_dim, pool->consumer);
     const DecodeShape sh = decode_shape(rows);
     const int ncw = sh.nrg * sh.wt;
     const int nreg = (c.head_dim / 16) * sh.nt * 4;
@@ -541,6 +546,8 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     // tcgen05 consumer: 16-token pages make 32 copies a stage, issued by two
     // warps; the 16 copies of 32-token pages measured faster from one warp
     p.split_producers = c.page_size < 32 ? 1 : 0;
+    if (clear_counters && cudaMemsetAsync(p.ws_count, 0, count_bytes, (cudaStream_t)stream) != cudaSuccess)
+        return SHKV_ERR_CUDA;
     cudaError_t e = use_umma ? launch_decode_umma(pool->tm_k2, pool->tm_v2, p, smem_bytes, (cudaStream_t)stream)
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);
@@ -775,7 +782,17 @@ shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_
     const int rows = n_models * (hq_per_model / pool->cfg.num_kv_heads);
     if (rows > 64)
         return SHKV_ERR_UNSUPPORTED;
-    *consumer = use_umma_consumer(rows, pool->cfg.head_dim) ? SHKV_CONSUMER_TCGEN05 : SHKV_CONSUMER_MMA_SYNC;
+    *consumer = use_umma_consumer(rows, pool->cfg.head_dim, pool->consumer) ? SHKV_CONSUMER_TCGEN05
+                                                                            : SHKV_CONSUMER_MMA_SYNC;
+    return SHKV_OK;
+}
+
+shkv_status shkv_pool_set_decode_consumer(shkv_pool *pool, int32_t consumer)
+{
+    if (!pool || (consumer != SHKV_CONSUMER_AUTO && consumer != SHKV_CONSUMER_MMA_SYNC &&
+                  consumer != SHKV_CONSUMER_TCGEN05))
+        return SHKV_ERR_INVALID_ARG;
+    pool->consumer = consumer;
     return SHKV_OK;
 }
 
@@ -852,25 +869,76 @@ static __device__ __align__(256) unsigned char shkv_noalloc_scratch[SHKV_NOALLOC
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices];
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of shkv_noalloc_scratch on the current device, looked up
-// once per device and cached.  (In host code the array's name is only a
-// host-side stand-in, never a device address.)
-shkv_status noalloc_scratch(int device, void **ptr)
+// Driver entry points reached through the runtime, so the library needs no
+// libcuda at load time (as for the tensor-map encoder).
+template <typename Fn>
+Fn driver_fn(const char *name, int version)
 {
-    if (device < 0 || device >= kMaxDevices)
-        return SHKV_ERR_UNSUPPORTED;
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(ptr);
+}
+
+// Unique ID (within the process) of the context current on this thread, or
+// 0 when none is current.  IDs are never reused, unlike context handles: a
+// context made after cudaDeviceReset gets a new one.
+shkv_status current_context_id(unsigned long long *id)
+{
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    if (!get_current || !get_id)
+        return SHKV_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS)
+        return SHKV_ERR_CUDA;
+    *id = 0;
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS)
+        return SHKV_ERR_CUDA;
+    return SHKV_OK;
+}
+
+struct ScratchAddress {
+    unsigned long long context_id;
+    void *ptr;
+};
+std::mutex g_noalloc_mutex;
+std::vector<ScratchAddress> g_noalloc_addresses;
+
+// Device address of shkv_noalloc_scratch in the current context, looked up
+// with cudaGetSymbolAddress the first time a context asks and cached by the
+// context's unique ID.  (In host code the array's name is only a host-side
+// stand-in, never a device address.)  A module loaded again in a new
+// context -- after cudaDeviceReset, or in a context the caller made -- has
+// its own scratch and its own entry.
+shkv_status noalloc_scratch(void **ptr)
+{
+    unsigned long long id = 0;
+    shkv_status st = current_context_id(&id);
+    if (st != SHKV_OK)
+        return st;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[device]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, shkv_noalloc_scratch) != cudaSuccess || !p)
-            return SHKV_ERR_CUDA;
-        g_noalloc_ptr[device] = p;
+    if (id != 0)
+        for (const ScratchAddress &a : g_noalloc_addresses)
+            if (a.context_id == id) {
+                *ptr = a.ptr;
+                return SHKV_OK;
+            }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, shkv_noalloc_scratch) != cudaSuccess || !p)
+        return SHKV_ERR_CUDA;
+    if (id == 0) {                       // the lookup made the primary context current
+        st = current_context_id(&id);
+        if (st != SHKV_OK || id == 0)
+            return st != SHKV_OK ? st : SHKV_ERR_CUDA;
     }
-    *ptr = g_noalloc_ptr[device];
+    g_noalloc_addresses.push_back({id, p});
+    *ptr = p;
     return SHKV_OK;
 }
 
@@ -880,7 +948,7 @@ extern "C" shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t ba
                                                      int32_t hq_per_model, const void *q, float scale, void *out,
                                                      float *lse_out, void *stream)
 {
-    if (!pool)
+    if (!pool || !out)
         return SHKV_ERR_INVALID_ARG;
     size_t need = 0;
     shkv_status st = shkv_decode_workspace_size(pool, batch, n_models, hq_per_model, &need);
@@ -894,13 +962,11 @@ extern "C" shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t ba
     if (device != pool->device)
         return SHKV_ERR_INVALID_ARG;
     void *scratch = nullptr;
-    st = noalloc_scratch(device, &scratch);
+    st = noalloc_scratch(&scratch);
     if (st != SHKV_OK)
         return st;
-    // the per-(request, head) arrival counters lead the workspace and must start at zero
-    const size_t count_bytes = align_up((uint32_t)(batch * pool->cfg.num_kv_heads * 4), 256);
-    if (cudaMemsetAsync(scratch, 0, count_bytes, (cudaStream_t)stream) != cudaSuccess)
-        return SHKV_ERR_CUDA;
-    return shkv_decode_attention(pool, batch, n_models, hq_per_model, q, scale, out, lse_out, scratch, need,
-                                 stream);
+    // decode_impl checks every argument first, then zeroes the arrival
+    // counters at the front of the scratch on `stream`, then launches
+    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, scratch, need, stream,
+                       nullptr, /*clear_counters=*/true);
 }

@@ -138,9 +138,20 @@ class SharedKVPool:
                                 _stream_ptr(stream))
         return (out, lse) if (return_lse or lse is not None) else out
 
+    _CONSUMERS = {"auto": N.SHKV_CONSUMER_AUTO, "mma": N.SHKV_CONSUMER_MMA_SYNC, "mma.sync": N.SHKV_CONSUMER_MMA_SYNC,
+                  "umma": N.SHKV_CONSUMER_TCGEN05, "tcgen05": N.SHKV_CONSUMER_TCGEN05}
+
+    def set_decode_consumer(self, consumer: str = "auto") -> None:
+        """Name the decode consumer kernel of this pool: 'auto' (default),
+        'mma' / 'mma.sync', or 'umma' / 'tcgen05' (taken where the shape
+        allows it)."""
+        if consumer not in self._CONSUMERS:
+            raise ValueError(f"unknown consumer {consumer!r}")
+        N.shkv_pool_set_decode_consumer(self.handle, self._CONSUMERS[consumer])
+
     def decode_consumer(self, n_models: int, hq: int) -> str:
         """'tcgen05' or 'mma.sync': the consumer kernel decode_attention runs
-        for this shape under the current environment."""
+        for this shape on this pool."""
         c = N.shkv_decode_consumer(self.handle, n_models, hq)
         return "tcgen05" if c == N.SHKV_CONSUMER_TCGEN05 else "mma.sync"
 

@@ -159,9 +159,9 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
  * Two interchangeable consumers implement the same result: warp-level
  * mma.sync tiles and, for head_dim 128, tcgen05 tiles with the accumulators
  * in tensor memory (tokens along the MMA's M dimension, 128-token stages).
- * shkv_decode_consumer() reports which one a call runs; setting the
- * environment variable SHKV_DECODE_CONSUMER to "mma" or "umma" overrides the
- * automatic choice where the shape allows it (read on every call).
+ * shkv_decode_consumer() reports which one a call runs;
+ * shkv_pool_set_decode_consumer() names one for a pool where the shape
+ * allows it (no call reads the process environment).
  * Supported: batch in [1, SHKV_MAX_BATCH], every L_b >= 1,
  * hq_per_model % num_kv_heads == 0, rows per KV head
  * n_models * hq_per_model / num_kv_heads <= 64.
@@ -328,12 +328,25 @@ shkv_status shkv_pages_stats(const shkv_pages *pages, shkv_pages_info *info);
 shkv_status shkv_pages_refcount(const shkv_pages *pages, int32_t page, int32_t *count);
 
 /* Consumer kernels of shkv_decode_attention. */
+#define SHKV_CONSUMER_AUTO (-1)
 #define SHKV_CONSUMER_MMA_SYNC 0
 #define SHKV_CONSUMER_TCGEN05 1
 
 /*
+ * Name the consumer kernel that shkv_decode_attention and
+ * shkv_decode_attention_tails run on this pool: SHKV_CONSUMER_AUTO (the
+ * default set at creation: tcgen05 for head_dim 128 and 16 to 64 rows per KV
+ * head, mma.sync otherwise), SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05.
+ * Both compute the same result; naming one serves tests and measurements.
+ * tcgen05 is taken only where the shape allows it (head_dim 128, at most 64
+ * rows per KV head); elsewhere mma.sync runs.  Host-only, no device work.
+ * Errors: SHKV_ERR_INVALID_ARG (null pool, unknown value).
+ */
+shkv_status shkv_pool_set_decode_consumer(shkv_pool *pool, int32_t consumer);
+
+/*
  * Which consumer shkv_decode_attention would run on this pool for n_models
- * decoders of hq_per_model query heads, given the environment as it is now:
+ * decoders of hq_per_model query heads, given the pool's consumer setting:
  * *consumer = SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05.  Host-only; no
  * device work.  Errors: SHKV_ERR_INVALID_ARG (null pointers, counts < 1),
  * SHKV_ERR_UNSUPPORTED (hq_per_model % num_kv_heads != 0 or more than 64
@@ -405,12 +418,15 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
  * SHKV_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the library
  * holds until the process exits.
  *   - The call allocates nothing: no cudaMalloc / cudaFree / allocating
- *     library routine.  Before each launch it clears the scratch's arrival
- *     counters with cudaMemsetAsync on `stream`.
- *   - Set-up: the first call on a device (the current device, which must be
- *     the pool's device) looks up the scratch's device address with
- *     cudaGetSymbolAddress and caches it.  Make that first call before any
- *     stream capture on that device.
+ *     library routine.  Once every argument check has passed, it clears the
+ *     scratch's arrival counters with cudaMemsetAsync on `stream`, then
+ *     launches; a rejected call enqueues nothing.
+ *   - Set-up: the first call in a CUDA context (the current device, which
+ *     must be the pool's device) looks up the scratch's device address with
+ *     cudaGetSymbolAddress and caches it under the context's unique ID, so a
+ *     new context (after cudaDeviceReset, or one the caller creates) gets
+ *     its own lookup and never a stale address.  Make the first call in a
+ *     context before any stream capture in it.
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents; calls whose executions overlap on the GPU (different streams
  *     without ordering) race on it and give wrong results.
@@ -422,6 +438,27 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
 shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t batch, int32_t n_models,
                                           int32_t hq_per_model, const void *q, float scale,
                                           void *out, float *lse_out, void *stream);
+
+/*
+ * Divide a decode batch among world_size replicas (host only, no CUDA).
+ * PrefillShare's framework scope runs decode in a data-parallel pool of
+ * GPUs; the decode step shards by request with no exchange step, so each
+ * replica holds and streams only the pages of the requests it owns.
+ * Requests are taken longest first (by pages, ceil(seq_lens[b] / page_size),
+ * ties by index) and each goes to the replica with the fewest pages so far
+ * (ties to the lower rank): every replica computes the same assignment from
+ * the same lengths.  The heaviest replica holds at most the mean plus the
+ * largest single request.
+ *   seq_lens    host int32 [batch], each >= 0
+ *   owner       host int32 [batch]: receives the replica of each request
+ *   rank_pages  host int64 [world_size] or NULL: receives each replica's
+ *               pages (unique KV bytes = pages * page_size * num_kv_heads *
+ *               head_dim * 4)
+ * Errors: SHKV_ERR_INVALID_ARG (null pointers, negative length,
+ * page_size < 1, world_size < 1).
+ */
+shkv_status shkv_partition_requests(int32_t batch, const int32_t *seq_lens, int32_t page_size,
+                                    int32_t world_size, int32_t *owner, int64_t *rank_pages);
 
 /* Static description of a status code. */
 const char *shkv_status_string(shkv_status status);

@@ -2,14 +2,20 @@
 inputs, read pages back for the oracle, and apply the stated tolerance.
 
 Tolerance (bf16 inputs, fp32 accumulation, fp64 oracle): elementwise
-|gpu - ref| <= 1e-2 beyond the rounding of the bf16 output itself, i.e.
-<= 1e-2 + half a bf16 ulp of ref (the output format is bf16, and an exact
-result of magnitude >= 2.56 cannot be stored within 1e-2: around 4.6, for
-instance, bf16 values are 2^-5 apart; for the averaged outputs of long
-contexts the extra term is below 0.005), and per-row normwise
-max_k |gpu - ref| / max_k |ref| <= 2e-2 (outputs are convex combinations of
-V rows whose magnitude shrinks with context length, so an elementwise
-relative error is ill-posed near 0).
+|gpu - ref| <= 1e-2 (+ half a bf16 ulp of ref where |ref| >= 2, see below),
+and per-row normwise max_k |gpu - ref| / max_k |ref| <= 2e-2 (outputs are
+convex combinations of V rows whose magnitude shrinks with context length,
+so an elementwise relative error is ill-posed near 0).
+
+The output format is bf16.  Below 2 its spacing is at most 2^-7, so the
+rounding of the output takes at most 0.004 of the 1e-2 bar and the bar is
+applied as it stands: that covers every output of a context of more than a
+few dozen tokens.  From 2 up the spacing is 2^-6 or more, so rounding alone
+takes 0.0078 or more (from 4 up, more than the whole bar): there the
+absolute error is measured beyond the rounding of the bf16 output itself,
+|gpu - ref| <= 1e-2 + half a bf16 ulp of ref.  Only rows that attend a
+handful of keys return such values (near a single N(0,1) V entry): short
+decode contexts and the first partial-prefill tokens.
 """
 import numpy as np
 import torch
@@ -20,6 +26,7 @@ from cross_model_shared_gb300 import workloads as W
 
 ABS_TOL = 1e-2
 REL_TOL = 2e-2
+ROUNDING_FROM = 2.0      # |ref| from which the bf16 output rounding is not charged to the bar
 LSE_TOL = 2e-3
 
 
@@ -31,8 +38,14 @@ def torch_to_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+# Decode consumer the pools made by make_pool name ("auto", "mma" or "umma");
+# the `umma` / `mma` fixtures of the consumer tests set it for one test.
+CONSUMER = {"name": "auto"}
+
+
 def make_pool(wl: W.Workload, k, v, lens=None, extra_max_batch: int = 0) -> SharedKVPool:
-    """Pool over the given K/V (numpy bf16 bits or bf16 CUDA tensors)."""
+    """Pool over the given K/V (numpy bf16 bits or bf16 CUDA tensors), with
+    the decode consumer CONSUMER names."""
     if isinstance(k, np.ndarray):
         k, v = bits_to_torch(k), bits_to_torch(v)
     lens = wl.lens_final if lens is None else lens
@@ -40,6 +53,7 @@ def make_pool(wl: W.Workload, k, v, lens=None, extra_max_batch: int = 0) -> Shar
                         max_pages_per_seq=wl.max_pages_per_seq, k_pages=k, v_pages=v,
                         initial_seq_lens=np.asarray(lens, np.int32))
     pool.block_table[: wl.B].copy_(torch.from_numpy(wl.block_table))
+    pool.set_decode_consumer(CONSUMER["name"])
     torch.cuda.synchronize()
     return pool
 
@@ -57,12 +71,16 @@ def compare(out_gpu: torch.Tensor, ref: np.ndarray, lse_gpu=None, lse_ref=None, 
     assert np.isfinite(got).all(), f"{what}: non-finite output"
     err = np.abs(got - ref)
     abs_err = float(err.max()) if err.size else 0.0
-    beyond = err - bf16_half_ulp(ref)
-    beyond_err = float(beyond.max()) if err.size else 0.0
     denom = np.maximum(np.abs(ref).max(axis=-1), 1e-30)
     rel_err = float((err.max(axis=-1) / denom).max()) if err.size else 0.0
-    assert beyond_err <= ABS_TOL, (f"{what}: max abs error beyond bf16 output rounding {beyond_err:.3e} > {ABS_TOL} "
-                                   f"(raw max {abs_err:.3e})")
+    rounding = np.where(np.abs(ref) >= ROUNDING_FROM, bf16_half_ulp(ref), 0.0)
+    beyond = err - rounding
+    beyond_err = float(beyond.max()) if err.size else 0.0
+    small = np.abs(ref) < ROUNDING_FROM
+    small_err = float(err[small].max()) if small.any() else 0.0
+    assert beyond_err <= ABS_TOL, (f"{what}: max abs error {beyond_err:.3e} > {ABS_TOL} (beyond the bf16 rounding "
+                                   f"of outputs >= {ROUNDING_FROM}; raw max {abs_err:.3e}, below "
+                                   f"{ROUNDING_FROM}: {small_err:.3e})")
     assert rel_err <= REL_TOL, f"{what}: max row-relative error {rel_err:.3e} > {REL_TOL}"
     if lse_gpu is not None:
         lg = lse_gpu.cpu().numpy().astype(np.float64)

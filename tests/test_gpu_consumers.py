@@ -2,8 +2,8 @@
 
 libshkv has two consumers for the same decode step: warp-level mma.sync
 tiles and, for head dim 128, tcgen05 tiles with tokens along the MMA's M
-dimension and the accumulators in tensor memory.  SHKV_DECODE_CONSUMER
-selects one per call; these tests force the tcgen05 consumer on every row
+dimension and the accumulators in tensor memory.  A pool names one with
+shkv_pool_set_decode_consumer; these tests force the tcgen05 consumer on every row
 count class (padded N of 16, 32, 48 and 64; three- and two-stage rings;
 4 and 8 pages per 128-token stage), check that it is the one that ran, and
 compare with the oracle and with the invariants the definition fixes.  The
@@ -17,14 +17,16 @@ import torch
 import oracle
 from cross_model_shared_gb300 import _native as N
 from cross_model_shared_gb300 import workloads as W
-from tests.gpu_common import bits_to_torch, compare, make_pool, oracle_for_requests, torch_to_bits
+from tests.gpu_common import CONSUMER, bits_to_torch, compare, make_pool, oracle_for_requests, torch_to_bits
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture
-def umma(monkeypatch):
-    monkeypatch.setenv("SHKV_DECODE_CONSUMER", "umma")
+def umma():
+    CONSUMER["name"] = "umma"
+    yield
+    CONSUMER["name"] = "auto"
 
 
 SHAPES = {
@@ -209,12 +211,13 @@ def test_umma_full_size_qwen14b_sampled(umma):
 # the mma.sync consumer where the automatic choice is tcgen05
 # --------------------------------------------------------------------------
 @pytest.fixture
-def mma(monkeypatch):
-    monkeypatch.setenv("SHKV_DECODE_CONSUMER", "mma")
+def mma():
+    CONSUMER["name"] = "mma"
+    yield
+    CONSUMER["name"] = "auto"
 
 
-def test_automatic_choice_by_rows_and_head_dim(monkeypatch):
-    monkeypatch.delenv("SHKV_DECODE_CONSUMER", raising=False)
+def test_automatic_choice_by_rows_and_head_dim():
     for shape, want in [("qwen14b", "tcgen05"), ("r24", "tcgen05"), ("r64", "tcgen05"), ("long", "tcgen05"),
                         ("llama8b", "mma.sync"), ("r1", "mma.sync")]:
         sh = SHAPES[shape]
