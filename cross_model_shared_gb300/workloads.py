@@ -247,10 +247,12 @@ def make_tails(wl: Workload, tail_lens, seed: int = 0, reserve_tokens: int = 0, 
     return tt, tl.astype(np.int32)
 
 
-def make_workload(name: str) -> Workload:
-    """The named configuration, seeded by its index."""
+def make_workload(name: str, replica: int = 0) -> Workload:
+    """The named configuration, seeded by its index.  ``replica`` r > 0 draws
+    another batch of the same shape and length mix (seeded by the index and
+    r), for a job whose global batch is several batches of the configuration."""
     c = CONFIGS[name]
-    rng = np.random.default_rng(c["seed"])
+    rng = np.random.default_rng(c["seed"] if replica == 0 else [c["seed"], 5005, replica])
     lens = _lengths(B=c["B"], rng=rng, **c["lens"])
     lens_final = lens + c["n_append"]
     bt, num_pages = _assign_pages(lens_final, c["P"], rng)
