@@ -12,6 +12,7 @@ previous call's contents; each call clears what must start at zero).
 import pytest
 import torch
 
+import oracle
 from cross_model_shared_gb300 import _native as N
 from cross_model_shared_gb300 import workloads as W
 from tests.gpu_common import bits_to_torch, compare, make_pool
@@ -28,11 +29,14 @@ def _noalloc(pool, q, n_models, scale):
     return out, lse
 
 
-@pytest.mark.parametrize("shape,lens", [
+SHAPES = [
     (dict(N=2, Hq=32, Hkv=8, D=128, P=16), [40000, 700, 3000, 64]),     # Llama-3.1-8B heads, split units
     (dict(N=8, Hq=40, Hkv=8, D=128, P=32), [5000, 1025, 33]),           # Qwen3-14B heads, R = 40
-])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(shape, lens):
+]
+
+
+@pytest.mark.parametrize("shape,lens", SHAPES)
+def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(shape, lens):
     wl = W.custom_workload("noalloc", B=len(lens), lens_prefill=lens, seed=31, **shape)
     q_bits = W.gen_q(wl)
     k, v = W.gen_pool(wl)
@@ -40,11 +44,56 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(shape, lens):
     q = bits_to_torch(q_bits)
     ref, ref_lse = pool.decode_attention(q, wl.N, scale=wl.scale, return_lse=True)
     assert pool.check_errors() == 0
-    ref64 = ref.double().cpu().numpy()
+    o64, l64 = oracle.decode_attention(q_bits, k, v, wl.block_table, wl.lens_final, n_models=wl.N, hq=wl.Hq,
+                                       scale=wl.scale)
     for call in range(2):
         out, lse = _noalloc(pool, q, wl.N, wl.scale)
         assert pool.check_errors() == 0, f"device error bits on call {call}"
-        compare(out, ref64, lse, ref_lse.double().cpu().numpy(), what=f"noalloc call {call}")
+        compare(out, o64, lse, l64, what=f"noalloc call {call} vs oracle")
+        # same kernel, same split plan: the same bits as the workspace entry point
+        assert torch.equal(out, ref), f"call {call}: output differs from shkv_decode_attention"
+        assert torch.equal(lse, ref_lse), f"call {call}: lse differs from shkv_decode_attention"
+
+
+def test_noalloc_is_exact_after_a_call_that_set_error_bits():
+    """A call over an out-of-range block-table entry (bounds-checked on the
+    device: the page is skipped and a flag set) leaves the shared scratch as
+    it may; the next call must still give the exact result."""
+    shape, lens = SHAPES[0]
+    wl = W.custom_workload("noalloc_err", B=len(lens), lens_prefill=lens, seed=37, **shape)
+    q_bits = W.gen_q(wl)
+    k, v = W.gen_pool(wl)
+    pool = make_pool(wl, k, v)
+    q = bits_to_torch(q_bits)
+    ref, ref_lse = pool.decode_attention(q, wl.N, scale=wl.scale, return_lse=True)
+    assert pool.check_errors() == 0
+    saved = int(pool.block_table[0, 5].item())
+    pool.block_table[0, 5] = wl.num_pages + 11
+    _noalloc(pool, q, wl.N, wl.scale)
+    assert pool.check_errors() & N.SHKV_ERRF_PAGE_OOB
+    pool.block_table[0, 5] = saved
+    for call in range(2):
+        out, lse = _noalloc(pool, q, wl.N, wl.scale)
+        assert pool.check_errors() == 0, f"device error bits on call {call}"
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse), f"call {call} after the flagged call"
+
+
+def test_noalloc_rejected_call_enqueues_nothing():
+    """Argument errors return before the scratch is touched; the next valid
+    call is exact."""
+    shape, lens = SHAPES[1]
+    wl = W.custom_workload("noalloc_rej", B=len(lens), lens_prefill=lens, seed=41, **shape)
+    q_bits = W.gen_q(wl)
+    k, v = W.gen_pool(wl)
+    pool = make_pool(wl, k, v)
+    q = bits_to_torch(q_bits)
+    ref = pool.decode_attention(q, wl.N, scale=wl.scale)
+    with pytest.raises(N.ShkvError) as e:
+        _noalloc(pool, q, wl.N, float("nan"))
+    assert e.value.status == N.SHKV_ERR_INVALID_ARG
+    out, _ = _noalloc(pool, q, wl.N, wl.scale)
+    assert pool.check_errors() == 0
+    assert torch.equal(out, ref)
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():
