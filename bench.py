@@ -12,8 +12,13 @@ oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl shkv|reference]
 
-Under torchrun each rank runs an independent replica of the workload on its
-own GPU (the path shards by request with no exchange step): weak scaling.
+The default workload is Qwen3-14B attention (128 requests, 8 decoders,
+contexts from a truncated log-normal with mean 27K tokens, ~14.5 GB of KV per
+step), the largest configuration.  Under torchrun the global batch is N
+batches of the configuration; the host partitioner (shkv_partition_requests)
+gives each rank its requests, balanced by unique KV bytes, and each rank
+holds and streams only its own pages: the path shards by request with no
+exchange step, per-GPU work stays about one batch (weak scaling).
 """
 from __future__ import annotations
 
@@ -55,12 +60,14 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="llama8b", choices=W.CONFIG_ORDER)
+    ap.add_argument("--config", default="qwen14b", choices=W.CONFIG_ORDER)
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first B requests of the workload (reduced case for profiling)")
     ap.add_argument("--impl", default="shkv", choices=["shkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--isolated", type=int, default=20,
+                    help="single decode launches timed one at a time, each after an L2 flush (0: skip)")
     ap.add_argument("--prefix-pages", action="store_true",
                     help="host-side page-manager run: a seeded multi-agent workflow over the prefix pool")
     ap.add_argument("--prefill-tokens", type=int, default=0,
@@ -72,12 +79,92 @@ def parse_args():
     return ap.parse_args()
 
 
-def load_workload(args) -> W.Workload:
-    wl = W.make_workload(args.config)
+def load_workload(args, replica: int = 0) -> W.Workload:
+    wl = W.make_workload(args.config, replica)
     if args.batch and args.batch < wl.B:
         wl = W.custom_workload(f"{wl.name}[:{args.batch}]", B=args.batch, N=wl.N, Hq=wl.Hq, Hkv=wl.Hkv, D=wl.D,
                                P=wl.P, lens_prefill=wl.lens_prefill[:args.batch], n_append=wl.n_append, seed=wl.seed)
     return wl
+
+
+class Job:
+    """The whole job's requests and this rank's share of them.  One rank: the
+    configuration itself.  N ranks: N batches of the configuration (replica
+    r drawn with its own seed), divided among the ranks by the library's
+    host partitioner, each rank holding only its own requests' pages."""
+
+    def __init__(self, args, world_size: int, rank: int, partition: bool = True):
+        self.base = load_workload(args)
+        parts = [self.base] + [load_workload(args, r) for r in range(1, world_size)]
+        self.lens_prefill = np.concatenate([w.lens_prefill for w in parts]).astype(np.int32)
+        self.lens_final = np.concatenate([w.lens_final for w in parts]).astype(np.int32)
+        self.world_size, self.rank = world_size, rank
+        b = self.base
+        self.page_bytes = b.P * b.Hkv * b.D * 2 * 2
+        self.qo_bytes_per_request = 2 * b.rows * b.D * 2
+        self.kv_bytes = int(((self.lens_final.astype(np.int64) + b.P - 1) // b.P).sum()) * self.page_bytes
+        if not partition:
+            return
+        if world_size == 1:
+            self.owner = np.zeros(b.B, np.int32)
+            self.rank_pages = np.array([int(b.pages_per_request().sum())], np.int64)
+            self.local = b
+        else:
+            from cross_model_shared_gb300 import _native as N
+            self.owner, self.rank_pages = N.shkv_partition_requests(self.lens_final, b.P, world_size)
+            mine = np.flatnonzero(self.owner == rank)
+            self.local = W.custom_workload(f"{b.name} shard {rank}/{world_size}", B=len(mine), N=b.N, Hq=b.Hq,
+                                           Hkv=b.Hkv, D=b.D, P=b.P, lens_prefill=self.lens_prefill[mine],
+                                           n_append=b.n_append, seed=1000 * b.seed + rank + 1)
+
+    def rank_requests(self):
+        return [int((self.owner == r).sum()) for r in range(self.world_size)]
+
+    def rank_bytes(self):
+        """Algorithmic bytes of one step on each rank: its unique KV pages +
+        its queries read + its outputs written."""
+        return [int(self.rank_pages[r]) * self.page_bytes + n * self.qo_bytes_per_request
+                for r, n in enumerate(self.rank_requests())]
+
+    def total_bytes(self) -> int:
+        """Algorithmic bytes of one step of the whole job (every rank's)."""
+        return self.kv_bytes + len(self.lens_final) * self.qo_bytes_per_request
+
+
+def workload_config(job: "Job"):
+    """The `config` object of both arms' JSON lines: the workload by name
+    and shape, the job's global batch, and how L2 reuse between timed steps
+    is excluded."""
+    per_rank_kv = job.kv_bytes // job.world_size
+    l2 = l2_label(per_rank_kv, pool_copies_for(per_rank_kv))
+    b = job.base
+    return {
+        "workload": b.name, "batch": int(len(job.lens_final)), "decoders": b.N, "hq_per_decoder": b.Hq,
+        "hkv": b.Hkv, "head_dim": b.D, "page_size": b.P, "rows_per_kv_head": b.R,
+        "mean_context": float(job.lens_final.mean()), "kv_bytes_per_step": job.kv_bytes,
+        "step_bytes": job.total_bytes(),
+        "l2": l2, "parallelism": f"request shards x{job.world_size}",
+    }
+
+
+L2_BYTES = 129 * 2**20
+ROTATE_BELOW_BYTES = 10**9
+
+
+def pool_copies_for(kv_bytes: int) -> int:
+    """Copies of a pool to rotate through so that consecutive steps read
+    different memory: enough to pass 1 GB of KV, at most 16."""
+    if kv_bytes >= ROTATE_BELOW_BYTES:
+        return 1
+    return int(min(16, -(-ROTATE_BELOW_BYTES // max(1, kv_bytes))))
+
+
+def l2_label(kv_bytes: int, copies: int) -> str:
+    if copies == 1:
+        return f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV per step vs 129 MB of L2"
+    total = copies * kv_bytes
+    resident = "larger than L2" if total > 2 * L2_BYTES else "L2-resident (warm)"
+    return f"{copies} pool copies rotated step by step ({total / 1e9:.2f} GB, {resident})"
 
 
 def dist_env():
@@ -209,23 +296,28 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float):
-    """Time the fp64 oracle on whole requests (all rows, full context) until
-    the budget is spent.  Returns (KV GB/s over the sampled requests, cores,
-    description)."""
+def quantile_requests(lens, n: int = 8):
+    """A fixed subset of up to n requests at evenly spaced length quantiles
+    (shortest, ..., median, ..., longest)."""
+    order = np.argsort(np.asarray(lens), kind="stable")
+    idx = np.unique(np.rint(np.linspace(0, len(order) - 1, min(n, len(order)))).astype(int))
+    return [int(order[i]) for i in idx]
+
+
+def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float, step_kv_bytes: int):
+    """Time the fp64 oracle on whole requests (all rows, full context): a
+    fixed subset of 8 requests at the workload's length quantiles, cycled
+    until the budget is spent.  The rate (KV GB/s) is extrapolated to a whole
+    step.  Returns the cpu_baseline object."""
     import oracle
-    order = np.argsort(wl.lens_final, kind="stable")
+    picks = quantile_requests(wl.lens_final)
     kv_bytes, elapsed, done = 0, 0.0, []
     cache = {}
     i = 0
-    # whole requests, starting at the median length and cycling through the
-    # batch, until the time budget is spent
-    while elapsed < budget_s and i < 64 * wl.B:
-        b = int(order[(len(order) // 2 + i) % len(order)])
+    while elapsed < budget_s and i < 64 * len(picks):
+        b = picks[i % len(picks)]
         if b not in cache:
             cache[b] = fetch_pages(b)
-            if len(cache) > 8:
-                cache.pop(next(iter(cache)))
         kb, vb, npg = cache[b]
         bt = np.arange(npg, dtype=np.int32)[None, :]
         t0 = time.perf_counter()
@@ -235,25 +327,29 @@ def cpu_oracle_sample(wl: W.Workload, q_bits, fetch_pages, budget_s: float):
         kv_bytes += npg * wl.P * wl.Hkv * wl.D * 4
         done.append(b)
         i += 1
-    desc = (f"{len(done)} whole requests of {wl.name} ({len(set(done))} distinct; all {wl.rows} stacked rows, "
-            f"full context, {sum(int(wl.lens_final[b]) for b in done)} tokens), fp64, {oracle.num_threads()} threads")
-    return kv_bytes / elapsed / 1e9, oracle.num_threads(), desc, elapsed
+    value = kv_bytes / elapsed / 1e9
+    lens = [int(wl.lens_final[b]) for b in picks]
+    desc = (f"{len(picks)} whole requests of {wl.name} at its length quantiles ({min(lens)}..{max(lens)} tokens; "
+            f"all {wl.rows} stacked rows, full context), {len(done)} oracle calls, fp64, "
+            f"{oracle.num_threads()} threads; rate extrapolated to the whole step")
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+            "seconds": round(elapsed, 2), "extrapolated_step_s": step_kv_bytes / (value * 1e9)}
 
 
 def run_reference(args):
     """The oracle as the reference arm, on the host cores (rank 0 only): each
     step is one whole request of the workload (all stacked rows, full
-    context), cycling from the median length like the cpu_baseline sample;
-    pages are drawn on the host (up to 8 distinct requests, untimed)."""
+    context), cycling through the 8 requests at its length quantiles like the
+    cpu_baseline sample; their pages are drawn on the host (untimed)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     import oracle
-    wl = load_workload(args)
+    job = Job(args, ws, 0, partition=False)      # the GPU arm's global batch at this world size
+    wl = job.base
     q = W.gen_q(wl)
     rng = np.random.default_rng(wl.seed + 77)
-    order = np.argsort(wl.lens_final, kind="stable")
-    n_distinct = min(8, wl.B)
+    picks = quantile_requests(wl.lens_final)
     cache = {}
 
     def pages(b):
@@ -268,7 +364,7 @@ def run_reference(args):
     wall0 = time.perf_counter()
     total_steps = args.steps + args.warmup
     for s in range(total_steps):
-        b = int(order[(len(order) // 2 + s % n_distinct) % len(order)])
+        b = picks[s % len(picks)]
         kb, vb, npg = pages(b)
         bt = np.arange(npg, dtype=np.int32)[None, :]
         t0 = time.perf_counter()
@@ -282,15 +378,18 @@ def run_reference(args):
         if time.perf_counter() - wall0 > 240.0 and len(done) > 0:
             break                      # keep the arm within a few minutes
     value = kv_bytes / elapsed / 1e9
-    desc = (f"{len(done)} timed steps, each one whole request of {wl.name} ({len(set(done))} distinct; all "
-            f"{wl.rows} stacked rows, full context), fp64 oracle, {oracle.num_threads()} threads")
+    lens = [int(wl.lens_final[b]) for b in picks]
+    desc = (f"{len(done)} timed steps, each one whole request of {wl.name} from the {len(picks)} at its length "
+            f"quantiles ({min(lens)}..{max(lens)} tokens; all {wl.rows} stacked rows, full context), fp64 oracle, "
+            f"{oracle.num_threads()} threads")
+    kv_step = job.kv_bytes
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(1, len(done)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "parallelism": "host cores"},
+        "config": workload_config(job),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "extrapolated_step_s": kv_step / (value * 1e9)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -664,7 +763,8 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    wl = load_workload(args)
+    job = Job(args, ws, rank)
+    wl = job.local
     q_bits = W.gen_q(wl)
     k_dev, v_dev = W.gen_pool_device(wl, device=dev)
     pool = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
@@ -683,19 +783,32 @@ def run_gpu(args):
         torch.cuda.synchronize()
         append_ms = e0.elapsed_time(e1)
         del kn, vn
+    # Small pools are rotated: step i reads copy i % n, so consecutive steps
+    # never find each other's pages in L2.
+    n_copies = pool_copies_for(job.kv_bytes // ws)
+    pools = [pool]
+    for _ in range(1, n_copies):
+        p2 = SharedKVPool(wl.num_pages, wl.P, wl.Hkv, wl.D, max_batch=wl.B, max_pages_per_seq=wl.max_pages_per_seq,
+                          device=dev, k_pages=k_dev.clone(), v_pages=v_dev.clone(), initial_seq_lens=wl.lens_final)
+        p2.block_table.copy_(pool.block_table)
+        pools.append(p2)
     q = torch.from_numpy(q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty_like(q)
-    ws_t = pool.workspace(wl.B, wl.N, wl.Hq)
+    for p_ in pools:
+        p_.workspace(wl.B, wl.N, wl.Hq)
     torch.cuda.synchronize()
+    it = [0]
 
     def step():
-        pool.decode_attention(q, wl.N, scale=wl.scale, out=out)
+        pools[it[0] % n_copies].decode_attention(q, wl.N, scale=wl.scale, out=out)
+        it[0] += 1
 
     for _ in range(max(3, args.warmup)):
         step()
-    flags = pool.check_errors()
-    if flags:
-        raise RuntimeError(f"device error bits 0x{flags:x} during warm-up")
+    for p_ in pools:
+        flags = p_.check_errors()
+        if flags:
+            raise RuntimeError(f"device error bits 0x{flags:x} during warm-up")
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -716,14 +829,38 @@ def run_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
-    flags = pool.check_errors()
-    if flags:
-        raise RuntimeError(f"device error bits 0x{flags:x} in the timed region")
+    for p_ in pools:
+        flags = p_.check_errors()
+        if flags:
+            raise RuntimeError(f"device error bits 0x{flags:x} in the timed region")
 
     ms_per_step = ms / args.steps
-    nbytes = step_bytes(wl)
-    value = job_throughput_gbs(nbytes, args.steps, ws, ms * 1e-3)
-    per_gpu = nbytes / (ms_per_step * 1e-3) / 1e9
+    nbytes = job.total_bytes()
+    value = nbytes * args.steps / (ms * 1e-3) / 1e9
+    local_bytes = job.rank_bytes()[rank]
+    local_ms = ev0.elapsed_time(ev1) / args.steps
+    per_gpu = local_bytes / (local_ms * 1e-3) / 1e9
+
+    # --- isolated launches: each one after an L2 flush (a write over twice
+    # the L2 size, itself a kernel between consecutive decode launches, so no
+    # launch overlaps its predecessor), timed on its own
+    isolated = None
+    if args.isolated > 0:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.isolated)]
+        for i, (a, b) in enumerate(evs):
+            flush.fill_(i & 0xff)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        iso_ms = sorted(a.elapsed_time(b) for a, b in evs)
+        med = statistics.median(iso_ms)
+        isolated = {"ms": med, "min_ms": iso_ms[0], "max_ms": iso_ms[-1], "launches": len(iso_ms),
+                    "gbs": local_bytes / (med * 1e-3) / 1e9, "frac": None,
+                    "how": "median of single launches, each after an L2 flush (a 258 MB write kernel)"}
+        del flush
 
     # --- the same kernel once per decoder, without sharing (N launches/step)
     q_models = [q[:, m * wl.Hq:(m + 1) * wl.Hq].contiguous() for m in range(wl.N)]
@@ -733,30 +870,30 @@ def run_gpu(args):
         pool.decode_attention(q_models[m], 1, scale=wl.scale, out=out_m[m])
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(u_steps):
+    for i in range(u_steps):
+        p_ = pools[i % n_copies]
         for m in range(wl.N):
-            pool.decode_attention(q_models[m], 1, scale=wl.scale, out=out_m[m])
+            p_.decode_attention(q_models[m], 1, scale=wl.scale, out=out_m[m])
     ev1.record(stream)
     torch.cuda.synchronize()
     unshared_ms = ev0.elapsed_time(ev1) / u_steps
 
     # --- end to end through the C ABI: pinned host q in, host out back, per step
     e_steps = max(10, min(args.steps, 1000))
-    pipe = E2EPipeline(q, lambda qd, od: pool.decode_attention(qd, wl.N, scale=wl.scale, out=od))
-    e2e_step = pipe.step
-
+    pipe = E2EPipeline(q, lambda qd, od: pools[pipe.i % n_copies].decode_attention(qd, wl.N, scale=wl.scale,
+                                                                                     out=od))
     for _ in range(3):
-        e2e_step()
+        pipe.step()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(e_steps):
-        e2e_step()
+        pipe.step()
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
-    e2e_value = job_throughput_gbs(nbytes, e_steps, ws, e2e_s)
-    qbytes = q.numel() * 2
+    e2e_value = nbytes * e_steps / e2e_s / 1e9
+    qbytes = len(job.lens_final) * wl.rows * wl.D * 2
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -766,35 +903,33 @@ def run_gpu(args):
             kb = k_dev.index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16)
             vb = v_dev.index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16)
             return kb, vb, npg
-        v_cpu, cores, desc, secs = cpu_oracle_sample(wl, q_bits, fetch, args.cpu_budget_s)
-        cpu = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-               "seconds": round(secs, 2)}
+        cpu = cpu_oracle_sample(wl, q_bits, fetch, args.cpu_budget_s, job.kv_bytes)
 
     peak, peak_kind = measured_peaks()
+    if isolated is not None:
+        isolated["frac"] = isolated["gbs"] / peak
     consumer = pool.decode_consumer(wl.N, wl.Hq)
-    traffic = profiled_traffic(consumer, wl.name)
+    traffic = profiled_traffic(consumer, job.base.name) if ws == 1 else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": wl.name, "batch": wl.B, "decoders": wl.N, "hq_per_decoder": wl.Hq, "hkv": wl.Hkv,
-                "head_dim": wl.D, "page_size": wl.P, "rows_per_kv_head": wl.R,
-                "mean_context": float(wl.lens_final.mean()), "kv_bytes_per_step": W.unique_kv_bytes(wl),
-                "step_bytes": nbytes, "l2": "inputs larger than L2" if W.unique_kv_bytes(wl) > 2 * 129e6
-                else "L2-resident working set (warm)", "parallelism": f"replicas x{ws}",
-            },
+            "config": workload_config(job),
             "steps_per_s": 1e3 / ms_per_step,
-            "decoder_tokens_per_s": wl.B * wl.N * 1e3 / ms_per_step,
+            "decoder_tokens_per_s": len(job.lens_final) * wl.N * 1e3 / ms_per_step,
             "pct_of_hbm_peak": {"measured_copy": 100 * per_gpu / peak, "nominal_8tbs": 100 * per_gpu / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
                          "frac": per_gpu / peak, "peak_kind": peak_kind, "traffic": traffic,
-                         "kernel": KERNELS[consumer]["name"], "consumer": consumer},
+                         "kernel": KERNELS[consumer]["name"], "consumer": consumer,
+                         "bytes_per_launch": local_bytes},
+            "isolated": isolated,
             "unshared": {"ms_per_step": unshared_ms, "launches_per_step": wl.N,
-                         "speedup_of_sharing": unshared_ms / ms_per_step},
+                         "speedup_of_sharing": unshared_ms / local_ms},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": qbytes, "d2h_bytes_per_step": qbytes,
                     "steps": e_steps, "copies": "own streams, two buffers: overlap the neighbouring steps' kernels"},
+            "shards": {"requests": job.rank_requests(), "step_bytes": job.rank_bytes(),
+                       "partitioner": "shkv_partition_requests (longest first, fewest pages)"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -71,6 +71,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
     assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True and d["n_gpus"] == 1
     assert d["value"] > 0 and d["config"]["workload"] == "tiny"
+    import argparse
+    gpu_arm_config = bench.workload_config(bench.Job(argparse.Namespace(config="tiny", batch=0), 1, 0,
+                                                     partition=False))
+    assert d["config"] == gpu_arm_config             # the same keys and values as the GPU arm's line
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]
@@ -91,3 +95,31 @@ def test_reference_arm_under_torchrun_prints_once():
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
     assert out.returncode == 0, out.stderr[-2000:]
     assert len([l for l in out.stdout.splitlines() if l.startswith("{")]) == 1
+
+
+def test_job_shards_the_global_batch_by_the_partitioner():
+    """Under torchrun the bench's global batch is N batches of the workload;
+    each rank's local workload holds exactly its requests (by the library's
+    partitioner), and the ranks' step bytes add up to the job's."""
+    import argparse
+
+    import numpy as np
+
+    from cross_model_shared_gb300 import build as B
+    B.build()
+    args = argparse.Namespace(config="qwen14b", batch=0)
+    one = bench.Job(args, 1, 0)
+    assert one.local is one.base and one.total_bytes() == bench.step_bytes(one.base)
+    jobs = [bench.Job(args, 4, r) for r in range(4)]
+    j0 = jobs[0]
+    assert len(j0.lens_final) == 4 * j0.base.B
+    assert np.array_equal(j0.lens_final[:j0.base.B], one.lens_final)
+    got = sorted(np.concatenate([j.local.lens_final for j in jobs]).tolist())
+    assert got == sorted(j0.lens_final.tolist())
+    for r, j in enumerate(jobs):
+        assert np.array_equal(j.owner, j0.owner)
+        assert bench.step_bytes(j.local) == j0.rank_bytes()[r]
+    assert sum(j0.rank_bytes()) == j0.total_bytes()
+    cfg = bench.workload_config(j0)
+    assert cfg["batch"] == 4 * j0.base.B and cfg["workload"] == "qwen14b"
+    assert cfg == bench.workload_config(bench.Job(args, 4, 0, partition=False))
