@@ -388,10 +388,13 @@ __device__ void pf_softmax(const PrefillParams &p, const PfCtx &c, const Tile &t
     const float sl2 = p.scale_log2;
     float m_use = -INFINITY, lsum = 0.f;
     bool alive = true;
+    // the softmax warps poll their barriers (measured faster than sleeping
+    // on them, which the issuers and producers do): their waits sit on the
+    // tile's chain QK -> softmax -> PV
     auto wait = [&](uint32_t bar, uint32_t parity) {
         bool ok = false;
         if (alive)
-            ok = pf_wait(bar, parity, c.abort_flag, p.err);
+            ok = mbar_wait_bounded(bar, parity, c.abort_flag, p.err);
         alive = __all_sync(0xffffffffu, ok) && alive;
         return alive;
     };
