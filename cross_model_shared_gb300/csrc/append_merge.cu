@@ -11,37 +11,61 @@
 namespace shkv {
 
 // Partial-prefill append (PrefillShare Sec. 3.3 / Sec. 7): token t of request
-// b lands at logical position L_b + t of the shared paged cache.  One
-// (request, token, head) row of D bf16 values is moved per group of D/8
-// threads, 16 bytes each, so a warp writes 2 (D=128) or 4 (D=64) whole rows
-// with full-sector coalescing on both sides.  The old lengths come from the
-// pool's host copy; block 0 then publishes L_b + T (no thread of this kernel
-// reads seq_lens after that store).
+// b lands at logical position L_b + t of the shared paged cache.  One warp
+// per appended token: its page and slot are looked up once, then the lanes
+// move the token's Hkv head rows of K and V (D bf16 each) as 16-byte vectors
+// -- contiguous on the source side, whole head rows of 128 or 256 bytes on
+// the destination side.  The old lengths come from the pool's host copy;
+// block 0 then publishes L_b + T (no thread of this kernel reads seq_lens
+// after that store).
 __global__ void __launch_bounds__(256) shkv_append_kernel(const __grid_constant__ AppendParams p)
 {
     pdl_launch_dependents();
     pdl_wait_prior();
-    const int hv = p.head_vecs;                      // 16-byte vectors per head row
-    const int64_t rows = (int64_t)p.batch * p.n_new * p.hkv;
-    const int64_t total = rows * hv;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = i / hv;
-        const int v = (int)(i - row * hv);
-        const int g = (int)(row % p.hkv);
-        const int64_t bt_ = row / p.hkv;
-        const int t = (int)(bt_ % p.n_new);
-        const int b = (int)(bt_ / p.n_new);
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    const int hv = p.head_vecs;                      // 16-byte vectors per head row: 8 or 16
+    const int log2hv = __ffs(hv) - 1;
+    const int per_tok = p.hkv * hv;                  // vectors per token, of K or of V
+    const int64_t ntok = (int64_t)p.batch * p.n_new;
+    for (int64_t tok = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); tok < ntok;
+         tok += (int64_t)gridDim.x * warps) {
+        const int b = (int)(tok / p.n_new);
+        const int t = (int)(tok - (int64_t)b * p.n_new);
         const int pos = p.old_len[b] + t;
         const int page = __ldg(p.block_table + (int64_t)b * p.max_pages + pos / p.page_size);
         if (page < 0 || page >= p.num_pages) {
-            if (v == 0)
+            if (lane == 0)
                 atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
             continue;
         }
-        const int64_t dst = (((int64_t)page * p.hkv + g) * p.page_size + pos % p.page_size) * hv + v;
-        p.k_pages[dst] = __ldg(p.k_new + i);
-        p.v_pages[dst] = __ldg(p.v_new + i);
+        const int slot = pos % p.page_size;
+        const uint4 *ks = p.k_new + tok * per_tok;
+        const uint4 *vs = p.v_new + tok * per_tok;
+        const int64_t row0 = (int64_t)page * p.hkv;
+        // up to 4 vectors of K and 4 of V a lane in flight before their stores
+        // (the copy is bound by the bytes in flight, not by instructions)
+        for (int j0 = 0; j0 < per_tok; j0 += 128) {
+            uint4 kv[4], vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * 32 + lane;
+                if (j < per_tok) {
+                    kv[u] = __ldg(ks + j);
+                    vv[u] = __ldg(vs + j);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * 32 + lane;
+                if (j < per_tok) {
+                    const int g = j >> log2hv, v = j & (hv - 1);
+                    const int64_t dst = ((row0 + g) * p.page_size + slot) * hv + v;
+                    p.k_pages[dst] = kv[u];
+                    p.v_pages[dst] = vv[u];
+                }
+            }
+        }
     }
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
@@ -54,8 +78,8 @@ __global__ void __launch_bounds__(256) shkv_append_kernel(const __grid_constant_
 
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream)
 {
-    const int64_t total = (int64_t)p.batch * p.n_new * p.hkv * p.head_vecs;
-    int64_t blocks = (total + 255) / 256;
+    const int64_t ntok = (int64_t)p.batch * p.n_new;
+    int64_t blocks = (ntok + 7) / 8;                 // 8 warps a block, one token each
     if (blocks > (int64_t)num_sms * 8)
         blocks = (int64_t)num_sms * 8;
     if (blocks < 1)
