@@ -758,10 +758,10 @@ def run_gpu(args):
     from cross_model_shared_gb300 import SharedKVPool
 
     ws, rank, local = dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
 
     job = Job(args, ws, rank)
     wl = job.local

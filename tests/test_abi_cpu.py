@@ -48,6 +48,8 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.shkv_decode_attention(None, 1, 1, 1, None, 1.0, None, None, None, 0, None) == N.SHKV_ERR_INVALID_ARG
     assert lib.shkv_splitkv_merge(0, 1, 1, 4, None, None, None, None, None) == N.SHKV_ERR_INVALID_ARG
     assert lib.shkv_splitkv_merge(1, 1, 1, 6, 16, 16, 16, None, None) == N.SHKV_ERR_INVALID_ARG  # D % 4
+    assert lib.shkv_pool_set_decode_consumer(None, 0) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_decode_attention_noalloc(None, 1, 1, 1, None, 1.0, None, None, None) == N.SHKV_ERR_INVALID_ARG
 
 
 SEGMENT_COST = 16  # chunks charged per (request, head) segment by the planner

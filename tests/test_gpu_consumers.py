@@ -252,3 +252,22 @@ def test_mma_long_single_request_split_and_merged(mma):
     ref, lref = oracle.decode_attention(q, k, v, wl.block_table, wl.lens_final, n_models=wl.N, hq=wl.Hq,
                                         scale=wl.scale)
     compare(out, ref, lse, lref, what="mma split")
+
+
+def test_consumer_setting_is_per_pool_and_checked():
+    """A pool's consumer choice applies to that pool only; unknown values are
+    rejected by the binding and by the C entry point."""
+    sh = SHAPES["long"]
+    wl = W.custom_workload("setting", B=1, lens_prefill=[40], seed=1, **sh)
+    k, v = W.gen_pool(wl)
+    a, b = make_pool(wl, k, v), make_pool(wl, k, v)
+    a.set_decode_consumer("mma")
+    assert a.decode_consumer(wl.N, wl.Hq) == "mma.sync"
+    assert b.decode_consumer(wl.N, wl.Hq) == "tcgen05"
+    a.set_decode_consumer("auto")
+    assert a.decode_consumer(wl.N, wl.Hq) == "tcgen05"
+    with pytest.raises(ValueError):
+        a.set_decode_consumer("fastest")
+    with pytest.raises(N.ShkvError) as e:
+        N.shkv_pool_set_decode_consumer(a.handle, 7)
+    assert e.value.status == N.SHKV_ERR_INVALID_ARG
