@@ -117,7 +117,7 @@ def load() -> ctypes.CDLL:
         "shkv_decode_attention": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
         "shkv_splitkv_merge": [i32, i32, i32, i32, vp, vp, vp, vp, vp],
         "shkv_check_errors": [vp, vp, u32p],
-        "shkv_plan_decode": [i32, i32p, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+        "shkv_plan_decode": [i32, i32p, i32, i32, i32, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
         "shkv_decode_consumer": [vp, i32, i32, ctypes.POINTER(i32)],
         "shkv_pool_set_decode_consumer": [vp, i32],
@@ -210,14 +210,17 @@ def shkv_check_errors(pool: int, stream: int) -> int:
     return flags.value
 
 
-def shkv_plan_decode(lens, page_size: int, num_kv_heads: int, max_ctas: int):
-    """Host-only split plan: (cta_begin list, num_ctas, num_splits)."""
+def shkv_plan_decode(lens, page_size: int, num_kv_heads: int, n_models: int, hq_per_model: int, consumer: int,
+                     max_ctas: int):
+    """Host-only split plan for `consumer` (SHKV_CONSUMER_MMA_SYNC or
+    SHKV_CONSUMER_TCGEN05): (cta_begin list, num_ctas, num_splits)."""
     import numpy as np
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     begin = np.zeros(max_ctas + 1, dtype=np.int64)
     nc, ns = ctypes.c_int32(), ctypes.c_int32()
-    _check(load().shkv_plan_decode(len(lens), lens.ctypes.data, page_size, num_kv_heads, max_ctas,
-                                   begin.ctypes.data, ctypes.byref(nc), ctypes.byref(ns)), "shkv_plan_decode")
+    _check(load().shkv_plan_decode(len(lens), lens.ctypes.data, page_size, num_kv_heads, n_models, hq_per_model,
+                                   consumer, max_ctas, begin.ctypes.data, ctypes.byref(nc), ctypes.byref(ns)),
+           "shkv_plan_decode")
     return begin[: nc.value + 1].copy(), nc.value, ns.value
 
 

@@ -127,25 +127,68 @@ bool make_pool_map_2d(CUtensorMap *tm, void *base, const shkv_pool_config &c)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// What a CTA's range costs the consumer that runs it, in tokens of one KV
+// head streamed (a token is a row of K and a row of V, 4 * head_dim bytes).
+// A range holds pieces of (request, head) units; a piece costs
+//   its stages, whole: tokens rounded up to the ring's stage (the stage grid
+//          starts at the piece's first page);
+//   seg    the segment's query load, row sums, log-sum-exp and output write;
+//   first  if it starts inside its unit (an opening split piece);
+//   last   if it ends inside its unit (a closing split piece: its partial,
+//          arrival and, as the last arriver, the merge, at the end of the
+//          CTA's range where nothing hides them).
+struct PlanCosts {
+    int64_t stage, seg, first, last;
+};
+
+// tcgen05 consumer: the segment epilogue and the split merge handle one
+// output row per stacked query row, so those costs grow with the rows; per
+// row, in tokens: segment 12, opening piece 5, closing piece 20 (the first
+// two fitted to per-CTA exit times on GB300 at 16 rows and 16-token pages,
+// which put the closing piece at 11.5; 20 measured as fast or faster on
+// every workload, 0.5x and 1.5x of all three slower).  mma.sync consumer:
+// SHKV_SEGMENT_COST_CHUNKS pages a piece, nothing for a split (the values
+// its sweep settled on).
+#ifndef SHKV_PLAN_SEG_X2
+#define SHKV_PLAN_SEG_X2 24      // twice the tokens per row: segment
+#endif
+#ifndef SHKV_PLAN_FIRST_X2
+#define SHKV_PLAN_FIRST_X2 10    // opening split piece
+#endif
+#ifndef SHKV_PLAN_LAST_X2
+#define SHKV_PLAN_LAST_X2 40     // closing split piece
+#endif
+PlanCosts plan_costs(bool umma, int32_t page_size, int32_t rows)
+{
+    if (umma) {
+        const int64_t r = rows;
+        return {128, SHKV_PLAN_SEG_X2 * r / 2, SHKV_PLAN_FIRST_X2 * r / 2, SHKV_PLAN_LAST_X2 * r / 2};
+    }
+    return {page_size < kStageTokens ? page_size : kStageTokens, (int64_t)kSegmentCostChunks * page_size, 0, 0};
+}
+
 // The split plan, shared by the plan query and the decode launch so both
 // describe the same work division.  Chunks are (request, head, page) triples
-// in request-major order; W = Hkv * sum_b ceil(L_b / P).  Each (request,
-// head) unit costs its pages plus kSegmentCostChunks (the fixed work of
-// starting and finishing a segment), and the weighted sequence is cut into
-// `num_ctas` equal parts.  Cuts are then made strictly increasing so every
-// CTA owns at least one chunk.
+// in request-major order; W = Hkv * sum_b ceil(L_b / P).  The chunk sequence
+// is cut into at most `num_ctas` contiguous ranges so that the costliest
+// range (under `k`) is as cheap as the greedy fill below can make it: for a
+// bound B, each CTA takes whole units while it stays within B, then as many
+// whole stages of the next unit as fit with that piece's closing cost; the
+// smallest B for which the fill needs no more than num_ctas CTAs is found by
+// bisection (it lies within one unit's fixed costs and a stage of the mean).
+// Every range owns at least one chunk; fewer than num_ctas ranges can
+// result, and num_ctas is then lowered to match.
 //   prefix     [batch + 1] pages before each request
 //   last_fill  [batch] tokens in each request's last page (nullable)
 //   cuts       [num_ctas + 1] first chunk of each CTA, cuts[num_ctas] = W
-shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv, int32_t max_ctas,
-                       int32_t *prefix, uint8_t *last_fill, int32_t *cuts, int64_t *total_chunks,
-                       int32_t *num_ctas, bool allow_empty = false)
+shkv_status build_plan_uncached(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv,
+                                int32_t max_ctas, const PlanCosts &k, int32_t *prefix, uint8_t *last_fill,
+                                int32_t *cuts, int64_t *total_chunks, int32_t *num_ctas, bool allow_empty)
 {
     if (batch < 1 || batch > SHKV_MAX_BATCH || !lens || page_size <= 0 || page_size > 255 || hkv <= 0 ||
         max_ctas <= 0)
         return SHKV_ERR_INVALID_ARG;
     prefix[0] = 0;
-    int64_t nonempty = 0;
     for (int b = 0; b < batch; ++b) {
         if (lens[b] < (allow_empty ? 0 : 1))
             return SHKV_ERR_INVALID_ARG;
@@ -154,7 +197,6 @@ shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, in
         if (next * hkv > INT32_MAX)
             return SHKV_ERR_UNSUPPORTED;
         prefix[b + 1] = (int32_t)next;
-        nonempty += pages > 0;
         if (last_fill)
             last_fill[b] = (uint8_t)(pages > 0 ? lens[b] - (pages - 1) * page_size : 0);
     }
@@ -166,55 +208,154 @@ shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, in
         C = kMaxCtas;
     if (C < 1)
         C = 1;
-
-    const int64_t alpha = kSegmentCostChunks;
-    const int64_t T = W + alpha * nonempty * hkv;
-    int64_t c = 1, cw = 0, cb = 0;   // next cut, weight and chunks before the current unit
-    for (int b = 0; b < batch && c < C; ++b) {
-        const int64_t pg = prefix[b + 1] - prefix[b];
-        if (pg == 0)
-            continue;                // an empty request owns no chunks and costs nothing
-        for (int g = 0; g < hkv && c < C; ++g) {
-            const int64_t wu = pg + alpha;
-            while (c < C) {
-                const int64_t target = c * T / C;
-                if (target >= cw + wu)
-                    break;
-                const int64_t o = target - cw - alpha;
-                cuts[c] = (int32_t)(cb + (o > 0 ? o : 0));
-                ++c;
-            }
-            cw += wu;
-            cb += pg;
-        }
-    }
-    for (; c < C; ++c)
-        cuts[c] = (int32_t)W;
     cuts[0] = 0;
-    cuts[C] = (int32_t)W;
-    for (int64_t i = 1; i < C; ++i)
-        if (cuts[i] <= cuts[i - 1])
-            cuts[i] = cuts[i - 1] + 1;
-    for (int64_t i = C - 1; i >= 1; --i)
-        if (cuts[i] >= cuts[i + 1])
-            cuts[i] = cuts[i + 1] - 1;
     *total_chunks = W;
-    *num_ctas = (int32_t)C;
+    if (W == 0) {
+        for (int64_t i = 1; i <= C; ++i)
+            cuts[i] = 0;
+        *num_ctas = (int32_t)C;
+        return SHKV_OK;
+    }
+
+    const int64_t P = page_size;
+    const int64_t rb = k.stage > P ? k.stage / P : 1;           // pages a stage step covers
+    const int64_t step = ceil_div(rb * P, k.stage) * k.stage;    // tokens a step costs
+    auto stages = [&](int64_t pages) { return ceil_div(pages * P, k.stage) * k.stage; };
+    // A unit's rest after s pages, s a whole number of steps: where pages and
+    // stages nest, its stages are the unit's less the s pages.
+    const bool nested = k.stage % P == 0 || P % k.stage == 0;
+
+    // Greedy fill under bound B: the number of ranges it makes (C + 1 once it
+    // needs more than C); with `out`, the cuts as well.  A request's hkv
+    // units cost the same, so whole ones are taken in one step.
+    std::vector<int64_t> unit_cost((size_t)batch);
+    int64_t whole = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t pg = prefix[b + 1] - prefix[b];
+        unit_cost[b] = pg > 0 ? k.seg + stages(pg) : 0;
+        whole += hkv * unit_cost[b];
+    }
+    auto fill = [&](int64_t B, int32_t *out) -> int64_t {
+        int64_t c = 0, acc = 0;                // current range and its cost so far
+        for (int b = 0; b < batch; ++b) {
+            const int64_t uc = unit_cost[b];
+            if (uc == 0)
+                continue;                      // an empty request owns no chunks and costs nothing
+            if (acc + hkv * uc <= B) {         // the whole request fits
+                acc += hkv * uc;
+                continue;
+            }
+            const int64_t pg = prefix[b + 1] - prefix[b];
+            int64_t g = 0, s = 0;              // unit of the request; its pages already given out
+            while (g < hkv) {
+                if (s == 0) {
+                    while (g < hkv && acc + uc <= B) {
+                        acc += uc;
+                        ++g;
+                    }
+                    if (g == hkv)
+                        break;
+                }
+                const int64_t open = k.seg + (s > 0 ? k.first : 0);
+                const int64_t rest = nested ? uc - k.seg - s * P : stages(pg - s);
+                if (acc + open + rest <= B) {  // the rest of a split unit
+                    acc += open + rest;
+                    s = 0;
+                    ++g;
+                    continue;
+                }
+                const int64_t room = B - acc - open - k.last;
+                int64_t m = room > 0 ? room / step : 0;    // whole steps that fit
+                const int64_t max_m = (pg - s - 1) / rb;   // leave a page for the rest
+                if (m > max_m)
+                    m = max_m;
+                if (m == 0 && acc == 0)
+                    return C + 1;              // not even one step fits an empty range
+                if (++c >= C)
+                    return C + 1;
+                if (out)
+                    out[c] = (int32_t)(hkv * prefix[b] + g * pg + s + m * rb);
+                s += m * rb;
+                acc = 0;
+            }
+        }
+        return c + 1;
+    };
+    // The bound lies within a step and a split's fixed costs above the mean;
+    // it is found to within 1/2048 of the mean (at least 16 tokens).
+    const int64_t fixed_max = k.seg + k.first + k.last + step;
+    const int64_t tol = std::max<int64_t>(16, whole / C / 2048);
+    int64_t lo = ceil_div(whole, C) - 1;       // infeasible below the mean
+    int64_t hi = ceil_div(whole, C) + fixed_max;
+    while (fill(hi, nullptr) > C)
+        hi += hi - lo;
+    while (hi - lo > tol) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (fill(mid, nullptr) <= C)
+            hi = mid;
+        else
+            lo = mid;
+    }
+    // Cuts strictly increase: a range that opens inside a unit takes at least
+    // one step of it, and a cut at a unit's start closes a range that holds work.
+    const int64_t used = fill(hi, cuts);
+    cuts[used] = (int32_t)W;
+    *num_ctas = (int32_t)used;
     return SHKV_OK;
 }
 
-// CTA whose range [cuts[c], cuts[c+1]) holds chunk idx.
-int32_t cta_of_host(const int32_t *cuts, int32_t C, int64_t idx)
+// build_plan_uncached behind a one-entry cache per host thread: a call that
+// repeats the previous call's inputs exactly (every layer of a model decodes
+// the same lengths in a step) copies its plan instead of making it again.
+shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, int32_t hkv, int32_t max_ctas,
+                       const PlanCosts &k, int32_t *prefix, uint8_t *last_fill, int32_t *cuts,
+                       int64_t *total_chunks, int32_t *num_ctas, bool allow_empty = false)
 {
-    int32_t lo = 0, hi = C;
-    while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) / 2;
-        if (cuts[mid] <= idx)
-            lo = mid;
-        else
-            hi = mid;
+    struct Entry {
+        bool valid = false, allow_empty = false;
+        int32_t batch = 0, page_size = 0, hkv = 0, max_ctas = 0, num_ctas = 0;
+        int64_t stage = 0, seg = 0, first = 0, last = 0, total = 0;
+        std::vector<int32_t> lens, prefix, cuts;
+        std::vector<uint8_t> last_fill;
+    };
+    thread_local Entry e;
+    if (e.valid && lens && batch == e.batch && page_size == e.page_size && hkv == e.hkv &&
+        max_ctas == e.max_ctas && allow_empty == e.allow_empty && k.stage == e.stage && k.seg == e.seg &&
+        k.first == e.first && k.last == e.last && memcmp(lens, e.lens.data(), sizeof(int32_t) * batch) == 0) {
+        memcpy(prefix, e.prefix.data(), sizeof(int32_t) * (batch + 1));
+        if (last_fill)
+            memcpy(last_fill, e.last_fill.data(), batch);
+        memcpy(cuts, e.cuts.data(), sizeof(int32_t) * (e.num_ctas + 1));
+        *total_chunks = e.total;
+        *num_ctas = e.num_ctas;
+        return SHKV_OK;
     }
-    return lo;
+    e.valid = false;
+    if (batch >= 1 && batch <= SHKV_MAX_BATCH)
+        e.last_fill.resize((size_t)batch);
+    const shkv_status st = build_plan_uncached(batch, lens, page_size, hkv, max_ctas, k, prefix,
+                                               batch >= 1 && batch <= SHKV_MAX_BATCH ? e.last_fill.data() : nullptr,
+                                               cuts, total_chunks, num_ctas, allow_empty);
+    if (st != SHKV_OK)
+        return st;
+    if (last_fill)
+        memcpy(last_fill, e.last_fill.data(), batch);
+    e.lens.assign(lens, lens + batch);
+    e.prefix.assign(prefix, prefix + batch + 1);
+    e.cuts.assign(cuts, cuts + *num_ctas + 1);
+    e.batch = batch;
+    e.page_size = page_size;
+    e.hkv = hkv;
+    e.max_ctas = max_ctas;
+    e.allow_empty = allow_empty;
+    e.stage = k.stage;
+    e.seg = k.seg;
+    e.first = k.first;
+    e.last = k.last;
+    e.total = *total_chunks;
+    e.num_ctas = *num_ctas;
+    e.valid = true;
+    return SHKV_OK;
 }
 
 size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms)
@@ -476,17 +617,17 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     if (workspace_bytes < workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim, pool->num_sms))
         return SHKV_ERR_INVALID_ARG;
 
+    const bool use_umma = use_umma_consumer(rows, c.head_dim, pool->consumer);
     DecodeParams p;
     memset(&p, 0, sizeof p);
     shkv_status st = build_plan(batch, fu ? fu->unit_tokens : pool->lens.data(), c.page_size, c.num_kv_heads,
-                                pool->num_sms, p.page_prefix, p.last_fill, p.cta_cut, &p.total_chunks, &p.num_ctas,
-                                pool->tails_view);
+                                pool->num_sms, plan_costs(use_umma, c.page_size, rows), p.page_prefix, p.last_fill,
+                                p.cta_cut, &p.total_chunks, &p.num_ctas, pool->tails_view);
     if (st != SHKV_OK)
         return st;
     if (p.total_chunks == 0)
         return SHKV_OK;
 
-    const bool use_umma = use_umma_consumer(rows, c.head_dim, pool->consumer);
     const DecodeShape sh = decode_shape(rows);
     const int ncw = sh.nrg * sh.wt;
     const int nreg = (c.head_dim / 16) * sh.nt * 4;
@@ -826,15 +967,21 @@ shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags)
 }
 
 shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t page_size, int32_t num_kv_heads,
-                             int32_t max_ctas, int64_t *cta_begin, int32_t *num_ctas, int32_t *num_splits)
+                             int32_t n_models, int32_t hq_per_model, int32_t consumer, int32_t max_ctas,
+                             int64_t *cta_begin, int32_t *num_ctas, int32_t *num_splits)
 {
-    if (!num_ctas)
+    if (!num_ctas || (consumer != SHKV_CONSUMER_MMA_SYNC && consumer != SHKV_CONSUMER_TCGEN05) || n_models < 1 ||
+        hq_per_model < 1 || num_kv_heads < 1)
         return SHKV_ERR_INVALID_ARG;
+    if (hq_per_model % num_kv_heads || n_models * (int64_t)(hq_per_model / num_kv_heads) > 64)
+        return SHKV_ERR_UNSUPPORTED;
+    const int32_t rows = n_models * (hq_per_model / num_kv_heads);
     std::vector<int32_t> prefix((size_t)SHKV_MAX_BATCH + 1);
     std::vector<int32_t> cuts((size_t)kMaxCtas + 1);
     int64_t W = 0;
     int32_t C = 0;
-    shkv_status st = build_plan(batch, seq_lens, page_size, num_kv_heads, max_ctas, prefix.data(), nullptr,
+    shkv_status st = build_plan(batch, seq_lens, page_size, num_kv_heads, max_ctas,
+                                plan_costs(consumer == SHKV_CONSUMER_TCGEN05, page_size, rows), prefix.data(), nullptr,
                                 cuts.data(), &W, &C);
     if (st != SHKV_OK)
         return st;
@@ -843,12 +990,16 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
         for (int c = 0; c <= C; ++c)
             cta_begin[c] = cuts[c];
     if (num_splits) {
-        int32_t n = 0;
+        // one pass over units and cuts together: with cuts[c] <= u0 < cuts[c + 1],
+        // the unit [u0, u1) is split iff cuts[c + 1] < u1
+        int32_t n = 0, c = 0;
         for (int b = 0; b < batch; ++b) {
             const int64_t pages = prefix[b + 1] - prefix[b];
-            for (int g = 0; g < num_kv_heads; ++g) {
+            for (int g = 0; g < num_kv_heads && pages > 0; ++g) {
                 const int64_t u0 = (int64_t)num_kv_heads * prefix[b] + g * pages;
-                if (cta_of_host(cuts.data(), C, u0) != cta_of_host(cuts.data(), C, u0 + pages - 1))
+                while (c + 1 < C && cuts[c + 1] <= u0)
+                    ++c;
+                if (c + 1 < C && cuts[c + 1] < u0 + pages)
                     ++n;
             }
         }

@@ -385,18 +385,31 @@ shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags);
  * Host-only view of how shkv_decode_attention divides work (no device
  * needed).  The (request, KV head, page) chunks, ordered request-major, are
  * cut into `num_ctas` contiguous, non-empty ranges, one per persistent CTA,
- * of equal cost where a range costs its chunks plus a fixed amount per
- * (request, head) it touches; a (request, head) whose pages straddle a cut
- * is split and merged by log-sum-exp.
- *   seq_lens    host int32 [batch] (each >= 1)
- *   max_ctas    upper bound on CTAs (normally the SM count)
- *   cta_begin   host int64 [max_ctas + 1] or NULL; receives the first chunk
- *               of every CTA and, at [num_ctas], the total chunk count
- *   num_ctas    receives the CTA count used
- *   num_splits  receives the number of (request, head) units that are split
+ * of equal estimated cost for the consumer that runs them; a (request, head)
+ * whose pages straddle a cut is split and merged by log-sum-exp.  Cost, in
+ * tokens of one KV head streamed: each (request, head) pays its ring stages
+ * whole (128 tokens on tcgen05, min(page_size, 32) on mma.sync) plus a fixed
+ * amount; on tcgen05 a cut inside a (request, head) adds the second piece's
+ * segment work and both pieces' partials and merge, and the fixed amounts
+ * grow with the stacked rows n_models * hq_per_model / num_kv_heads.
+ *   seq_lens      host int32 [batch] (each >= 1)
+ *   n_models, hq_per_model   as in shkv_decode_attention
+ *   consumer      SHKV_CONSUMER_MMA_SYNC or SHKV_CONSUMER_TCGEN05: the kernel
+ *                 the plan is for (shkv_decode_consumer names the one a pool
+ *                 would run)
+ *   max_ctas      upper bound on CTAs (normally the SM count)
+ *   cta_begin     host int64 [max_ctas + 1] or NULL; receives the first
+ *                 chunk of every CTA and, at [num_ctas], the total chunk count
+ *   num_ctas      receives the CTA count used
+ *   num_splits    receives the number of (request, head) units that are split
+ * Errors: SHKV_ERR_INVALID_ARG (null num_ctas, unknown consumer, counts < 1,
+ * batch above SHKV_MAX_BATCH, a length < 1, page_size above 255),
+ * SHKV_ERR_UNSUPPORTED (hq_per_model % num_kv_heads != 0, more than 64 rows
+ * per KV head, more than INT32_MAX chunks).
  */
 shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t page_size,
-                             int32_t num_kv_heads, int32_t max_ctas, int64_t *cta_begin,
+                             int32_t num_kv_heads, int32_t n_models, int32_t hq_per_model,
+                             int32_t consumer, int32_t max_ctas, int64_t *cta_begin,
                              int32_t *num_ctas, int32_t *num_splits);
 
 /*

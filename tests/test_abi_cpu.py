@@ -52,48 +52,118 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.shkv_decode_attention_noalloc(None, 1, 1, 1, None, 1.0, None, None, None) == N.SHKV_ERR_INVALID_ARG
 
 
-SEGMENT_COST = 16  # chunks charged per (request, head) segment by the planner
+def plan_costs(consumer, P, rows):
+    """The cost model the header documents for shkv_plan_decode, in tokens:
+    (stage, per piece, extra for an opening split piece, extra for a closing
+    split piece)."""
+    if consumer == N.SHKV_CONSUMER_TCGEN05:
+        return 128, 12 * rows, 5 * rows, 20 * rows
+    return min(P, 32), 16 * P, 0, 0
 
 
-@pytest.mark.parametrize("lens,P,H,C", [
-    ([256], 16, 2, 152),                       # tiny
-    ([1, 2, 3, 4000, 17], 16, 8, 152),
-    ([131584] * 4, 16, 8, 152),                # long context: every unit split
-    (list(range(1, 300)), 32, 8, 152),
-    ([5], 16, 1, 152),                         # fewer chunks than CTAs
-    ([512] * 40 + [32768] * 3, 16, 8, 152),    # many short requests next to long ones
-    ([1 + (37 * i) % 96 for i in range(1024)], 16, 8, 152),   # the largest batch, ragged
-    ([1] * 1024, 32, 2, 152),                  # the largest batch, one token each
+def range_costs(begin, lens, P, H, costs):
+    """Brute force: each range's cost, piece by piece (stage grid from the
+    piece's first page)."""
+    stage, seg, first, last = costs
+    units, off = [], 0
+    for l in lens:
+        pg = -(-l // P)
+        for _ in range(H):
+            units.append((off, off + pg))
+            off += pg
+    out = []
+    for c in range(len(begin) - 1):
+        a, b = int(begin[c]), int(begin[c + 1])
+        t = 0
+        for u0, u1 in units:
+            lo, hi = max(a, u0), min(b, u1)
+            if lo < hi:
+                t += -(-(hi - lo) * P // stage) * stage + seg + (first if lo > u0 else 0) + (last if hi < u1 else 0)
+        out.append(t)
+    return np.array(out), units
+
+
+@pytest.mark.parametrize("consumer", [N.SHKV_CONSUMER_MMA_SYNC, N.SHKV_CONSUMER_TCGEN05])
+@pytest.mark.parametrize("lens,P,H,NM,HQ,C", [
+    ([256], 16, 2, 2, 16, 152),                        # tiny
+    ([1, 2, 3, 4000, 17], 16, 8, 4, 32, 152),
+    ([131584] * 4, 16, 8, 8, 16, 152),                 # long context: every unit split
+    (list(range(1, 300)), 32, 8, 8, 40, 152),
+    ([5], 16, 1, 1, 16, 152),                          # fewer chunks than CTAs
+    ([512] * 40 + [32768] * 3, 16, 8, 4, 32, 152),     # many short requests next to long ones
+    ([1 + (37 * i) % 96 for i in range(1024)], 16, 8, 2, 32, 152),   # the largest batch, ragged
+    ([1] * 1024, 32, 2, 1, 32, 152),                   # the largest batch, one token each
+    ([70000, 3, 9000, 1, 65536], 64, 4, 2, 16, 7),     # pages larger than a stage, few CTAs
 ])
-def test_plan_covers_every_chunk_with_balanced_cost(lib, lens, P, H, C):
-    begin, nc, ns = N.shkv_plan_decode(lens, P, H, C)
+def test_plan_covers_every_chunk_with_balanced_cost(lib, consumer, lens, P, H, NM, HQ, C):
+    begin, nc, ns = N.shkv_plan_decode(lens, P, H, NM, HQ, consumer, C)
     pages = [(l + P - 1) // P for l in lens]
     W = H * sum(pages)
-    assert begin[0] == 0 and begin[-1] == W
-    sizes = np.diff(begin)
-    assert (sizes >= 1).all()                                   # every CTA owns work
-    assert nc <= C and nc == min(C, max(1, -(-W // 8)))
-    # brute force: segments per CTA and units straddling a cut
-    units = []
-    off = 0
-    for p_ in pages:
-        for _ in range(H):
-            units.append((off, off + p_))
-            off += p_
+    assert begin[0] == 0 and begin[-1] == W and len(begin) == nc + 1
+    assert (np.diff(begin) >= 1).all()                          # every CTA owns work
+    c_max = min(C, max(1, -(-W // 8)))
+    assert 1 <= nc <= c_max
+    costs = plan_costs(consumer, P, NM * HQ // H)
+    cost, units = range_costs(begin, lens, P, H, costs)
     cuts = begin.tolist()
     n_split = sum(1 for u0, u1 in units if any(u0 < c < u1 for c in cuts[1:-1]))
     assert ns == n_split and ns <= nc - 1
-    cost = []
-    for c in range(nc):
-        a, b = cuts[c], cuts[c + 1]
-        segs = sum(1 for u0, u1 in units if u0 < b and u1 > a)
-        cost.append((b - a) + SEGMENT_COST * segs)
-    target = (W + SEGMENT_COST * len(units)) / nc
-    assert max(cost) <= target + 3 * SEGMENT_COST + 2, (max(cost), target)
+    # the bisection's bound: within a stage step and one split's fixed costs
+    # of the mean over c_max ranges, to its tolerance
+    stage, seg, first, last = costs
+    step = -(-max(1, stage // P) * P // stage) * stage
+    whole = H * sum(seg + -(-pg * P // stage) * stage for pg in pages)
+    tol = max(16, whole // c_max // 2048)
+    assert cost.max() <= -(-whole // c_max) + seg + first + last + step + tol, (cost.max(), whole / c_max)
 
 
-def test_plan_rejects_empty_requests_and_oversized_batches(lib):
-    with pytest.raises(N.ShkvError):
-        N.shkv_plan_decode([3, 0, 5], 16, 2, 152)
-    with pytest.raises(N.ShkvError):
-        N.shkv_plan_decode([1] * (N.SHKV_MAX_BATCH + 1), 16, 2, 152)
+def test_plan_cuts_on_the_stage_grid_of_each_piece(lib):
+    """tcgen05 plan: a cut inside a (request, head) leaves the piece before it
+    a whole number of 128-token stages, counted from the piece's first page."""
+    lens = [131584] * 4 + [5000, 77, 3000]
+    P, H = 16, 8
+    begin, nc, ns = N.shkv_plan_decode(lens, P, H, 8, 16, N.SHKV_CONSUMER_TCGEN05, 152)
+    assert ns >= 32                                  # every long unit is cut, many times over
+    _, units = range_costs(begin, lens, P, H, plan_costs(N.SHKV_CONSUMER_TCGEN05, P, 16))
+    cuts = begin.tolist()
+    for u0, u1 in units:
+        inner = [c for c in cuts[1:-1] if u0 < c < u1]
+        for a, b in zip([u0] + inner, inner):
+            assert (b - a) % (128 // P) == 0
+
+
+def test_plan_is_repeatable_and_follows_its_inputs(lib):
+    """Equal inputs give equal plans (the host keeps each thread's last plan
+    and reuses it only for identical inputs); another consumer or one more
+    page re-plans."""
+    lens = [int(x) for x in np.random.default_rng(5).integers(1, 9000, 64)]
+    T, M = N.SHKV_CONSUMER_TCGEN05, N.SHKV_CONSUMER_MMA_SYNC
+    a = N.shkv_plan_decode(lens, 16, 8, 4, 32, T, 152)
+    b = N.shkv_plan_decode(lens, 16, 8, 4, 32, T, 152)
+    assert np.array_equal(a[0], b[0]) and a[1:] == b[1:]
+    m = N.shkv_plan_decode(lens, 16, 8, 4, 32, M, 152)
+    assert not np.array_equal(a[0], m[0])
+    lens2 = list(lens)
+    lens2[7] = (lens2[7] + 15) // 16 * 16 + 1        # one more page for one request
+    c = N.shkv_plan_decode(lens2, 16, 8, 4, 32, T, 152)
+    assert c[0][-1] == a[0][-1] + 8
+    d = N.shkv_plan_decode(lens, 16, 8, 4, 32, T, 152)
+    assert np.array_equal(a[0], d[0]) and a[1:] == d[1:]
+
+
+def test_plan_rejects_bad_arguments(lib):
+    T = N.SHKV_CONSUMER_TCGEN05
+    for args, status in [
+        (([3, 0, 5], 16, 2, 1, 2, T, 152), N.SHKV_ERR_INVALID_ARG),                 # an empty request
+        (([1] * (N.SHKV_MAX_BATCH + 1), 16, 2, 1, 2, T, 152), N.SHKV_ERR_INVALID_ARG),
+        (([5], 16, 2, 1, 2, 7, 152), N.SHKV_ERR_INVALID_ARG),                      # unknown consumer
+        (([5], 16, 2, 1, 2, N.SHKV_CONSUMER_AUTO, 152), N.SHKV_ERR_INVALID_ARG),   # AUTO needs a pool
+        (([5], 16, 2, 0, 2, T, 152), N.SHKV_ERR_INVALID_ARG),                      # no decoders
+        (([5], 16, 2, 1, 2, T, 0), N.SHKV_ERR_INVALID_ARG),                        # no CTAs
+        (([5], 256, 2, 1, 2, T, 152), N.SHKV_ERR_INVALID_ARG),                     # page_size above 255
+        (([5], 16, 2, 1, 3, T, 152), N.SHKV_ERR_UNSUPPORTED),                      # hq % hkv
+        (([5], 16, 2, 9, 16, T, 152), N.SHKV_ERR_UNSUPPORTED),                     # 72 rows per KV head
+    ]:
+        with pytest.raises(N.ShkvError) as e:
+            N.shkv_plan_decode(*args)
+        assert e.value.status == status, args
