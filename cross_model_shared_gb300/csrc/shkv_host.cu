@@ -143,12 +143,11 @@ struct PlanCosts {
 
 // tcgen05 consumer: the segment epilogue and the split merge handle one
 // output row per stacked query row, so those costs grow with the rows; per
-// row, in tokens: segment 12, opening piece 5, closing piece 20 (the first
-// two fitted to per-CTA exit times on GB300 at 16 rows and 16-token pages,
-// which put the closing piece at 11.5; 20 measured as fast or faster on
-// every workload, 0.5x and 1.5x of all three slower).  mma.sync consumer:
-// SHKV_SEGMENT_COST_CHUNKS pages a piece, nothing for a split (the values
-// its sweep settled on).
+// row, in tokens: segment 12, opening piece 5, closing piece 28 (fitted to
+// per-CTA exit times on GB300 at 16 rows and 16-token pages, then swept:
+// closing piece 11.5 / 20 / 28 per row, opening 5 / 8 / 12, and all three
+// at 0.5x and 1.5x).  mma.sync consumer: SHKV_SEGMENT_COST_CHUNKS pages a
+// piece, nothing for a split (charging splits measured slower).
 #ifndef SHKV_PLAN_SEG_X2
 #define SHKV_PLAN_SEG_X2 24      // twice the tokens per row: segment
 #endif
@@ -156,7 +155,7 @@ struct PlanCosts {
 #define SHKV_PLAN_FIRST_X2 10    // opening split piece
 #endif
 #ifndef SHKV_PLAN_LAST_X2
-#define SHKV_PLAN_LAST_X2 40     // closing split piece
+#define SHKV_PLAN_LAST_X2 56     // closing split piece
 #endif
 PlanCosts plan_costs(bool umma, int32_t page_size, int32_t rows)
 {
@@ -164,7 +163,14 @@ PlanCosts plan_costs(bool umma, int32_t page_size, int32_t rows)
         const int64_t r = rows;
         return {128, SHKV_PLAN_SEG_X2 * r / 2, SHKV_PLAN_FIRST_X2 * r / 2, SHKV_PLAN_LAST_X2 * r / 2};
     }
-    return {page_size < kStageTokens ? page_size : kStageTokens, (int64_t)kSegmentCostChunks * page_size, 0, 0};
+#ifndef SHKV_PLAN_MMA_FIRST
+#define SHKV_PLAN_MMA_FIRST 0    // pages: opening split piece
+#endif
+#ifndef SHKV_PLAN_MMA_LAST
+#define SHKV_PLAN_MMA_LAST 0     // pages: closing split piece
+#endif
+    return {page_size < kStageTokens ? page_size : kStageTokens, (int64_t)kSegmentCostChunks * page_size,
+            (int64_t)SHKV_PLAN_MMA_FIRST * page_size, (int64_t)SHKV_PLAN_MMA_LAST * page_size};
 }
 
 // The split plan, shared by the plan query and the decode launch so both

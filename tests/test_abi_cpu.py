@@ -57,7 +57,7 @@ def plan_costs(consumer, P, rows):
     (stage, per piece, extra for an opening split piece, extra for a closing
     split piece)."""
     if consumer == N.SHKV_CONSUMER_TCGEN05:
-        return 128, 12 * rows, 5 * rows, 20 * rows
+        return 128, 12 * rows, 5 * rows, 28 * rows
     return min(P, 32), 16 * P, 0, 0
 
 
