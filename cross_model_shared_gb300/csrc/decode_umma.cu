@@ -85,32 +85,43 @@ static_assert(kD == 32 * kTokenGroups, "one softmax thread per column of O^T and
 __host__ __device__ constexpr int tc_nr(int rows) { return (rows + 15) / 16 * 16; }
 // N of the PV MMA: 48 is rounded up to a whole 64-column swizzle span.
 __host__ __device__ constexpr int tc_npv(int nr) { return nr == 48 ? 64 : nr; }
+// At 16 padded rows P^T has a buffer of its own (room for it beside a 3-slot
+// ring exists only there), so a slot's K half is free once its QK product
+// has completed and is refilled then, a PV product earlier than its V half.
+__host__ __device__ constexpr bool tc_sep_p(int nr) { return nr == 16; }
+// Entries of the validity-word ring when the K half is released early: the K
+// producer runs at most 5 stages ahead of the softmax (3 K slots past the
+// QK product, which is at most 2 S buffers past the softmax).
+constexpr int kMetaRing = 8;
 
 struct TcSmem {
     uint32_t ring, stage_bytes, qtile, qhalf, qbuf, qbuf_bytes, scr, rowoff, bars, meta, misc, tslot, total;
 };
 
 // Ring of `stages` slots of [K | V][half][128 tokens][128 B] (both 128-byte
-// swizzled), the Q tile [half][NR rows][128 B] (swizzled, K-major), one
-// staging buffer of the next segment's query rows, the cross-warp scratch
-// and the row-offset table, then the barriers.
-__host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages)
+// swizzled), with tc_sep_p the P^T buffer [128 tokens][128 B] (swizzled, as
+// P^T over a K tile's first half), the Q tile [half][NR rows][128 B]
+// (swizzled, K-major), one staging buffer of the next segment's query rows,
+// the cross-warp scratch and the row-offset table, then the barriers and
+// the validity words.
+__host__ __device__ inline TcSmem tc_smem_layout(int rows, int stages, bool sep)
 {
     TcSmem u;
     const int nr = tc_nr(rows);
     u.stage_bytes = (uint32_t)(2 * kTT * kD * 2);
     u.ring = 0;
     u.qhalf = (uint32_t)nr * 128u;
-    u.qtile = u.ring + (uint32_t)stages * u.stage_bytes;
+    u.qtile = u.ring + (uint32_t)stages * u.stage_bytes + (sep ? (uint32_t)(kTT * 128) : 0u);
     u.qbuf = u.qtile + (uint32_t)kHalves * u.qhalf;
     u.qbuf_bytes = align_up((uint32_t)(rows * kD * 2), 128);
     u.scr = u.qbuf + u.qbuf_bytes;
     u.rowoff = u.scr + (uint32_t)(kScrRows * 64 * 4);
     // full_k[stages], empty[stages], p_full[stages], full_v[stages], qfull,
-    // qempty, s_full[2], s_free[2], q_ready, q_tile_free, fin
+    // qempty, s_full[2], s_free[2], q_ready, q_tile_free, fin; with tc_sep_p
+    // also empty_k[stages], meta_full[kMetaRing]
     u.bars = align_up(u.rowoff + 64u * 4u, 8);
-    u.meta = u.bars + (uint32_t)((4 * stages + 9) * 8);
-    u.misc = u.meta + (uint32_t)(stages * kMetaWords * 4);
+    u.meta = u.bars + (uint32_t)((4 * stages + 9 + (sep ? stages + kMetaRing : 0)) * 8);
+    u.misc = u.meta + (uint32_t)((sep ? kMetaRing : stages) * kMetaWords * 4);
     u.tslot = u.misc + 8;
     u.total = u.misc + 16 + 1024;   // + slack to align the base to 1024 bytes
     return u;
@@ -141,9 +152,46 @@ __device__ __forceinline__ uint32_t s_free_b(const TcCtx &c, int b) { return bar
 __device__ __forceinline__ uint32_t q_ready_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 6); }
 __device__ __forceinline__ uint32_t q_tile_free_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 7); }
 __device__ __forceinline__ uint32_t fin_b(const TcCtx &c) { return bar_at(c, 4 * c.stages + 8); }
+// (tc_sep_p) the K half of ring slot s is free: its QK product has completed
+__device__ __forceinline__ uint32_t empty_k_b(const TcCtx &c, int s) { return bar_at(c, 4 * c.stages + 9 + s); }
+// (tc_sep_p) validity-word entry i holds stage k (k % kMetaRing == i)
+__device__ __forceinline__ uint32_t meta_b(const TcCtx &c, int i) { return bar_at(c, 5 * c.stages + 9 + i); }
 __device__ __forceinline__ uint32_t slot_addr(const TcCtx &c, int slot)
 {
     return c.base + c.lay.ring + (uint32_t)slot * c.lay.stage_bytes;
+}
+// Where P^T of a stage lives: over the stage's K tile (half 0), or (kSep)
+// in the P buffer right after the ring.
+template <bool kSep>
+__device__ __forceinline__ uint32_t p_base(const TcCtx &c, uint32_t kst)
+{
+    if constexpr (kSep)
+        return c.lay.ring + (uint32_t)c.stages * c.lay.stage_bytes;
+    else
+        return kst;
+}
+template <bool kSep>
+__device__ __forceinline__ uint32_t p_tile(const TcCtx &c)
+{
+    return c.base + p_base<kSep>(c, c.lay.ring);
+}
+// descriptor offset (bytes >> 4) of K step ks of P^T: `off` for slot-resident P^T
+template <bool kSep>
+__device__ __forceinline__ uint32_t p_off(uint32_t off, int ks)
+{
+    if constexpr (kSep)
+        return (uint32_t)ks * 128u;
+    else
+        return off;
+}
+// Entry of stage k's validity words: its slot, or (kSep) k % kMetaRing.
+template <bool kSep>
+__device__ __forceinline__ int meta_entry(int k, int slot)
+{
+    if constexpr (kSep)
+        return k % kMetaRing;
+    else
+        return slot;
 }
 
 // A softmax thread's rows: 8-row chunks alternate between the two row
@@ -234,7 +282,7 @@ __host__ __device__ constexpr int pow2_at_least(int n) { return n <= 8 ? 8 : n <
 // of each per stage) the K warp copies K, the query rows and the validity
 // word while the V warp copies V; otherwise (8 of each) the K warp issues
 // all of them, K first, and the V warp has nothing to do (measured faster).
-template <bool kIsK>
+template <bool kIsK, bool kSep>
 __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p, const TcCtx &c)
 {
     const int lane = threadIdx.x & 31;
@@ -331,8 +379,15 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                     pinfo[rb] = (uint32_t)__shfl_sync(0xffffffffu, my_info, rb);
             }
             bool ok = true;
-            if (alive)      // every lane polls (measured faster than one lane and a warp barrier)
-                ok = mbar_wait_bounded(empty_b(c, slot), (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
+            if constexpr (kSep && kIsK) {
+                // the K warp of split producers refills a slot's K half once QK freed it
+                if (alive)
+                    ok = mbar_wait_bounded(split ? empty_k_b(c, slot) : empty_b(c, slot),
+                                           (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
+            } else {
+                if (alive)  // every lane polls (measured faster than one lane and a warp barrier)
+                    ok = mbar_wait_bounded(empty_b(c, slot), (uint32_t)(((k / stages) & 1) ^ 1), c.abort_flag, p.err);
+            }
             alive = alive && __all_sync(0xffffffffu, ok);
             const bool my_valid = copier && my_tok < tok_end && my_id >= 0 && my_id < p.num_pages;
             // lanes 0..RB-1 copy page rb = lane (half 0 for K): their ballot is the page mask
@@ -343,7 +398,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                         if (!((mask >> rb) & 1u) && tok0 + rb * P < tok_end)
                             atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
                     volatile uint32_t *meta =
-                        reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta) + slot * kMetaWords;
+                        reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta) + meta_entry<kSep>(k, slot) * kMetaWords;
                     if (fused) {
 #pragma unroll
                         for (int rb = 0; rb < 8; ++rb)
@@ -351,6 +406,8 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                                 meta[1 + rb] = pinfo[rb];
                     }
                     meta[0] = mask | ((uint32_t)k << 8);   // valid pages + stage tag
+                    if constexpr (kSep)
+                        mbar_arrive(meta_b(c, k % kMetaRing));
                     mbar_arrive_expect_tx(full_b(c, slot), (uint32_t)__popc(mask) * page_bytes);
                 }
                 if (!kIsK || !split)
@@ -436,6 +493,7 @@ __device__ void tc_warm_l2(const CUtensorMap *tmK, const CUtensorMap *tmV, const
 template <int NR>
 __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
+    constexpr bool kSep = tc_sep_p(NR);
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_qk = umma_idesc_bf16(128, NR, false, false);
@@ -475,6 +533,8 @@ __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     umma_bf16(d, ak[i], bq[i], idesc_qk, i ? 1u : 0u);
             }
             umma_commit(s_full_b(c, buf));
+            if constexpr (kSep)
+                umma_commit(empty_k_b(c, slot));
             if (j == nst - 1)
                 umma_commit(q_tile_free_b(c));
         }
@@ -489,17 +549,19 @@ __device__ void tc_qk(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     mbar_drain_bounded(fin_b(c), 0u);
 }
 
-// O^T += V^T P^T for each stage; P^T sits over the stage's K tile (half 0).
+// O^T += V^T P^T for each stage; P^T sits over the stage's K tile (half 0),
+// or in the P buffer (sep_p).
 template <int NR>
 __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
+    constexpr bool kSep = tc_sep_p(NR);
     constexpr int NPV = tc_npv(NR);
     const int stages = c.stages;
     const int P = p.page_size;
     const uint32_t idesc_pv = umma_idesc_bf16(128, NPV, true, true);
-    // V^T (A) and P^T (B, over the K tile's first half), both MN-major
+    // V^T (A) and P^T (B, over the K tile's first half or in the P buffer), both MN-major
     const uint64_t vd0 = umma_sdesc_sw128(slot_addr(c, 0) + (uint32_t)(kTT * kD * 2), (uint32_t)(kTT * 128), 1024u);
-    const uint64_t pd0 = umma_sdesc_sw128(slot_addr(c, 0), (uint32_t)(kTT * 128), 1024u);
+    const uint64_t pd0 = umma_sdesc_sw128(p_tile<kSep>(c), (uint32_t)(kTT * 128), 1024u);
     bool alive = true;
     int kbase = 0;
     Segment s = locate(p, c.cta_begin, c.cta_end);
@@ -513,7 +575,7 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             for (int ks = 0; ks < kTT / 16; ++ks) {
                 const uint32_t off = ((uint32_t)slot * c.lay.stage_bytes + (uint32_t)ks * 2048u) >> 4;
                 av[ks] = vd0 + off;
-                bp[ks] = pd0 + off;
+                bp[ks] = pd0 + p_off<kSep>(off, ks);
             }
             if (alive)
                 alive = mbar_wait_bounded(p_full_b(c, slot), (uint32_t)((k / stages) & 1), c.abort_flag, p.err);
@@ -544,6 +606,7 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 template <int NR>
 __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
+    constexpr bool kSep = tc_sep_p(NR);
     constexpr int NH = NR / 2;                 // rows per thread
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -624,9 +687,14 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(s_free_b(c, buf));
-            // the slot's validity word (the QK MMA has already consumed the data)
-            wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
-            const uint32_t tagged = alive ? meta[slot * kMetaWords] : 0u;
+            // the stage's validity word (the QK MMA has already consumed the data);
+            // with sep_p the slot's K barrier may already be a phase further on
+            const int mi = meta_entry<kSep>(k, slot);
+            if constexpr (kSep)
+                wait(meta_b(c, mi), (uint32_t)((k / kMetaRing) & 1));
+            else
+                wait(full_b(c, slot), (uint32_t)((k / stages) & 1));
+            const uint32_t tagged = alive ? meta[mi * kMetaWords] : 0u;
             if (alive && (tagged >> 8) != ((uint32_t)k & 0xffffffu)) {
                 if (lane == 0) {
                     atomicOr(p.err, SHKV_ERRF_PIPELINE);
@@ -636,7 +704,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
             }
             const int tok0 = s.p0 * P + j * kTT;
             // fused tails: this token's page holds info (valid tokens, decoder)
-            const uint32_t tinfo = fused && alive ? meta[slot * kMetaWords + 1 + (t >> log2P)] : (kAllDecoders << 8);
+            const uint32_t tinfo = fused && alive ? meta[mi * kMetaWords + 1 + (t >> log2P)] : (kAllDecoders << 8);
             const uint32_t tdec = (tinfo >> 8) & 0xffu;
             const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) &&
                                (fused ? (uint32_t)(t & (P - 1)) < (tinfo & 0xffu) : (tok0 + t < lim));
@@ -715,8 +783,13 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     lex[i] *= alpha[half_row(hh, i)];
                 }
             }
-            // --- this token's part of P^T, over the stage's K tile (half 0)
-            uint8_t *prow = c.smem + kst + (uint32_t)t * 128u;
+            // --- this token's part of P^T, over the stage's K tile (half 0) or, with
+            // sep_p, in the P buffer once the previous stage's PV has read it
+            if constexpr (kSep) {
+                if (k > 0)
+                    wait(empty_b(c, (k - 1) % stages), (uint32_t)(((k - 1) / stages) & 1));
+            }
+            uint8_t *prow = c.smem + p_base<kSep>(c, kst) + (uint32_t)t * 128u;
 #pragma unroll
             for (int ch = 0; ch < NH / 8; ++ch) {
                 uint32_t hi[4];
@@ -908,7 +981,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         c.base = raw + pad;
     }
     c.stages = p.stages;
-    c.lay = tc_smem_layout(p.rows, p.stages);
+    c.lay = tc_smem_layout(p.rows, p.stages, tc_sep_p(NR));
     c.abort_flag = reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.misc);
     c.bcast = reinterpret_cast<uint32_t *>(c.smem + c.lay.misc + 4);
     c.cta_begin = p.cta_cut[blockIdx.x];
@@ -931,6 +1004,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(q_ready_b(c), kSoftmaxWarps);
         mbar_init(q_tile_free_b(c), 1);
         mbar_init(fin_b(c), 2);                              // one commit per MMA issuer
+        if constexpr (tc_sep_p(NR)) {
+            for (int s = 0; s < c.stages; ++s)
+                mbar_init(empty_k_b(c, s), 1);               // the QK product's commit
+            for (int i = 0; i < kMetaRing; ++i)
+                mbar_init(meta_b(c, i), 1);                  // the K producer
+        }
         *c.abort_flag = 0u;
         *c.bcast = 0u;
         fence_barrier_init();
@@ -960,9 +1039,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait_prior();                       // global memory only from here on
 
     if (warp == kProducerWarp)
-        tc_producer<true>(&tmK, &tmV, p, c);
+        tc_producer<true, tc_sep_p(NR)>(&tmK, &tmV, p, c);
     else if (warp == kVProducerWarp)
-        tc_producer<false>(&tmK, &tmV, p, c);
+        tc_producer<false, tc_sep_p(NR)>(&tmK, &tmV, p, c);
     else if (warp == kQkWarp) {
         if ((threadIdx.x & 31) == 0)
             tc_qk<NR>(p, c, tmem);
@@ -986,12 +1065,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 int umma_stages(int rows)
 {
     int st = kTcMaxStages;
-    while (st >= 2 && tc_smem_layout(rows, st).total > (uint32_t)kSmemLimit)
+    while (st >= 2 && tc_smem_layout(rows, st, tc_sep_p(tc_nr(rows))).total > (uint32_t)kSmemLimit)
         --st;
     return st >= 2 ? st : 0;
 }
 
-uint32_t umma_smem_bytes(int rows, int stages) { return tc_smem_layout(rows, stages).total; }
+uint32_t umma_smem_bytes(int rows, int stages) { return tc_smem_layout(rows, stages, tc_sep_p(tc_nr(rows))).total; }
 
 template <int NR>
 static cudaError_t launch_umma_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
