@@ -157,8 +157,25 @@ struct PlanCosts {
 #ifndef SHKV_PLAN_LAST_X2
 #define SHKV_PLAN_LAST_X2 56     // closing split piece
 #endif
+// At 16 rows the K half of a slot is refilled right after QK, so the next
+// segment streams during a segment's epilogue: cheaper pieces (refitted on
+// that kernel's exit times: 7, 4 and 23 tokens a row; swept against 12/5/28,
+// 6/3/20, 8/4/28 and 5/4/23).
+#ifndef SHKV_PLAN16_SEG_X2
+#define SHKV_PLAN16_SEG_X2 14
+#endif
+#ifndef SHKV_PLAN16_FIRST_X2
+#define SHKV_PLAN16_FIRST_X2 8
+#endif
+#ifndef SHKV_PLAN16_LAST_X2
+#define SHKV_PLAN16_LAST_X2 46
+#endif
 PlanCosts plan_costs(bool umma, int32_t page_size, int32_t rows)
 {
+    if (umma && rows <= 16) {
+        const int64_t r = rows;
+        return {128, SHKV_PLAN16_SEG_X2 * r / 2, SHKV_PLAN16_FIRST_X2 * r / 2, SHKV_PLAN16_LAST_X2 * r / 2};
+    }
     if (umma) {
         const int64_t r = rows;
         return {128, SHKV_PLAN_SEG_X2 * r / 2, SHKV_PLAN_FIRST_X2 * r / 2, SHKV_PLAN_LAST_X2 * r / 2};

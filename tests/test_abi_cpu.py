@@ -56,6 +56,8 @@ def plan_costs(consumer, P, rows):
     """The cost model the header documents for shkv_plan_decode, in tokens:
     (stage, per piece, extra for an opening split piece, extra for a closing
     split piece)."""
+    if consumer == N.SHKV_CONSUMER_TCGEN05 and rows <= 16:
+        return 128, 7 * rows, 4 * rows, 23 * rows
     if consumer == N.SHKV_CONSUMER_TCGEN05:
         return 128, 12 * rows, 5 * rows, 28 * rows
     return min(P, 32), 16 * P, 0, 0
