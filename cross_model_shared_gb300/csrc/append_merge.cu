@@ -20,8 +20,8 @@ namespace shkv {
 // after that store).
 __global__ void __launch_bounds__(256) shkv_append_kernel(const __grid_constant__ AppendParams p)
 {
-    pdl_launch_dependents();
     pdl_wait_prior();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int hv = p.head_vecs;                      // 16-byte vectors per head row: 8 or 16
@@ -95,8 +95,8 @@ __global__ void __launch_bounds__(256)
                       const float *__restrict__ lse_part, __nv_bfloat16 *__restrict__ out,
                       float *__restrict__ lse_out)
 {
-    pdl_launch_dependents();
     pdl_wait_prior();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t nrow = (int64_t)batch * rows;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -140,12 +140,18 @@ __global__ void __launch_bounds__(256)
         lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
-// One block per request: its unit of shared pages then each decoder's tail
-// pages, with each page's valid tokens and attending decoder.
-__global__ void __launch_bounds__(256) shkv_tails_unit_kernel(const __grid_constant__ TailsUnitParams p)
+// One warp per request builds its row of the unit table: its shared pages
+// then each decoder's tail pages, with each page's valid tokens and attending
+// decoder.  The warp fits beside a decode CTA on an SM (at most 32 registers,
+// no shared memory), so it runs while the previous kernel still does: it
+// lets the next kernel be scheduled at once, reads the tables through L2
+// only (they were written by work that completed before this kernel could
+// start, see shkv_decode_attention_tails), writes the table buffer that the
+// previous decode does not read, and waits for the previous kernel only at
+// its end, so the decode after it starts only once both have completed.
+__global__ void __maxnreg__(32) shkv_tails_unit_kernel(const __grid_constant__ TailsUnitParams p)
 {
     pdl_launch_dependents();
-    pdl_wait_prior();
     const int b = blockIdx.x;
     const int P = p.page_size;
     const int L = p.shared_len[b];
@@ -153,11 +159,11 @@ __global__ void __launch_bounds__(256) shkv_tails_unit_kernel(const __grid_const
     int U = S;
     for (int m = 0; m < p.n_models; ++m)
         U += (p.tail_len[b * p.n_models + m] + P - 1) / P;
-    for (int j = threadIdx.x; j < U; j += blockDim.x) {
+    for (int j = threadIdx.x; j < U; j += 32) {
         int id, cnt;
         uint32_t dec = kAllDecoders;
         if (j < S) {
-            id = __ldg(p.block_table + (int64_t)b * p.bt_stride + j);
+            id = __ldcg(p.block_table + (int64_t)b * p.bt_stride + j);
             cnt = j == S - 1 ? L - j * P : P;
         } else {
             int jt = j - S, m = 0;
@@ -169,25 +175,26 @@ __global__ void __launch_bounds__(256) shkv_tails_unit_kernel(const __grid_const
             }
             const int T = p.tail_len[b * p.n_models + m];
             const int pages = (T + P - 1) / P;
-            id = __ldg(p.tail_table + ((int64_t)b * p.n_models + m) * p.tt_stride + jt);
+            id = __ldcg(p.tail_table + ((int64_t)b * p.n_models + m) * p.tt_stride + jt);
             cnt = jt == pages - 1 ? T - jt * P : P;
             dec = (uint32_t)m;
         }
         p.unit_table[(int64_t)b * p.ustride + j] = id;
         p.unit_info[(int64_t)b * p.ustride + j] = (uint32_t)cnt | (dec << 8);
     }
+    pdl_wait_prior();
 }
 
 cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream)
 {
-    return launch_pdl(shkv_tails_unit_kernel, p.batch, 256, 0u, stream, p);
+    return launch_pdl(shkv_tails_unit_kernel, p.batch, 32, 0u, stream, p);
 }
 
 // dst[i] = value for i < n (grid-stride).
 __global__ void __launch_bounds__(256) shkv_fill_kernel(float *__restrict__ dst, int64_t n, float value)
 {
-    pdl_launch_dependents();
     pdl_wait_prior();
+    pdl_launch_dependents();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         dst[i] = value;
 }

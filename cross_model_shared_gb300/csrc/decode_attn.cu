@@ -555,7 +555,6 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
                        const __grid_constant__ DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    pdl_launch_dependents();
     Ctx c;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -601,9 +600,11 @@ __global__ void __launch_bounds__(NT == 1 ? kMaxThreadsNT1 : kMaxThreadsNT2, 1)
     if (warp == ncw) {
         warm_l2<D>(&tmK, &tmV, p, c);
         pdl_wait_prior();                   // global memory only from here on
+        pdl_launch_dependents();            // (after the wait: see launch.cuh)
         producer<D, FUSED>(&tmK, &tmV, p, c);
     } else {
         pdl_wait_prior();
+        pdl_launch_dependents();
         if (warp < ncw)
             consumer<D, NT, FUSED>(p, c);
     }

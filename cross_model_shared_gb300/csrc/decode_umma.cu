@@ -972,7 +972,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const __grid_constant__ DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    pdl_launch_dependents();
     TcCtx c;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -1037,6 +1036,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     else if (warp == kVProducerWarp)
         tc_warm_l2<false>(&tmK, &tmV, p, c);
     pdl_wait_prior();                       // global memory only from here on
+    pdl_launch_dependents();                // (after the wait: see launch.cuh)
 
     if (warp == kProducerWarp)
         tc_producer<true, tc_sep_p(NR)>(&tmK, &tmV, p, c);

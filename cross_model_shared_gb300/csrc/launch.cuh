@@ -11,7 +11,12 @@ namespace shkv {
 
 // kern<<<grid, block, smem, stream>>>(args...), allowed to start its CTAs
 // while the previous kernel of the stream is still finishing.  The kernel
-// must call pdl_wait_prior() before it touches global memory.
+// must call pdl_wait_prior() before it touches global memory, and calls
+// pdl_launch_dependents() only after that wait: so once a kernel of this
+// library lets its dependent start, everything before it in the stream has
+// completed.  The per-decoder tails unit kernel relies on this (it is the
+// one exception to the first rule: it reads the page tables before its wait,
+// see shkv_tails_unit_kernel).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, uint32_t smem, cudaStream_t stream,
                        Args &&...args)

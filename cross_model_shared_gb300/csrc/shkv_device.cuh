@@ -176,10 +176,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 }
 
 // Programmatic dependent launch (kernels launched with
-// cudaLaunchAttributeProgrammaticStreamSerialization).  A CTA lets the next
-// kernel of the stream schedule its CTAs as SMs free up, and waits for the
+// cudaLaunchAttributeProgrammaticStreamSerialization).  A CTA waits for the
 // previous kernel to complete, its memory visible, before it touches global
-// memory; both are no-ops without the launch attribute.
+// memory, then lets the next kernel of the stream schedule its CTAs as SMs
+// free up; both are no-ops without the launch attribute.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -614,11 +615,13 @@ struct FusedUnits {
 // request b's unit is fu's row b instead of the pool's block table.  With
 // clear_counters, once every check has passed, the workspace's arrival
 // counters are zeroed on the stream before the launch (for a workspace whose
-// previous contents are unknown).
+// previous contents are unknown).  before_launch, if given, is called once
+// every check has passed, right before the decode kernel is enqueued (the
+// tails path enqueues its unit kernel there); its error aborts the call.
 shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
                         float scale, void *out, float *out_f32, float *lse_out, void *workspace,
                         size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr,
-                        bool clear_counters = false)
+                        bool clear_counters = false, const std::function<cudaError_t()> *before_launch = nullptr)
 {
     if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
         hq_per_model < 1)
@@ -712,6 +715,8 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     p.split_producers = c.page_size < 32 ? 1 : 0;
     if (clear_counters && cudaMemsetAsync(p.ws_count, 0, count_bytes, (cudaStream_t)stream) != cudaSuccess)
         return SHKV_ERR_CUDA;
+    if (before_launch && (*before_launch)() != cudaSuccess)
+        return SHKV_ERR_CUDA;
     cudaError_t e = use_umma ? launch_decode_umma(pool->tm_k2, pool->tm_v2, p, smem_bytes, (cudaStream_t)stream)
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);
@@ -734,9 +739,53 @@ TailsWorkspace tails_workspace(const shkv_pool *pool, const shkv_tails *tails, i
                                             pool->num_sms));
     w.stride = (size_t)c.max_pages_per_seq + (size_t)tails->n_models * tails->max_tail_pages;
     w.table = align256((size_t)batch * w.stride * 4);
-    w.total = w.decode + 2 * w.table;
+    w.total = w.decode + 4 * w.table;          // two buffers of (unit table, page words)
     return w;
 }
+
+// The unit-table buffer (0 or 1) the next tails call on a workspace uses: the
+// calls on one workspace alternate, so a call's unit kernel, which runs
+// while the previous kernel still does, never writes the buffer the previous
+// call's decode reads.  A small table keyed by workspace address, least
+// recently used out; a workspace evicted after 64 others were used since
+// starts again at buffer 0.
+struct UnitBufferTable {
+    struct Entry {
+        const void *ws;
+        uint64_t used;
+        int next;
+    };
+    std::mutex mu;
+    std::vector<Entry> entries;
+    uint64_t clock = 0;
+
+    int next(const void *ws)
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (const Entry &e : entries)
+            if (e.ws == ws)
+                return e.next;
+        return 0;
+    }
+    void used(const void *ws, int buf)
+    {
+        std::lock_guard<std::mutex> g(mu);
+        ++clock;
+        for (Entry &e : entries)
+            if (e.ws == ws) {
+                e.next = buf ^ 1;
+                e.used = clock;
+                return;
+            }
+        if (entries.size() >= 64) {
+            auto lru = std::min_element(entries.begin(), entries.end(),
+                                        [](const Entry &a, const Entry &b) { return a.used < b.used; });
+            entries.erase(lru);
+        }
+        entries.push_back({ws, clock, buf ^ 1});
+    }
+};
+UnitBufferTable g_unit_buffers;
 
 }  // namespace
 
@@ -921,20 +970,32 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
         unit_tokens[b] = (int32_t)(pages * P);
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int buf = g_unit_buffers.next(workspace);
     up.block_table = pool->cfg.block_table;
     up.tail_table = tails->view->cfg.block_table;
-    up.unit_table = reinterpret_cast<int32_t *>(ws + w.decode);
-    up.unit_info = reinterpret_cast<uint32_t *>(ws + w.decode + w.table);
+    up.unit_table = reinterpret_cast<int32_t *>(ws + w.decode + (size_t)(2 * buf) * w.table);
+    up.unit_info = reinterpret_cast<uint32_t *>(ws + w.decode + (size_t)(2 * buf + 1) * w.table);
     up.bt_stride = pool->cfg.max_pages_per_seq;
     up.tt_stride = tails->max_tail_pages;
     up.ustride = (int32_t)w.stride;
     up.batch = batch;
     up.n_models = N;
     up.page_size = P;
-    if (cudaError_t e = launch_tails_units(up, (cudaStream_t)stream); e != cudaSuccess)
-        return SHKV_ERR_CUDA;
+    // the unit kernel is enqueued right before the decode, once every check
+    // of the decode has passed (never alone: see UnitBufferTable)
+    bool launched = false;
+    const std::function<cudaError_t()> units = [&]() {
+        const cudaError_t e = launch_tails_units(up, (cudaStream_t)stream);
+        launched = e == cudaSuccess;
+        return e;
+    };
     const FusedUnits fu{up.unit_table, up.unit_info, up.ustride, unit_tokens.data()};
-    return decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu);
+    const shkv_status st =
+        decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu, false,
+                    &units);
+    if (launched)
+        g_unit_buffers.used(workspace, buf);
+    return st;
 }
 
 shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)

@@ -251,7 +251,16 @@ shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_t
  * unit (its shared pages, then each decoder's tail pages, read from the
  * device block and tail tables with the host copies of the lengths), then
  * the decode kernel streams every unit once for all N*G stacked rows, a tail
- * page being attended by its own decoder's G rows only.  Supported:
+ * page being attended by its own decoder's G rows only.  The layout kernel
+ * runs while the previous kernel of `stream` is still running (one warp per
+ * request, beside that kernel's CTAs), into one of two buffers in
+ * `workspace` that alternate between calls on the same workspace; it reads
+ * the block and tail tables without waiting for that kernel.  So a kernel
+ * enqueued on `stream` before this call that writes those tables must not
+ * let programmatic dependents start (griddepcontrol.launch_dependents /
+ * cudaTriggerProgrammaticLaunchCompletion) before its writes; copies,
+ * kernels launched without programmatic stream serialization and this
+ * library's own kernels are fine.  Supported:
  * batch * n_models <= SHKV_MAX_BATCH, n_models <= 254, rest as
  * shkv_decode_attention.  Errors as shkv_decode_attention (the device copies
  * of the lengths are not compared: SHKV_ERRF_SEQ_LEN is not raised here).
