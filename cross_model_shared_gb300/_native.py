@@ -45,6 +45,7 @@ SHKV_CONSUMER_MMA_SYNC = 0
 SHKV_CONSUMER_TCGEN05 = 1
 
 SHKV_NOALLOC_SCRATCH_BYTES = 8 << 20
+SHKV_COUNT_REGION_BYTES = 1 << 20
 
 
 class shkv_pool_config(ctypes.Structure):

@@ -146,11 +146,14 @@ __global__ void __launch_bounds__(256)
 // no shared memory), so it runs while the previous kernel still does: it
 // lets the next kernel be scheduled at once, reads the tables through L2
 // only (they were written by work that completed before this kernel could
-// start, see shkv_decode_attention_tails), writes the table buffer that the
-// previous decode does not read, and waits for the previous kernel only at
-// its end, so the decode after it starts only once both have completed.
+// start, see shkv_decode_attention_tails), writes tables at a position the
+// previous decode does not read (else, wait_first, it waits at its start),
+// and waits for the previous kernel at its end, so the decode after it starts
+// only once both have completed.
 __global__ void __maxnreg__(32) shkv_tails_unit_kernel(const __grid_constant__ TailsUnitParams p)
 {
+    if (p.wait_first)
+        pdl_wait_prior();       // its table position may be in use by the previous decode
     pdl_launch_dependents();
     const int b = blockIdx.x;
     const int P = p.page_size;

@@ -93,6 +93,11 @@ __host__ __device__ constexpr bool tc_sep_p(int nr) { return nr == 16; }
 // producer runs at most 5 stages ahead of the softmax (3 K slots past the
 // QK product, which is at most 2 S buffers past the softmax).
 constexpr int kMetaRing = 8;
+// Fused tails: the softmax needs each token's page word (valid tokens,
+// attending decoder).  Up to 32 rows it loads the word from the unit's page
+// word table itself, a stage ahead; above, where its registers are short,
+// the K producer publishes a stage's words beside its validity word.
+__host__ __device__ constexpr bool tc_words_by_producer(int nr) { return nr > 32; }
 
 struct TcSmem {
     uint32_t ring, stage_bytes, qtile, qhalf, qbuf, qbuf_bytes, scr, rowoff, bars, meta, misc, tslot, total;
@@ -282,7 +287,7 @@ __host__ __device__ constexpr int pow2_at_least(int n) { return n <= 8 ? 8 : n <
 // of each per stage) the K warp copies K, the query rows and the validity
 // word while the V warp copies V; otherwise (8 of each) the K warp issues
 // all of them, K first, and the V warp has nothing to do (measured faster).
-template <bool kIsK, bool kSep>
+template <bool kIsK, bool kSep, bool kWords>
 __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeParams &p, const TcCtx &c)
 {
     const int lane = threadIdx.x & 31;
@@ -312,10 +317,11 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
     int last_issued_stage = -1;
     int q_issued = -1;
     Segment s = locate(p, c.cta_begin, c.cta_end);
-    const int32_t *info_tab = reinterpret_cast<const int32_t *>(p.page_info);
-    const bool fused = kIsK && p.fused != 0;          // the K warp publishes page_info
     int pre = unit_entry(p.block_table, p, s.b, s.p0 + lane, s.p1);
-    int pre_i = fused ? unit_entry(info_tab, p, s.b, s.p0 + lane, s.p1) : -1;
+    // kWords (fused tails, the K warp): page words, in windows like the ids
+    constexpr bool words = kWords && kIsK;
+    const int32_t *info_tab = reinterpret_cast<const int32_t *>(p.page_info);
+    int pre_i = words ? unit_entry(info_tab, p, s.b, s.p0 + lane, s.p1) : -1;
     for (;;) {
         const bool has_next = s.seg_end < c.cta_end;
         Segment sn;
@@ -323,7 +329,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
         if (has_next) {
             sn = next_segment(p, s, c.cta_end);
             pre_next = unit_entry(p.block_table, p, sn.b, lane, sn.p1);
-            if (fused)
+            if constexpr (words)
                 pre_next_i = unit_entry(info_tab, p, sn.b, lane, sn.p1);
         }
         // (a unit of fused tails is not one sequence: no length to check)
@@ -352,7 +358,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
         int w0 = s.p0;                                   // block-table window [w0, w0+32)
         int cur = pre, cur_i = pre_i;
         int nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
-        int nxt_i = fused ? unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1) : -1;
+        int nxt_i = words ? unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1) : -1;
         for (int j = 0; j < nst; ++j) {
             const int k = kbase + j;
             const int slot = k % stages;
@@ -363,16 +369,16 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                 w0 += 32;
                 cur = nxt;
                 nxt = (w0 + 32 + lane < s.p1) ? __ldg(btrow + w0 + 32 + lane) : -1;
-                if (fused) {
+                if constexpr (words) {
                     cur_i = nxt_i;
                     nxt_i = unit_entry(info_tab, p, s.b, w0 + 32 + lane, s.p1);
                 }
             }
             const int my_tok = tok0 + my_rb * P;
             const int my_id = __shfl_sync(0xffffffffu, cur, ((my_tok >> log2P) - w0) & 31);
-            // page_info of page rb of the stage, gathered to lane 0 (lane rb < RB holds page rb)
+            // (words) page word of page rb of the stage, gathered to lane 0 (lane rb < RB holds page rb)
             uint32_t pinfo[8];
-            if (fused) {
+            if constexpr (words) {
                 const int my_info = __shfl_sync(0xffffffffu, cur_i, ((my_tok >> log2P) - w0) & 31);
 #pragma unroll
                 for (int rb = 0; rb < 8; ++rb)
@@ -399,7 +405,7 @@ __device__ void tc_producer(const CUtensorMap *tmK, const CUtensorMap *tmV, cons
                             atomicOr(p.err, SHKV_ERRF_PAGE_OOB);
                     volatile uint32_t *meta =
                         reinterpret_cast<volatile uint32_t *>(c.smem + c.lay.meta) + meta_entry<kSep>(k, slot) * kMetaWords;
-                    if (fused) {
+                    if constexpr (words) {
 #pragma unroll
                         for (int rb = 0; rb < 8; ++rb)
                             if (rb < RB)
@@ -603,7 +609,7 @@ __device__ void tc_pv(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 // ---------------------------------------------------------------------------
 // Thread (warp w, lane l): token / O^T column t = 32*(w%4) + l, and the
 // stacked rows half_row(w/4, i) for i < NR/2.
-template <int NR>
+template <int NR, bool FUSED>
 __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 {
     constexpr bool kSep = tc_sep_p(NR);
@@ -658,9 +664,20 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
     for (;;) {
         const int tok_end = s.p1 * P;
         const int nst = (tok_end - s.p0 * P + kTT - 1) / kTT;
-        const bool fused = p.fused != 0;
+        constexpr bool fused = FUSED;
         const int L = fused ? tok_end : plan_len(p, s);   // fused tails: valid tokens per page from page_info
         const int lim = L < tok_end ? L : tok_end;
+        // fused tails: this thread's token's page word (valid tokens, decoder)
+        // for stage jj, read through L2 (the unit kernel wrote it) a stage
+        // ahead of its use
+        auto page_word = [&](int jj) -> uint32_t {
+            const int pg = s.p0 + ((jj * kTT + t) >> log2P);
+            return jj < nst && pg < s.p1
+                       ? __ldcg(reinterpret_cast<const uint32_t *>(p.page_info) + (int64_t)s.b * p.max_pages + pg)
+                       : 0u;
+        };
+        constexpr bool own_words = fused && !tc_words_by_producer(NR);
+        uint32_t tinfo_next = own_words ? page_word(0) : (kAllDecoders << 8);
         float m_use[NH], lhi[NH], lex[NH];
 #pragma unroll
         for (int i = 0; i < NH; ++i) {
@@ -703,8 +720,11 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                 alive = false;
             }
             const int tok0 = s.p0 * P + j * kTT;
-            // fused tails: this token's page holds info (valid tokens, decoder)
-            const uint32_t tinfo = fused && alive ? meta[mi * kMetaWords + 1 + (t >> log2P)] : (kAllDecoders << 8);
+            uint32_t tinfo = tinfo_next;
+            if constexpr (own_words)
+                tinfo_next = page_word(j + 1);
+            else if constexpr (fused)
+                tinfo = alive ? meta[mi * kMetaWords + 1 + (t >> log2P)] : (kAllDecoders << 8);
             const uint32_t tdec = (tinfo >> 8) & 0xffu;
             const bool valid = alive && (((tagged & 0xffu) >> (t >> log2P)) & 1u) &&
                                (fused ? (uint32_t)(t & (P - 1)) < (tinfo & 0xffu) : (tok0 + t < lim));
@@ -966,7 +986,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
 
 // 12 warps at one CTA per SM: three warps share a 16K-register SM
 // sub-partition, so at most 168 registers a thread.
-template <int NR>
+template <int NR, bool FUSED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     shkv_decode_umma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ DecodeParams p)
@@ -1039,9 +1059,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_launch_dependents();                // (after the wait: see launch.cuh)
 
     if (warp == kProducerWarp)
-        tc_producer<true, tc_sep_p(NR)>(&tmK, &tmV, p, c);
+        tc_producer<true, tc_sep_p(NR), FUSED && tc_words_by_producer(NR)>(&tmK, &tmV, p, c);
     else if (warp == kVProducerWarp)
-        tc_producer<false, tc_sep_p(NR)>(&tmK, &tmV, p, c);
+        tc_producer<false, tc_sep_p(NR), false>(&tmK, &tmV, p, c);
     else if (warp == kQkWarp) {
         if ((threadIdx.x & 31) == 0)
             tc_qk<NR>(p, c, tmem);
@@ -1049,7 +1069,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if ((threadIdx.x & 31) == 0)
             tc_pv<NR>(p, c, tmem);
     } else
-        tc_softmax<NR>(p, c, tmem);
+        tc_softmax<NR, FUSED>(p, c, tmem);
 
     tc_fence_before();
     __syncthreads();
@@ -1076,7 +1096,7 @@ template <int NR>
 static cudaError_t launch_umma_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                                  uint32_t smem, cudaStream_t stream)
 {
-    auto kern = shkv_decode_umma_kernel<NR>;
+    auto kern = p.fused ? shkv_decode_umma_kernel<NR, true> : shkv_decode_umma_kernel<NR, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;

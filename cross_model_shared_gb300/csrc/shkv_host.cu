@@ -382,12 +382,21 @@ shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, in
     return SHKV_OK;
 }
 
+// A decode's workspace: the arrival counters (one per (request, head) unit)
+// in a region of fixed size at its front, then the split pieces' lse and
+// partials.  The counters of every call, whatever its shape, live in that
+// region and nothing else is ever written there, so a workspace whose region
+// starts zeroed stays zeroed between calls (the last arriver of each unit
+// clears its counter) when consecutive calls change batch or shape.
+constexpr size_t kCountRegion = SHKV_COUNT_REGION_BYTES;
+
 size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms)
 {
-    const size_t count = align_up((uint32_t)(batch * hkv * 4), 256);
+    (void)batch;
+    (void)hkv;
     const size_t lse = align_up((uint32_t)(2 * num_sms * rows * 4), 256);
     const size_t part = (size_t)2 * num_sms * rows * head_dim * 4;
-    return count + lse + part;
+    return kCountRegion + lse + part;
 }
 
 shkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SHKV_OK : SHKV_ERR_CUDA; }
@@ -640,6 +649,8 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     const int rows = n_models * group;
     if (rows > 64)
         return SHKV_ERR_UNSUPPORTED;
+    if ((int64_t)batch * c.num_kv_heads * 4 > (int64_t)kCountRegion)
+        return SHKV_ERR_UNSUPPORTED;
     if (workspace_bytes < workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim, pool->num_sms))
         return SHKV_ERR_INVALID_ARG;
 
@@ -681,7 +692,7 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t count_bytes = align_up((uint32_t)(batch * c.num_kv_heads * 4), 256);
+    const size_t count_bytes = align_up((uint32_t)(batch * c.num_kv_heads * 4), 256);   // in use by this call
     const size_t lse_bytes = align_up((uint32_t)(2 * pool->num_sms * rows * 4), 256);
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.out = static_cast<__nv_bfloat16 *>(out);
@@ -693,8 +704,8 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     p.seq_lens = c.seq_lens;
     p.err = c.error_word;
     p.ws_count = reinterpret_cast<uint32_t *>(ws);
-    p.ws_lse = reinterpret_cast<float *>(ws + count_bytes);
-    p.ws_part = reinterpret_cast<float *>(ws + count_bytes + lse_bytes);
+    p.ws_lse = reinterpret_cast<float *>(ws + kCountRegion);
+    p.ws_part = reinterpret_cast<float *>(ws + kCountRegion + lse_bytes);
     p.batch = batch;
     p.n_models = n_models;
     p.hq = hq_per_model;
@@ -743,49 +754,62 @@ TailsWorkspace tails_workspace(const shkv_pool *pool, const shkv_tails *tails, i
     return w;
 }
 
-// The unit-table buffer (0 or 1) the next tails call on a workspace uses: the
-// calls on one workspace alternate, so a call's unit kernel, which runs
-// while the previous kernel still does, never writes the buffer the previous
-// call's decode reads.  A small table keyed by workspace address, least
-// recently used out; a workspace evicted after 64 others were used since
-// starts again at buffer 0.
-struct UnitBufferTable {
+// What the last decode call on each workspace uses: [0, decode_end) (its
+// counters, lse and partials) and, for a call with per-decoder tails, its unit
+// table and page words [tab_lo, tab_hi).  A tails call's unit kernel runs
+// while the previous kernel of the stream still does, so it writes its
+// tables where the last call on the same workspace keeps nothing: the first
+// of its candidate positions that misses both ranges and fits; when none does
+// (shapes changed), the unit kernel waits for the previous kernel first.  A
+// small table keyed by workspace address, least recently used out after 64
+// others.
+struct WorkspaceUse {
     struct Entry {
         const void *ws;
         uint64_t used;
-        int next;
+        size_t decode_end, tab_lo, tab_hi;
     };
     std::mutex mu;
     std::vector<Entry> entries;
     uint64_t clock = 0;
 
-    int next(const void *ws)
+    // Offset of `bytes` of tables for a call whose decode part takes d bytes
+    // of a workspace of `limit` bytes (d + 2 * bytes <= limit).
+    size_t place(const void *ws, size_t d, size_t bytes, size_t limit, bool *wait_first)
     {
         std::lock_guard<std::mutex> g(mu);
+        *wait_first = false;
         for (const Entry &e : entries)
-            if (e.ws == ws)
-                return e.next;
-        return 0;
+            if (e.ws == ws) {
+                const size_t past = std::max(d, e.decode_end);
+                const size_t cands[] = {d, d + bytes, past, past + bytes, std::max(e.tab_hi, d),
+                                        limit >= bytes ? (limit - bytes) / 256 * 256 : 0};
+                for (size_t c : cands)
+                    if (c >= d && c + bytes <= limit && c >= e.decode_end && (c + bytes <= e.tab_lo || c >= e.tab_hi))
+                        return c;
+                *wait_first = true;
+                return d;
+            }
+        return d;
     }
-    void used(const void *ws, int buf)
+    void used(const void *ws, size_t decode_end, size_t tab_lo, size_t tab_hi)
     {
         std::lock_guard<std::mutex> g(mu);
         ++clock;
         for (Entry &e : entries)
             if (e.ws == ws) {
-                e.next = buf ^ 1;
-                e.used = clock;
+                e = {ws, clock, decode_end, tab_lo, tab_hi};
                 return;
             }
         if (entries.size() >= 64) {
             auto lru = std::min_element(entries.begin(), entries.end(),
-                                        [](const Entry &a, const Entry &b) { return a.used < b.used; });
+                                        [](const Entry &x, const Entry &y) { return x.used < y.used; });
             entries.erase(lru);
         }
-        entries.push_back({ws, clock, buf ^ 1});
+        entries.push_back({ws, clock, decode_end, tab_lo, tab_hi});
     }
 };
-UnitBufferTable g_unit_buffers;
+WorkspaceUse g_workspace_use;
 
 }  // namespace
 
@@ -797,8 +821,16 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
 {
     if (!out)
         return SHKV_ERR_INVALID_ARG;
-    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, workspace,
-                       workspace_bytes, stream);
+    const shkv_status st = decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out,
+                                       workspace, workspace_bytes, stream);
+    if (st == SHKV_OK) {     // the bytes a tails call after this one must leave alone while it runs
+        const int32_t rows = n_models * (hq_per_model / pool->cfg.num_kv_heads);
+        g_workspace_use.used(workspace,
+                             workspace_bytes_for(batch, pool->cfg.num_kv_heads, rows, pool->cfg.head_dim,
+                                                 pool->num_sms),
+                             0, 0);
+    }
+    return st;
 }
 
 shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new, int32_t hq_per_model,
@@ -970,11 +1002,13 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
         unit_tokens[b] = (int32_t)(pages * P);
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int buf = g_unit_buffers.next(workspace);
+    bool wait_first = false;
+    const size_t off = g_workspace_use.place(workspace, w.decode, 2 * w.table, workspace_bytes, &wait_first);
     up.block_table = pool->cfg.block_table;
     up.tail_table = tails->view->cfg.block_table;
-    up.unit_table = reinterpret_cast<int32_t *>(ws + w.decode + (size_t)(2 * buf) * w.table);
-    up.unit_info = reinterpret_cast<uint32_t *>(ws + w.decode + (size_t)(2 * buf + 1) * w.table);
+    up.unit_table = reinterpret_cast<int32_t *>(ws + off);
+    up.unit_info = reinterpret_cast<uint32_t *>(ws + off + w.table);
+    up.wait_first = wait_first ? 1 : 0;
     up.bt_stride = pool->cfg.max_pages_per_seq;
     up.tt_stride = tails->max_tail_pages;
     up.ustride = (int32_t)w.stride;
@@ -982,7 +1016,8 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
     up.n_models = N;
     up.page_size = P;
     // the unit kernel is enqueued right before the decode, once every check
-    // of the decode has passed (never alone: see UnitBufferTable)
+    // of the decode has passed (never alone, so the last tables a workspace
+    // recorded are the ones its last decode reads)
     bool launched = false;
     const std::function<cudaError_t()> units = [&]() {
         const cudaError_t e = launch_tails_units(up, (cudaStream_t)stream);
@@ -994,7 +1029,7 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
         decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu, false,
                     &units);
     if (launched)
-        g_unit_buffers.used(workspace, buf);
+        g_workspace_use.used(workspace, w.decode, off, off + 2 * w.table);
     return st;
 }
 

@@ -18,6 +18,7 @@ struct TailsUnitParams {
     int32_t *unit_table;            // [batch, ustride]
     uint32_t *unit_info;            // [batch, ustride]
     int32_t bt_stride, tt_stride, ustride, batch, n_models, page_size;
+    int32_t wait_first;             // wait for the previous kernel before reading and writing
     int32_t shared_len[SHKV_MAX_BATCH];   // L_b
     int32_t tail_len[SHKV_MAX_BATCH];     // T_bm at b * n_models + m
 };

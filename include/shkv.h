@@ -128,9 +128,11 @@ shkv_status shkv_append_kv(shkv_pool *pool, int32_t batch, int32_t n_new_tokens,
                            const void *k_new, const void *v_new, void *stream);
 
 /*
- * Bytes of device workspace shkv_decode_attention needs for this shape
- * (split-KV partials plus per-(request, KV head) arrival counters).
+ * Bytes of device workspace shkv_decode_attention needs for this shape: a
+ * region of SHKV_COUNT_REGION_BYTES at the front holding the per-(request,
+ * KV head) arrival counters of every call, then the split-KV partials.
  */
+#define SHKV_COUNT_REGION_BYTES (1u << 20)
 shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int32_t n_models,
                                        int32_t hq_per_model, size_t *bytes);
 
@@ -152,10 +154,11 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
  *   lse_out  device fp32 [batch, n_models * hq_per_model], or NULL
  *   workspace, workspace_bytes
  *            device scratch of at least shkv_decode_workspace_size() bytes.
- *            It must be zero-filled before its first use; every call that
- *            completes without device error bits leaves it zero-filled again,
- *            so it can be reused.  Calls sharing one workspace must not
- *            overlap on the GPU.
+ *            Its counter region (the first SHKV_COUNT_REGION_BYTES) must be
+ *            zero before its first use; every call that completes without
+ *            device error bits leaves it zero again and writes nothing else
+ *            there, so one workspace serves calls of any shape in turn.
+ *            Calls sharing one workspace must not overlap on the GPU.
  * Two interchangeable consumers implement the same result: warp-level
  * mma.sync tiles and, for head_dim 128, tcgen05 tiles with the accumulators
  * in tensor memory (tokens along the MMA's M dimension, 128-token stages).
@@ -164,7 +167,8 @@ shkv_status shkv_decode_workspace_size(const shkv_pool *pool, int32_t batch, int
  * allows it (no call reads the process environment).
  * Supported: batch in [1, SHKV_MAX_BATCH], every L_b >= 1,
  * hq_per_model % num_kv_heads == 0, rows per KV head
- * n_models * hq_per_model / num_kv_heads <= 64.
+ * n_models * hq_per_model / num_kv_heads <= 64,
+ * batch * num_kv_heads <= SHKV_COUNT_REGION_BYTES / 4.
  * Errors: SHKV_ERR_INVALID_ARG (null pointers, L_b == 0, shapes),
  * SHKV_ERR_UNSUPPORTED (outside the set above), SHKV_ERR_CUDA.
  */
@@ -238,8 +242,8 @@ shkv_status shkv_tails_get_lens(const shkv_tails *tails, int32_t batch, int32_t 
 shkv_status shkv_tails_append(shkv_tails *tails, int32_t batch, int32_t n_new_tokens, const void *k_new,
                               const void *v_new, void *stream);
 
-/* Workspace bytes for shkv_decode_attention_tails (zero-filled before the
- * first use, kept between calls). */
+/* Workspace bytes for shkv_decode_attention_tails (its counter region zero
+ * before the first use, as for shkv_decode_attention; kept between calls). */
 shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_tails *tails, int32_t batch,
                                              int32_t hq_per_model, size_t *bytes);
 
@@ -253,9 +257,11 @@ shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_t
  * the decode kernel streams every unit once for all N*G stacked rows, a tail
  * page being attended by its own decoder's G rows only.  The layout kernel
  * runs while the previous kernel of `stream` is still running (one warp per
- * request, beside that kernel's CTAs), into one of two buffers in
- * `workspace` that alternate between calls on the same workspace; it reads
- * the block and tail tables without waiting for that kernel.  So a kernel
+ * request, beside that kernel's CTAs), writing at one of two positions in
+ * `workspace`, the one that misses the tables of the previous call on the
+ * same workspace (when shapes changed so that neither does, it first waits
+ * for the previous kernel); it reads the block and tail tables without
+ * waiting for that kernel.  So a kernel
  * enqueued on `stream` before this call that writes those tables must not
  * let programmatic dependents start (griddepcontrol.launch_dependents /
  * cudaTriggerProgrammaticLaunchCompletion) before its writes; copies,

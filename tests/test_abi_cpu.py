@@ -169,3 +169,12 @@ def test_plan_rejects_bad_arguments(lib):
         with pytest.raises(N.ShkvError) as e:
             N.shkv_plan_decode(*args)
         assert e.value.status == status, args
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    for name in ("SHKV_MAX_BATCH", "SHKV_NOALLOC_SCRATCH_BYTES", "SHKV_COUNT_REGION_BYTES"):
+        m = re.search(rf"#define {name} \(?(\d+)u?(?: << (\d+))?\)?", text)
+        assert m, name
+        value = int(m.group(1)) << int(m.group(2) or 0)
+        assert getattr(N, name) == value, name

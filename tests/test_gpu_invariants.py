@@ -149,3 +149,42 @@ def test_host_argument_errors():
         pool.set_seq_lens([50, wl.max_pages_per_seq * wl.P + 1])
     assert e.value.status == N.SHKV_ERR_CAPACITY
     assert pool.check_errors() == 0
+
+
+def test_one_workspace_serves_calls_of_any_shape():
+    """Decodes of different batch sizes and stacked-row counts share one
+    workspace, back to back: every call's arrival counters sit in the fixed
+    counter region that nothing else writes, so a call never starts from
+    counters another call's partials left behind, and each matches the
+    oracle."""
+    import oracle
+    rng = np.random.default_rng(23)
+    cases = [setup([300, 2049, 64, 5000], seed=31, **LLAMA),
+             setup([int(x) for x in rng.integers(1, 6000, size=40)], seed=32, **QWEN14),
+             setup([9000, 17, 4000], seed=33, N=4, Hq=32, Hkv=8, D=128, P=16)]
+    need = 0
+    for wl, q, k, v, pool in cases:
+        need = max(need, N.shkv_decode_workspace_size(pool.handle, wl.B, wl.N, wl.Hq))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    qts = [bits_to_torch(c[1]) for c in cases]
+    order = [0, 1, 2, 0, 2, 1, 1, 0]
+    runs = []
+    for c in order:
+        wl = cases[c][0]
+        runs.append((c, torch.empty_like(qts[c]), torch.empty((wl.B, wl.N * wl.Hq), dtype=torch.float32,
+                                                              device="cuda")))
+    torch.cuda.synchronize()
+    for c, out, lse in runs:
+        wl, pool = cases[c][0], cases[c][4]
+        N.shkv_decode_attention(pool.handle, wl.B, wl.N, wl.Hq, qts[c].data_ptr(), float(wl.scale), out.data_ptr(),
+                                lse.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    torch.cuda.synchronize()
+    refs = []
+    for wl, q, k, v, pool in cases:
+        assert pool.check_errors() == 0
+        refs.append(oracle.decode_attention(q, k, v, wl.block_table, wl.lens_final, n_models=wl.N, hq=wl.Hq,
+                                            scale=wl.scale))
+    for i, (c, out, lse) in enumerate(runs):
+        compare(out, refs[c][0], lse, refs[c][1], what=f"call {i}")
+    counters = ws[: N.SHKV_COUNT_REGION_BYTES].view(torch.int32)
+    assert int(counters.abs().sum()) == 0          # the counter region is left zeroed

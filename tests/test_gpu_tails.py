@@ -181,27 +181,31 @@ def test_full_size_tails_sampled_requests(name):
 @pytest.mark.parametrize("shape", ["qwen8b", "llama8b"])
 def test_back_to_back_calls_on_one_workspace(shape):
     """A call's unit-layout kernel runs while the previous call's decode is
-    still running, into the other of two table buffers of the workspace.
-    Calls that alternate between two pools (different units) on one shared
-    workspace, enqueued with no synchronisation between them, each give their
-    own oracle result."""
+    still running, writing its tables where the previous call's are not (or
+    waiting first when shapes leave no such place).  Calls that cycle through
+    three pools of different shapes (batch, strides, so different table
+    positions) on one shared workspace, enqueued with no synchronisation
+    between them, each give their own oracle result."""
     rng = np.random.default_rng(17)
     n = SHAPES[shape]["N"]
     cases = [setup(shape, [300, 2049, 64, 5000], rng.integers(0, 400, size=(4, n)), seed=5),
-             setup(shape, [4000, 17, 900], rng.integers(0, 700, size=(3, n)), seed=9)]
+             setup(shape, [4000, 17, 900], rng.integers(0, 700, size=(3, n)), seed=9),
+             setup(shape, [int(x) for x in rng.integers(1, 3000, size=12)], rng.integers(0, 1500, size=(12, n)),
+                   seed=11)]
+    order = [0, 1, 0, 2, 1, 2, 0, 0, 2, 2, 1, 0]
     need = 0
     for wl, tt, tl, q, k, v, pool, tob in cases:
         need = max(need, N.shkv_decode_tails_workspace_size(pool.handle, tob.handle, wl.B, wl.Hq))
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     qts = [bits_to_torch(c[3]) for c in cases]
     runs = []
-    for i in range(8):
-        wl = cases[i % 2][0]
-        out = torch.empty_like(qts[i % 2])
+    for c in order:
+        wl = cases[c][0]
+        out = torch.empty_like(qts[c])
         lse = torch.empty((wl.B, wl.N * wl.Hq), dtype=torch.float32, device="cuda")
-        runs.append((i % 2, out, lse))
+        runs.append((c, out, lse))
     torch.cuda.synchronize()
-    for c, out, lse in runs:            # eight calls back to back, nothing between them
+    for c, out, lse in runs:            # twelve calls back to back, nothing between them
         wl, pool, tob = cases[c][0], cases[c][6], cases[c][7]
         N.shkv_decode_attention_tails(pool.handle, tob.handle, wl.B, wl.Hq, qts[c].data_ptr(), float(wl.scale),
                                       out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), None)
@@ -213,6 +217,6 @@ def test_back_to_back_calls_on_one_workspace(shape):
                                                   hq=wl.Hq, scale=wl.scale))
     for i, (c, out, lse) in enumerate(runs):
         compare(out, refs[c][0], lse, refs[c][1], what=f"call {i}")
-    for c in range(2):     # every call of a case gives the same bits
+    for c in range(len(cases)):     # every call of a case gives the same bits
         same = [r for r in runs if r[0] == c]
         assert all(torch.equal(r[1], same[0][1]) and torch.equal(r[2], same[0][2]) for r in same)
