@@ -504,7 +504,7 @@ def run_gpu_tails(args):
     value = job_throughput_gbs(nbytes, args.steps, 1, ms * 1e-3)
 
     # end to end through the C ABI: pinned host q in, host out back, per step
-    e_steps = max(10, min(args.steps, 1000))
+    e_steps = max(200, min(args.steps, 1000))     # host-timed: enough steps that a host stall is noise
     pipe = E2EPipeline(q, lambda qd, od: tails.decode_attention(qd, scale=wl.scale, out=od, lse=lse))
     e2e_step = pipe.step
 
