@@ -390,13 +390,19 @@ shkv_status build_plan(int32_t batch, const int32_t *lens, int32_t page_size, in
 // clears its counter) when consecutive calls change batch or shape.
 constexpr size_t kCountRegion = SHKV_COUNT_REGION_BYTES;
 
-size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms)
+// Bytes of the counter region: the fixed region, or (compact) only this
+// call's counters, for a scratch whose counters every call clears first.
+size_t count_region_bytes(int32_t batch, int32_t hkv, bool compact)
 {
-    (void)batch;
-    (void)hkv;
+    return compact ? align_up((uint32_t)(batch * hkv * 4), 256) : kCountRegion;
+}
+
+size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t head_dim, int32_t num_sms,
+                           bool compact = false)
+{
     const size_t lse = align_up((uint32_t)(2 * num_sms * rows * 4), 256);
     const size_t part = (size_t)2 * num_sms * rows * head_dim * 4;
-    return kCountRegion + lse + part;
+    return count_region_bytes(batch, hkv, compact) + lse + part;
 }
 
 shkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SHKV_OK : SHKV_ERR_CUDA; }
@@ -651,7 +657,7 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
         return SHKV_ERR_UNSUPPORTED;
     if ((int64_t)batch * c.num_kv_heads * 4 > (int64_t)kCountRegion)
         return SHKV_ERR_UNSUPPORTED;
-    if (workspace_bytes < workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim, pool->num_sms))
+    if (workspace_bytes < workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim, pool->num_sms, clear_counters))
         return SHKV_ERR_INVALID_ARG;
 
     const bool use_umma = use_umma_consumer(rows, c.head_dim, pool->consumer);
@@ -704,8 +710,9 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     p.seq_lens = c.seq_lens;
     p.err = c.error_word;
     p.ws_count = reinterpret_cast<uint32_t *>(ws);
-    p.ws_lse = reinterpret_cast<float *>(ws + kCountRegion);
-    p.ws_part = reinterpret_cast<float *>(ws + kCountRegion + lse_bytes);
+    const size_t count_region = count_region_bytes(batch, c.num_kv_heads, clear_counters);
+    p.ws_lse = reinterpret_cast<float *>(ws + count_region);
+    p.ws_part = reinterpret_cast<float *>(ws + count_region + lse_bytes);
     p.batch = batch;
     p.n_models = n_models;
     p.hq = hq_per_model;
@@ -1220,12 +1227,18 @@ extern "C" shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t ba
 {
     if (!pool || !out)
         return SHKV_ERR_INVALID_ARG;
-    size_t need = 0;
-    shkv_status st = shkv_decode_workspace_size(pool, batch, n_models, hq_per_model, &need);
-    if (st != SHKV_OK)
-        return st;
+    if (batch < 1 || n_models < 1 || hq_per_model < 1)
+        return SHKV_ERR_INVALID_ARG;
+    if (hq_per_model % pool->cfg.num_kv_heads)
+        return SHKV_ERR_UNSUPPORTED;
+    // the scratch's counters are cleared by every call, so it takes only this
+    // call's counters in front of the partials (the compact layout)
+    const int32_t rows = n_models * (hq_per_model / pool->cfg.num_kv_heads);
+    const size_t need = workspace_bytes_for(batch, pool->cfg.num_kv_heads, rows, pool->cfg.head_dim, pool->num_sms,
+                                            /*compact=*/true);
     if (need > (size_t)SHKV_NOALLOC_SCRATCH_BYTES)
         return SHKV_ERR_UNSUPPORTED;
+    shkv_status st;
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess)
         return SHKV_ERR_CUDA;

@@ -459,9 +459,11 @@ shkv_status shkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t pag
  *     contents; calls whose executions overlap on the GPU (different streams
  *     without ordering) race on it and give wrong results.
  * Errors: those of shkv_decode_attention; SHKV_ERR_UNSUPPORTED if the scratch
- * this shape needs (shkv_decode_workspace_size) exceeds
- * SHKV_NOALLOC_SCRATCH_BYTES; SHKV_ERR_INVALID_ARG if the current device is
- * not the pool's.
+ * this shape needs exceeds SHKV_NOALLOC_SCRATCH_BYTES (that is
+ * shkv_decode_workspace_size less its counter region, plus this call's
+ * batch * num_kv_heads counters rounded up to 256 bytes: the scratch's
+ * counters are cleared by every call); SHKV_ERR_INVALID_ARG if the current
+ * device is not the pool's.
  */
 shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t batch, int32_t n_models,
                                           int32_t hq_per_model, const void *q, float scale,
