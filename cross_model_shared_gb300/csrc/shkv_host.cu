@@ -757,7 +757,7 @@ TailsWorkspace tails_workspace(const shkv_pool *pool, const shkv_tails *tails, i
                                             pool->num_sms));
     w.stride = (size_t)c.max_pages_per_seq + (size_t)tails->n_models * tails->max_tail_pages;
     w.table = align256((size_t)batch * w.stride * 4);
-    w.total = w.decode + 4 * w.table;          // two buffers of (unit table, page words)
+    w.total = w.decode + 4 * w.table;          // room for two positions of (unit table, page words)
     return w;
 }
 
