@@ -162,28 +162,44 @@ __global__ void __maxnreg__(32) shkv_tails_unit_kernel(const __grid_constant__ T
     int U = S;
     for (int m = 0; m < p.n_models; ++m)
         U += (p.tail_len[b * p.n_models + m] + P - 1) / P;
-    for (int j = threadIdx.x; j < U; j += 32) {
-        int id, cnt;
-        uint32_t dec = kAllDecoders;
-        if (j < S) {
-            id = __ldcg(p.block_table + (int64_t)b * p.bt_stride + j);
-            cnt = j == S - 1 ? L - j * P : P;
-        } else {
-            int jt = j - S, m = 0;
-            for (;; ++m) {
-                const int pages = (p.tail_len[b * p.n_models + m] + P - 1) / P;
-                if (jt < pages)
-                    break;
-                jt -= pages;
+    // three entries a lane per pass (four spill at 32 registers), their
+    // table loads issued before any store
+    constexpr int kUnroll = 3;
+    for (int j0 = threadIdx.x; j0 < U; j0 += 32 * kUnroll) {
+        int id[kUnroll];
+        uint32_t info[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = j0 + 32 * u;
+            id[u] = -1;
+            info[u] = 0;
+            if (j >= U)
+                continue;
+            if (j < S) {
+                id[u] = __ldcg(p.block_table + (int64_t)b * p.bt_stride + j);
+                info[u] = (uint32_t)(j == S - 1 ? L - j * P : P) | (kAllDecoders << 8);
+            } else {
+                int jt = j - S, m = 0;
+                for (;; ++m) {
+                    const int pages = (p.tail_len[b * p.n_models + m] + P - 1) / P;
+                    if (jt < pages)
+                        break;
+                    jt -= pages;
+                }
+                const int T = p.tail_len[b * p.n_models + m];
+                const int pages = (T + P - 1) / P;
+                id[u] = __ldcg(p.tail_table + ((int64_t)b * p.n_models + m) * p.tt_stride + jt);
+                info[u] = (uint32_t)(jt == pages - 1 ? T - jt * P : P) | ((uint32_t)m << 8);
             }
-            const int T = p.tail_len[b * p.n_models + m];
-            const int pages = (T + P - 1) / P;
-            id = __ldcg(p.tail_table + ((int64_t)b * p.n_models + m) * p.tt_stride + jt);
-            cnt = jt == pages - 1 ? T - jt * P : P;
-            dec = (uint32_t)m;
         }
-        p.unit_table[(int64_t)b * p.ustride + j] = id;
-        p.unit_info[(int64_t)b * p.ustride + j] = (uint32_t)cnt | (dec << 8);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = j0 + 32 * u;
+            if (j < U) {
+                p.unit_table[(int64_t)b * p.ustride + j] = id[u];
+                p.unit_info[(int64_t)b * p.ustride + j] = info[u];
+            }
+        }
     }
     pdl_wait_prior();
 }
