@@ -564,7 +564,7 @@ def run_gpu_tails(args):
         "pct_of_hbm_peak": {"measured_copy": 100 * per_gpu / peak, "nominal_8tbs": 100 * per_gpu / NOMINAL_HBM_GBS},
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
                      "peak_kind": peak_kind, "traffic": None, "kernel": KERNELS[consumer]["name"],
-                     "consumer": consumer, "note": "whole step: tail pass + shared pass + merge"},
+                     "consumer": consumer, "note": "whole step: the unit-table kernel and one decode pass over shared pages and tails"},
         "unshared": None,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q.numel() * 2,
                 "d2h_bytes_per_step": q.numel() * 2, "steps": e_steps,

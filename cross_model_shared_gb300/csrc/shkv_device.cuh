@@ -33,7 +33,10 @@ constexpr int kMaxStages = SHKV_MAX_STAGES;
 // Consumer warps per row group, by number of row groups (1..4).  Fewer warps
 // than ring slots keeps most of the ring in flight while warps compute.
 #ifndef SHKV_WT_NT1
-#define SHKV_WT_NT1 4          // rows per warp = 8 (R <= 8)
+#define SHKV_WT_NT1 6          // rows per warp = 8 (R <= 8); the per-decoder-tails
+                               // instantiation needs the extra warps, and the
+                               // plain one takes the same count so that both
+                               // combine a unit's stages in the same order
 #endif
 #ifndef SHKV_WT_NRG1
 #define SHKV_WT_NRG1 3         // rows per warp = 16, one row group
