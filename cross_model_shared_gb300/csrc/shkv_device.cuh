@@ -57,7 +57,11 @@ constexpr int kMaxStages = SHKV_MAX_STAGES;
 #define SHKV_STAGES_PER_ISSUE 4
 #endif
 constexpr int kStagesPerIssue = SHKV_STAGES_PER_ISSUE;
-static_assert(kStagesPerIssue >= 1 && kStagesPerIssue <= 8, "stages per issue in [1, 8]");
+// The producer takes page ids from a 32-entry block-table window that moves
+// by 32 pages, so the pages of one issue pass (1 or 2 a stage) must divide
+// 32: a pass that straddles the window's end would read wrapped entries.
+static_assert(kStagesPerIssue == 1 || kStagesPerIssue == 2 || kStagesPerIssue == 4 || kStagesPerIssue == 8,
+              "stages per issue: 1, 2, 4 or 8");
 constexpr int kWtOfNrg[5] = {0, SHKV_WT_NRG1, SHKV_WT_NRG2, SHKV_WT_NRG3, SHKV_WT_NRG4};
 // More than 16 stacked rows: use 8-row groups (no padding of R to 16) when
 // set, else 16-row groups.  8-row groups take up to kNt1MultiWarps consumer
