@@ -15,12 +15,14 @@
 //   S_X[r, key]  = sum_d Q_X[r, d] K[key, d]      M = 128 rows, N = 128 keys
 //   O_X[r, d]   += sum_key P_X[r, key] V[key, d]  M = 128 rows, N = 128 = D
 // TMEM holds S_A, S_B, O_A, O_B (128 columns each).  A softmax thread owns one
-// row of one tile (its TMEM lane): per 64-key half it loads the scores into
-// registers, takes their maximum, exponentiates them against its running
-// maximum and writes P (bf16 pairs) over the S columns it has read, from
-// where the PV product reads it.  The running maximum moves only when a half's
-// maximum exceeds it by more than 2^kPRescaleLog2; the thread then rescales
-// its row of O (and, in the second half, the P it wrote for the first).  The
+// row of one tile (its TMEM lane): per stage it loads the row's 128 scores
+// into registers, exponentiates them against its running maximum and writes P
+// (bf16 pairs) over the first 64 columns of S, from where the PV product
+// reads it.  Where every score of a warp's rows is visible and the running
+// maxima are set, no stage maximum is taken; a row whose stage sum of P
+// exceeds 2^16 (or is not finite) sends its warp through the exact path:
+// mask, stage maximum, and a rescale of O and of the sum when the maximum
+// moves by more than 2^kPRescaleLog2, then P again.  The
 // two tiles keep the tensor core busy in turn: while one tile's softmax runs,
 // the other tile's PV and next QK do.  Key stages past a tile's last position
 // are skipped for that tile (and never loaded past the pair's last position);
