@@ -22,7 +22,9 @@
 //              the stacked rows; each thread keeps fp32 row sums for its
 //              token, reduced across the CTA at a segment end.  P^T (bf16)
 //              is written over the stage's K tile, which the QK MMA no
-//              longer needs.  At a segment end the same split reads O^T.
+//              longer needs; at 16 padded rows it has a buffer of its own
+//              instead, so a slot's K half is refilled as soon as its QK
+//              product completes.  At a segment end the same split reads O^T.
 //   warp 8     QK issuer (one lane): S^T of each stage as soon as its data
 //              has landed and an S buffer is free.
 //   warp 9     K producer: TMA of each page's two K column halves (one copy
