@@ -209,25 +209,6 @@ cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream)
     return launch_pdl(shkv_tails_unit_kernel, p.batch, 32, 0u, stream, p);
 }
 
-// dst[i] = value for i < n (grid-stride).
-__global__ void __launch_bounds__(256) shkv_fill_kernel(float *__restrict__ dst, int64_t n, float value)
-{
-    pdl_wait_prior();
-    pdl_launch_dependents();
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = value;
-}
-
-cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream)
-{
-    if (n <= 0)
-        return cudaSuccess;
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 1024)
-        blocks = 1024;
-    return launch_pdl(shkv_fill_kernel, (int)blocks, 256, 0u, stream, dst, n, value);
-}
-
 cudaError_t launch_merge(int n_splits, int batch, int rows, int head_dim, const float *o_part,
                          const float *lse_part, __nv_bfloat16 *out, float *lse_out, cudaStream_t stream)
 {

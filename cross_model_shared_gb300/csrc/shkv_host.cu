@@ -26,7 +26,6 @@ cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, c
 int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
-cudaError_t launch_fill_f32(float *dst, int64_t n, float value, cudaStream_t stream);
 cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream);
 int prefill_tiles_per_cta();
 uint32_t prefill_smem_bytes();
@@ -407,6 +406,96 @@ size_t workspace_bytes_for(int32_t batch, int32_t hkv, int32_t rows, int32_t hea
 
 shkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SHKV_OK : SHKV_ERR_CUDA; }
 
+// Device bytes [lo, hi).
+struct Span {
+    uintptr_t lo, hi;
+};
+
+Span span_of(const void *p, size_t bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, p ? a + bytes : a};
+}
+
+// The device bytes that the library's last kernel-launching call on each
+// stream reads or writes (its workspace bytes, queries, outputs, tables).
+// Every library kernel lets the next kernel of its stream start once it has
+// passed its own wait, so when a tails call's layout kernel starts, that
+// call's last kernel may still run while everything before it has
+// completed.  The layout kernel writes its tables before waiting only at an
+// offset of its workspace whose bytes miss all of these spans, whatever
+// pointer the earlier call used for them; when none fits, or the stream has
+// no record, it waits for the previous kernel first.  A small table keyed by
+// stream, least recently used out after 64 others (a stream whose record
+// was dropped just waits).
+struct StreamUse {
+    static constexpr int kMaxSpans = 8;
+    struct Entry {
+        const void *stream;
+        uint64_t used;
+        int n;
+        Span s[kMaxSpans];
+    };
+    std::mutex mu;
+    std::vector<Entry> entries;
+    uint64_t clock = 0;
+
+    // Offset of `bytes` of tables in workspace `ws` of `limit` bytes, at or
+    // after `d` (this call's decode part), for a call on `stream`.
+    size_t place(const void *stream, const uint8_t *ws, size_t d, size_t bytes, size_t limit, bool *wait_first)
+    {
+        std::lock_guard<std::mutex> g(mu);
+        *wait_first = true;
+        const uintptr_t base = reinterpret_cast<uintptr_t>(ws);
+        for (const Entry &e : entries) {
+            if (e.stream != stream)
+                continue;
+            std::vector<size_t> cands{d};
+            for (int i = 0; i < e.n; ++i)
+                if (e.s[i].hi > base + d && e.s[i].hi - base <= limit)
+                    cands.push_back((e.s[i].hi - base + 255) / 256 * 256);
+            if (limit >= bytes)
+                cands.push_back((limit - bytes) / 256 * 256);
+            std::sort(cands.begin(), cands.end());
+            for (size_t c : cands) {
+                if (c < d || c + bytes > limit)
+                    continue;
+                bool clear = true;
+                for (int i = 0; i < e.n && clear; ++i)
+                    clear = e.s[i].hi <= base + c || e.s[i].lo >= base + c + bytes;
+                if (clear) {
+                    *wait_first = false;
+                    return c;
+                }
+            }
+            return d;
+        }
+        return d;
+    }
+    // After a call on `stream` enqueued at least one kernel: the spans it
+    // touches (empty spans are skipped).
+    void record(const void *stream, std::initializer_list<Span> spans)
+    {
+        std::lock_guard<std::mutex> g(mu);
+        Entry rec{stream, ++clock, 0, {}};
+        for (const Span &s : spans)
+            if (s.hi > s.lo && rec.n < kMaxSpans)
+                rec.s[rec.n++] = s;
+        for (Entry &e : entries)
+            if (e.stream == stream) {
+                e = rec;
+                return;
+            }
+        if (entries.size() >= 64) {
+            auto lru = std::min_element(entries.begin(), entries.end(),
+                                        [](const Entry &x, const Entry &y) { return x.used < y.used; });
+            entries.erase(lru);
+        }
+        entries.push_back(rec);
+    }
+};
+StreamUse g_stream_use;
+
 // Launch shape of the decode kernel for R stacked rows per KV head.
 struct DecodeShape {
     int nt, nrg, wt, rpad;
@@ -592,6 +681,8 @@ shkv_status shkv_append_kv(shkv_pool *pool, int32_t batch, int32_t n_new_tokens,
     cudaError_t e = launch_append(p, pool->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return SHKV_ERR_CUDA;
+    const size_t new_bytes = (size_t)batch * n_new_tokens * c.num_kv_heads * c.head_dim * 2;
+    g_stream_use.record(stream, {span_of(k_new, new_bytes), span_of(v_new, new_bytes)});
     for (int b = 0; b < batch; ++b)
         pool->lens[b] += n_new_tokens;
     return SHKV_OK;
@@ -617,6 +708,7 @@ namespace {
 // Units of a decode with per-decoder tails in one pass: the unit table and
 // page info built on the device, their row stride, and each request's unit
 // length in tokens (whole pages), which the split plan is built from.
+
 struct FusedUnits {
     const int32_t *table;
     const uint32_t *info;
@@ -636,7 +728,8 @@ struct FusedUnits {
 shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
                         float scale, void *out, float *out_f32, float *lse_out, void *workspace,
                         size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr,
-                        bool clear_counters = false, const std::function<cudaError_t()> *before_launch = nullptr)
+                        bool clear_counters = false, const std::function<cudaError_t()> *before_launch = nullptr,
+                        Span tables = {0, 0})
 {
     if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
         hq_per_model < 1)
@@ -738,6 +831,13 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     cudaError_t e = use_umma ? launch_decode_umma(pool->tm_k2, pool->tm_v2, p, smem_bytes, (cudaStream_t)stream)
                              : launch_decode(c.head_dim, sh.nt, pool->tm_k, pool->tm_v, p, smem_bytes,
                                              (cudaStream_t)stream);
+    // what this call's kernels touch, for a tails call after it on the stream
+    // (recorded also when the decode launch failed after the unit kernel's)
+    const size_t qrows = (size_t)batch * n_models * hq_per_model;
+    g_stream_use.record(stream, {span_of(workspace, workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim,
+                                                                        pool->num_sms, clear_counters)),
+                                 span_of(q, qrows * c.head_dim * 2), span_of(out, qrows * c.head_dim * 2),
+                                 span_of(out_f32, qrows * c.head_dim * 4), span_of(lse_out, qrows * 4), tables});
     return cuda_status(e);
 }
 
@@ -761,62 +861,6 @@ TailsWorkspace tails_workspace(const shkv_pool *pool, const shkv_tails *tails, i
     return w;
 }
 
-// What the last decode call on each workspace uses: [0, decode_end) (its
-// counters, lse and partials) and, for a call with per-decoder tails, its unit
-// table and page words [tab_lo, tab_hi).  A tails call's unit kernel runs
-// while the previous kernel of the stream still does, so it writes its
-// tables where the last call on the same workspace keeps nothing: the first
-// of its candidate positions that misses both ranges and fits; when none does
-// (shapes changed), the unit kernel waits for the previous kernel first.  A
-// small table keyed by workspace address, least recently used out after 64
-// others.
-struct WorkspaceUse {
-    struct Entry {
-        const void *ws;
-        uint64_t used;
-        size_t decode_end, tab_lo, tab_hi;
-    };
-    std::mutex mu;
-    std::vector<Entry> entries;
-    uint64_t clock = 0;
-
-    // Offset of `bytes` of tables for a call whose decode part takes d bytes
-    // of a workspace of `limit` bytes (d + 2 * bytes <= limit).
-    size_t place(const void *ws, size_t d, size_t bytes, size_t limit, bool *wait_first)
-    {
-        std::lock_guard<std::mutex> g(mu);
-        *wait_first = false;
-        for (const Entry &e : entries)
-            if (e.ws == ws) {
-                const size_t past = std::max(d, e.decode_end);
-                const size_t cands[] = {d, d + bytes, past, past + bytes, std::max(e.tab_hi, d),
-                                        limit >= bytes ? (limit - bytes) / 256 * 256 : 0};
-                for (size_t c : cands)
-                    if (c >= d && c + bytes <= limit && c >= e.decode_end && (c + bytes <= e.tab_lo || c >= e.tab_hi))
-                        return c;
-                *wait_first = true;
-                return d;
-            }
-        return d;
-    }
-    void used(const void *ws, size_t decode_end, size_t tab_lo, size_t tab_hi)
-    {
-        std::lock_guard<std::mutex> g(mu);
-        ++clock;
-        for (Entry &e : entries)
-            if (e.ws == ws) {
-                e = {ws, clock, decode_end, tab_lo, tab_hi};
-                return;
-            }
-        if (entries.size() >= 64) {
-            auto lru = std::min_element(entries.begin(), entries.end(),
-                                        [](const Entry &x, const Entry &y) { return x.used < y.used; });
-            entries.erase(lru);
-        }
-        entries.push_back({ws, clock, decode_end, tab_lo, tab_hi});
-    }
-};
-WorkspaceUse g_workspace_use;
 
 }  // namespace
 
@@ -828,16 +872,8 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
 {
     if (!out)
         return SHKV_ERR_INVALID_ARG;
-    const shkv_status st = decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out,
-                                       workspace, workspace_bytes, stream);
-    if (st == SHKV_OK) {     // the bytes a tails call after this one must leave alone while it runs
-        const int32_t rows = n_models * (hq_per_model / pool->cfg.num_kv_heads);
-        g_workspace_use.used(workspace,
-                             workspace_bytes_for(batch, pool->cfg.num_kv_heads, rows, pool->cfg.head_dim,
-                                                 pool->num_sms),
-                             0, 0);
-    }
-    return st;
+    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, workspace,
+                       workspace_bytes, stream);
 }
 
 shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new, int32_t hq_per_model,
@@ -886,8 +922,14 @@ shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new
     const int64_t grid = (int64_t)batch * c.num_kv_heads * ((p.tiles + per_cta - 1) / per_cta);
     if (grid > INT32_MAX)
         return SHKV_ERR_UNSUPPORTED;
-    return cuda_status(launch_prefill_umma(pool->tm_k2, pool->tm_v2, p, prefill_smem_bytes(), (int)grid,
-                                           (cudaStream_t)stream));
+    const cudaError_t e =
+        launch_prefill_umma(pool->tm_k2, pool->tm_v2, p, prefill_smem_bytes(), (int)grid, (cudaStream_t)stream);
+    if (e == cudaSuccess) {
+        const size_t qrows = (size_t)batch * n_new * hq_per_model;
+        g_stream_use.record(stream, {span_of(q, qrows * c.head_dim * 2), span_of(out, qrows * c.head_dim * 2),
+                                     span_of(lse_out, qrows * 4)});
+    }
+    return cuda_status(e);
 }
 
 shkv_status shkv_tails_create(shkv_pool *pool, const shkv_tails_config *tc, shkv_tails **out)
@@ -1010,7 +1052,7 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     bool wait_first = false;
-    const size_t off = g_workspace_use.place(workspace, w.decode, 2 * w.table, workspace_bytes, &wait_first);
+    const size_t off = g_stream_use.place(stream, ws, w.decode, 2 * w.table, workspace_bytes, &wait_first);
     up.block_table = pool->cfg.block_table;
     up.tail_table = tails->view->cfg.block_table;
     up.unit_table = reinterpret_cast<int32_t *>(ws + off);
@@ -1025,19 +1067,10 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
     // the unit kernel is enqueued right before the decode, once every check
     // of the decode has passed (never alone, so the last tables a workspace
     // recorded are the ones its last decode reads)
-    bool launched = false;
-    const std::function<cudaError_t()> units = [&]() {
-        const cudaError_t e = launch_tails_units(up, (cudaStream_t)stream);
-        launched = e == cudaSuccess;
-        return e;
-    };
+    const std::function<cudaError_t()> units = [&]() { return launch_tails_units(up, (cudaStream_t)stream); };
     const FusedUnits fu{up.unit_table, up.unit_info, up.ustride, unit_tokens.data()};
-    const shkv_status st =
-        decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu, false,
-                    &units);
-    if (launched)
-        g_workspace_use.used(workspace, w.decode, off, off + 2 * w.table);
-    return st;
+    return decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu,
+                       false, &units, span_of(ws + off, 2 * w.table));
 }
 
 shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)
@@ -1072,6 +1105,11 @@ shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, in
         return SHKV_ERR_INVALID_ARG;
     cudaError_t e = launch_merge(n_splits, batch, rows, head_dim, o_part, lse_part,
                                  static_cast<__nv_bfloat16 *>(out), lse_out, (cudaStream_t)stream);
+    const size_t nrow = (size_t)batch * rows;
+    if (e == cudaSuccess && nrow > 0)
+        g_stream_use.record(stream, {span_of(o_part, n_splits * nrow * head_dim * 4),
+                                     span_of(lse_part, n_splits * nrow * 4), span_of(out, nrow * head_dim * 2),
+                                     span_of(lse_out, nrow * 4)});
     return cuda_status(e);
 }
 

@@ -257,16 +257,18 @@ shkv_status shkv_decode_tails_workspace_size(const shkv_pool *pool, const shkv_t
  * the decode kernel streams every unit once for all N*G stacked rows, a tail
  * page being attended by its own decoder's G rows only.  The layout kernel
  * runs while the previous kernel of `stream` is still running (one warp per
- * request, beside that kernel's CTAs), writing at one of two positions in
- * `workspace`, the one that misses the tables of the previous call on the
- * same workspace (when shapes changed so that neither does, it first waits
- * for the previous kernel); it reads the block and tail tables without
- * waiting for that kernel.  So a kernel
- * enqueued on `stream` before this call that writes those tables must not
- * let programmatic dependents start (griddepcontrol.launch_dependents /
- * cudaTriggerProgrammaticLaunchCompletion) before its writes; copies,
- * kernels launched without programmatic stream serialization and this
- * library's own kernels are fine.  Supported:
+ * request, beside that kernel's CTAs).  It writes its tables at an offset of
+ * `workspace` whose bytes miss every buffer that this library's previous
+ * call on `stream` reads or writes (that call's workspace bytes, queries,
+ * outputs, tables, appended K/V, merge inputs), under whatever pointers; when
+ * no offset does, or the library has no record of a call on `stream`, it
+ * first waits for the previous kernel.  It reads the block and tail tables
+ * without waiting for that kernel.  So a kernel enqueued on `stream` right
+ * before this call that lets programmatic dependents start
+ * (griddepcontrol.launch_dependents / cudaTriggerProgrammaticLaunchCompletion)
+ * must by then be done writing those tables and done with any bytes of
+ * `workspace`; copies, kernels launched without programmatic stream
+ * serialization and this library's own kernels are fine.  Supported:
  * batch * n_models <= SHKV_MAX_BATCH, n_models <= 254, rest as
  * shkv_decode_attention.  Errors as shkv_decode_attention (the device copies
  * of the lengths are not compared: SHKV_ERRF_SEQ_LEN is not raised here).

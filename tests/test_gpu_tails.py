@@ -220,3 +220,48 @@ def test_back_to_back_calls_on_one_workspace(shape):
     for c in range(len(cases)):     # every call of a case gives the same bits
         same = [r for r in runs if r[0] == c]
         assert all(torch.equal(r[1], same[0][1]) and torch.equal(r[2], same[0][2]) for r in same)
+
+
+@pytest.mark.parametrize("shape", ["qwen8b", "llama8b"])
+def test_next_call_workspace_over_the_running_calls_workspace(shape):
+    """Stream order lets a call use, as its workspace, bytes that the previous
+    call is still using under another pointer, so long as its own counter
+    region starts zeroed.  Here call B's workspace starts below call A's, so
+    that B's first table position is A's counter region, while A's decode is
+    still running when B's unit-layout kernel starts.  That kernel writes
+    before waiting, so it must find a position clear of every byte A's
+    kernels touch (or wait): both calls give the bits they give alone."""
+    rng = np.random.default_rng(29)
+    n = SHAPES[shape]["N"]
+    a = setup(shape, [9000, 12000, 7000, 15000], rng.integers(0, 400, size=(4, n)), seed=5)
+    b = setup(shape, [4000, 17, 900], rng.integers(0, 700, size=(3, n)), seed=9)
+
+    def run(case, ws_ptr, ws_bytes):
+        wl, pool, tob = case[0], case[6], case[7]
+        qt = bits_to_torch(case[3])
+        out = torch.empty_like(qt)
+        lse = torch.empty((wl.B, wl.N * wl.Hq), dtype=torch.float32, device="cuda")
+        N.shkv_decode_attention_tails(pool.handle, tob.handle, wl.B, wl.Hq, qt.data_ptr(), float(wl.scale),
+                                      out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, None)
+        return qt, out, lse
+
+    need = {id(c): N.shkv_decode_tails_workspace_size(c[6].handle, c[7].handle, c[0].B, c[0].Hq) for c in (a, b)}
+    alone = []
+    for c in (a, b):
+        ws = torch.zeros(need[id(c)], dtype=torch.uint8, device="cuda")
+        alone.append(run(c, ws.data_ptr(), ws.numel()))
+        torch.cuda.synchronize()
+    wlb = b[0]
+    d_b = -(-N.shkv_decode_workspace_size(b[6].handle, wlb.B, wlb.N, wlb.Hq) // 256) * 256   # B's decode part
+    a_off = d_b - 256                       # A's counters begin 256 bytes before B's first table position
+    arena = torch.zeros(max(a_off + need[id(a)], need[id(b)]) + 4096, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    ra = run(a, arena.data_ptr() + a_off, need[id(a)])
+    rb = run(b, arena.data_ptr(), need[id(b)])          # enqueued right behind A, nothing between them
+    torch.cuda.synchronize()
+    assert a[6].check_errors() == 0
+    for (q0, o0, l0), (q1, o1, l1), what in ((alone[0], ra, "A"), (alone[1], rb, "B")):
+        assert torch.equal(o0, o1) and torch.equal(l0, l1), what
+    ref = oracle.decode_attention_tails(a[3], a[4], a[5], a[0].block_table, a[0].lens_final, a[1], a[2],
+                                        n_models=a[0].N, hq=a[0].Hq, scale=a[0].scale)
+    compare(ra[1], ref[0], ra[2], ref[1], what="A")
