@@ -450,8 +450,6 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
                 const int d = mt * 16 + (lane >> 2) + (e >> 1) * 8;
                 if (!whole)
                     p.ws_part[orow * D + d] = acc;
-                else if (p.out_f32)
-                    p.out_f32[orow * D + d] = acc;
                 else
                     p.out[orow * D + d] = __float2bfloat16_rn(acc);
             }
@@ -517,10 +515,7 @@ __device__ void consumer(const DecodeParams &p, const Ctx &c)
 #pragma unroll
                     for (int h = 0; h < (D / 128 > 0 ? D / 128 : 1); ++h) {
                         const int d4 = lane + 32 * h;
-                        if (d4 < dq && p.out_f32) {
-                            reinterpret_cast<float4 *>(p.out_f32 + orow * D)[d4] =
-                                make_float4(acc[h].x * inv, acc[h].y * inv, acc[h].z * inv, acc[h].w * inv);
-                        } else if (d4 < dq) {
+                        if (d4 < dq) {
                             __nv_bfloat162 lo = __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
                             __nv_bfloat162 hi = __floats2bfloat162_rn(acc[h].z * inv, acc[h].w * inv);
                             uint2 packed;

@@ -907,8 +907,6 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     const float o = __uint_as_float(ov[i]) * scr[kScrSumHi * 64 + r];
                     if (!whole)
                         p.ws_part[((int64_t)slot_id * R + r) * kD + t] = o;
-                    else if (p.out_f32)
-                        p.out_f32[(row0 + rowoff[r]) * kD + t] = o;
                     else
                         p.out[(row0 + rowoff[r]) * kD + t] = __float2bfloat16_rn(o);
                 }
@@ -958,10 +956,7 @@ __device__ void tc_softmax(const DecodeParams &p, const TcCtx &c, uint32_t tmem)
                     }
                     const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
                     const int64_t orr = row0 + rowoff[rr];
-                    if (lane < dq && p.out_f32) {
-                        reinterpret_cast<float4 *>(p.out_f32 + orr * kD)[lane] =
-                            make_float4(acc.x * winv, acc.y * winv, acc.z * winv, acc.w * winv);
-                    } else if (lane < dq) {
+                    if (lane < dq) {
                         uint2 packed;
                         packed.x = pack_bf16x2(acc.x * winv, acc.y * winv);
                         packed.y = pack_bf16x2(acc.z * winv, acc.w * winv);

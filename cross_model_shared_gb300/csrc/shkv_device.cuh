@@ -109,8 +109,7 @@ constexpr int kSmemLimit = 232448;
 struct DecodeParams {
     const __nv_bfloat16 *q;    // [B, N*Hq, D]
     __nv_bfloat16 *out;        // [B, N*Hq, D]
-    float *out_f32;            // when set, final rows go here in fp32 instead of to out
-    float *lse_out;            // [B, N*Hq] or null (required with out_f32)
+    float *lse_out;            // [B, N*Hq] or null
     const int32_t *block_table;
     // Per-decoder tails in one pass: when set, a request's unit of pages is
     // its shared pages followed by each decoder's tail pages (block_table is

@@ -716,8 +716,7 @@ struct FusedUnits {
     const int32_t *unit_tokens;
 };
 
-// One decode launch: final rows to out (bf16) or, when out_f32 is set, to
-// out_f32 (fp32; lse_out then required).  Launches nothing when the pool has
+// One decode launch: final rows to out (bf16).  Launches nothing when the pool has
 // no chunks (every length zero, possible only for a tail view).  With fu,
 // request b's unit is fu's row b instead of the pool's block table.  With
 // clear_counters, once every check has passed, the workspace's arrival
@@ -726,15 +725,15 @@ struct FusedUnits {
 // every check has passed, right before the decode kernel is enqueued (the
 // tails path enqueues its unit kernel there); its error aborts the call.
 shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_t hq_per_model, const void *q,
-                        float scale, void *out, float *out_f32, float *lse_out, void *workspace,
+                        float scale, void *out, float *lse_out, void *workspace,
                         size_t workspace_bytes, void *stream, const FusedUnits *fu = nullptr,
                         bool clear_counters = false, const std::function<cudaError_t()> *before_launch = nullptr,
                         Span tables = {0, 0})
 {
-    if (!pool || !q || (!out && !out_f32) || (out_f32 && !lse_out) || !workspace || batch < 1 || n_models < 1 ||
+    if (!pool || !q || !out || !workspace || batch < 1 || n_models < 1 ||
         hq_per_model < 1)
         return SHKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(out_f32) || !aligned16(workspace) ||
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
         ((uintptr_t)lse_out & 3u))
         return SHKV_ERR_INVALID_ARG;
     if (!isfinite(scale))
@@ -795,7 +794,6 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     const size_t lse_bytes = align_up((uint32_t)(2 * pool->num_sms * rows * 4), 256);
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.out_f32 = out_f32;
     p.lse_out = lse_out;
     p.block_table = fu ? fu->table : c.block_table;
     p.page_info = fu ? fu->info : nullptr;
@@ -837,7 +835,7 @@ shkv_status decode_impl(shkv_pool *pool, int32_t batch, int32_t n_models, int32_
     g_stream_use.record(stream, {span_of(workspace, workspace_bytes_for(batch, c.num_kv_heads, rows, c.head_dim,
                                                                         pool->num_sms, clear_counters)),
                                  span_of(q, qrows * c.head_dim * 2), span_of(out, qrows * c.head_dim * 2),
-                                 span_of(out_f32, qrows * c.head_dim * 4), span_of(lse_out, qrows * 4), tables});
+                                 span_of(lse_out, qrows * 4), tables});
     return cuda_status(e);
 }
 
@@ -872,8 +870,8 @@ shkv_status shkv_decode_attention(shkv_pool *pool, int32_t batch, int32_t n_mode
 {
     if (!out)
         return SHKV_ERR_INVALID_ARG;
-    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, workspace,
-                       workspace_bytes, stream);
+    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, lse_out, workspace, workspace_bytes,
+                       stream);
 }
 
 shkv_status shkv_prefill_attention(shkv_pool *pool, int32_t batch, int32_t n_new, int32_t hq_per_model,
@@ -1069,8 +1067,8 @@ shkv_status shkv_decode_attention_tails(shkv_pool *pool, shkv_tails *tails, int3
     // recorded are the ones its last decode reads)
     const std::function<cudaError_t()> units = [&]() { return launch_tails_units(up, (cudaStream_t)stream); };
     const FusedUnits fu{up.unit_table, up.unit_info, up.ustride, unit_tokens.data()};
-    return decode_impl(pool, batch, N, hq_per_model, q, scale, out, nullptr, lse_out, ws, w.decode, stream, &fu,
-                       false, &units, span_of(ws + off, 2 * w.table));
+    return decode_impl(pool, batch, N, hq_per_model, q, scale, out, lse_out, ws, w.decode, stream, &fu, false,
+                       &units, span_of(ws + off, 2 * w.table));
 }
 
 shkv_status shkv_decode_consumer(const shkv_pool *pool, int32_t n_models, int32_t hq_per_model, int32_t *consumer)
@@ -1288,6 +1286,6 @@ extern "C" shkv_status shkv_decode_attention_noalloc(shkv_pool *pool, int32_t ba
         return st;
     // decode_impl checks every argument first, then zeroes the arrival
     // counters at the front of the scratch on `stream`, then launches
-    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, nullptr, lse_out, scratch, need, stream,
-                       nullptr, /*clear_counters=*/true);
+    return decode_impl(pool, batch, n_models, hq_per_model, q, scale, out, lse_out, scratch, need, stream, nullptr,
+                       /*clear_counters=*/true);
 }
