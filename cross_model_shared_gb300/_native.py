@@ -37,7 +37,7 @@ EXPORTS = [
     "shkv_decode_attention_tails", "shkv_pages_create", "shkv_pages_destroy", "shkv_pages_acquire",
     "shkv_pages_publish", "shkv_pages_release", "shkv_pages_alloc_transfer", "shkv_pages_stats",
     "shkv_pages_refcount", "shkv_prefill_attention", "shkv_pool_set_decode_consumer",
-    "shkv_partition_requests",
+    "shkv_partition_requests", "shkv_selftest_bounded_wait",
 ]
 
 SHKV_CONSUMER_AUTO = -1
@@ -118,6 +118,7 @@ def load() -> ctypes.CDLL:
         "shkv_decode_attention": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
         "shkv_splitkv_merge": [i32, i32, i32, i32, vp, vp, vp, vp, vp],
         "shkv_check_errors": [vp, vp, u32p],
+        "shkv_selftest_bounded_wait": [vp, vp],
         "shkv_plan_decode": [i32, i32p, i32, i32, i32, i32, i32, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "shkv_decode_attention_noalloc": [vp, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp],
         "shkv_decode_consumer": [vp, i32, i32, ctypes.POINTER(i32)],
@@ -209,6 +210,10 @@ def shkv_check_errors(pool: int, stream: int) -> int:
     if st not in (SHKV_OK, SHKV_ERR_DEVICE):
         raise ShkvError(st, "shkv_check_errors")
     return flags.value
+
+
+def shkv_selftest_bounded_wait(pool: int, stream: int) -> None:
+    _check(load().shkv_selftest_bounded_wait(pool, stream), "shkv_selftest_bounded_wait")
 
 
 def shkv_plan_decode(lens, page_size: int, num_kv_heads: int, n_models: int, hq_per_model: int, consumer: int,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libshkv.so")
-SOURCES = ["decode_attn.cu", "decode_umma.cu", "prefill_umma.cu", "append_merge.cu", "shkv_host.cu",
+SOURCES = ["decode_attn.cu", "decode_umma.cu", "prefill_umma.cu", "append_merge.cu", "selftest.cu", "shkv_host.cu",
            "page_manager.cpp", "shard.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -26,6 +26,7 @@ cudaError_t launch_decode_umma(const CUtensorMap &tmK, const CUtensorMap &tmV, c
 int umma_stages(int rows);
 uint32_t umma_smem_bytes(int rows, int stages);
 cudaError_t launch_append(const AppendParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t *err, cudaStream_t stream);
 cudaError_t launch_tails_units(const TailsUnitParams &p, cudaStream_t stream);
 int prefill_tiles_per_cta();
 uint32_t prefill_smem_bytes();
@@ -1109,6 +1110,13 @@ shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, in
                                      span_of(lse_part, n_splits * nrow * 4), span_of(out, nrow * head_dim * 2),
                                      span_of(lse_out, nrow * 4)});
     return cuda_status(e);
+}
+
+shkv_status shkv_selftest_bounded_wait(shkv_pool *pool, void *stream)
+{
+    if (!pool)
+        return SHKV_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_selftest(pool->cfg.error_word, (cudaStream_t)stream));
 }
 
 shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags)

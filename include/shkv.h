@@ -399,6 +399,20 @@ shkv_status shkv_splitkv_merge(int32_t n_splits, int32_t batch, int32_t rows, in
 shkv_status shkv_check_errors(shkv_pool *pool, void *stream, uint32_t *flags);
 
 /*
+ * Self-test of the bounded waits (no counterpart on the pages): enqueues on
+ * `stream` one small kernel whose only waiting thread waits, with the wait
+ * every kernel of this library uses, for a barrier that nothing completes.
+ * After the wait's limit (2 s of device time) it gives up, sets
+ * SHKV_ERRF_TIMEOUT in the pool's error word and the kernel exits; it reads
+ * and writes nothing else.  shkv_check_errors then reports the bit.  For
+ * checking on the device at hand that a stalled pipeline ends with an error
+ * status instead of a hang, and that the context stays usable after it.
+ * Errors: SHKV_ERR_INVALID_ARG for a null pool, SHKV_ERR_CUDA if the launch
+ * fails.
+ */
+shkv_status shkv_selftest_bounded_wait(shkv_pool *pool, void *stream);
+
+/*
  * Host-only view of how shkv_decode_attention divides work (no device
  * needed).  The (request, KV head, page) chunks, ordered request-major, are
  * cut into `num_ctas` contiguous, non-empty ranges, one per persistent CTA,

@@ -110,6 +110,27 @@ def test_out_of_range_page_sets_flag_and_is_skipped():
     assert pool.check_errors() == 0          # reading clears the word
 
 
+def test_a_stalled_wait_ends_with_the_timeout_flag():
+    """The library's waits are bounded: a kernel whose wait nothing completes
+    gives up after the limit (2 s of device time), sets SHKV_ERRF_TIMEOUT and
+    exits.  The host reads the bit, and the same context then decodes the
+    same bits as before."""
+    import time
+    wl, q, k, v, pool = setup([300, 2000], **LLAMA)
+    ref = pool.decode_attention(bits_to_torch(q), wl.N).clone()
+    assert pool.check_errors() == 0
+    t0 = time.perf_counter()
+    N.shkv_selftest_bounded_wait(pool.handle, None)
+    flags = pool.check_errors()
+    waited = time.perf_counter() - t0
+    assert flags == N.SHKV_ERRF_TIMEOUT
+    assert 1.9 < waited < 60.0
+    assert pool.check_errors() == 0
+    out = pool.decode_attention(bits_to_torch(q), wl.N)
+    assert pool.check_errors() == 0
+    assert torch.equal(out, ref)
+
+
 def test_device_length_disagreeing_with_host_copy_sets_flag():
     wl, q, k, v, pool = setup([300, 300], **LLAMA)
     pool.seq_lens[0] = 17                     # behind the pool's back
