@@ -451,14 +451,17 @@ struct StreamUse {
         for (const Entry &e : entries) {
             if (e.stream != stream)
                 continue;
-            std::vector<size_t> cands{d};
+            size_t cands[kMaxSpans + 2];
+            int nc = 0;
+            cands[nc++] = d;
             for (int i = 0; i < e.n; ++i)
                 if (e.s[i].hi > base + d && e.s[i].hi - base <= limit)
-                    cands.push_back((e.s[i].hi - base + 255) / 256 * 256);
+                    cands[nc++] = (e.s[i].hi - base + 255) / 256 * 256;
             if (limit >= bytes)
-                cands.push_back((limit - bytes) / 256 * 256);
-            std::sort(cands.begin(), cands.end());
-            for (size_t c : cands) {
+                cands[nc++] = (limit - bytes) / 256 * 256;
+            std::sort(cands, cands + nc);
+            for (int ci = 0; ci < nc; ++ci) {
+                const size_t c = cands[ci];
                 if (c < d || c + bytes > limit)
                     continue;
                 bool clear = true;
