@@ -459,20 +459,21 @@ struct StreamUse {
                     cands[nc++] = (e.s[i].hi - base + 255) / 256 * 256;
             if (limit >= bytes)
                 cands[nc++] = (limit - bytes) / 256 * 256;
-            std::sort(cands, cands + nc);
+            size_t best = limit;                 // the lowest candidate that fits and is clear
             for (int ci = 0; ci < nc; ++ci) {
                 const size_t c = cands[ci];
-                if (c < d || c + bytes > limit)
+                if (c < d || c + bytes > limit || c >= best)
                     continue;
                 bool clear = true;
                 for (int i = 0; i < e.n && clear; ++i)
                     clear = e.s[i].hi <= base + c || e.s[i].lo >= base + c + bytes;
-                if (clear) {
-                    *wait_first = false;
-                    return c;
-                }
+                if (clear)
+                    best = c;
             }
-            return d;
+            if (best == limit)
+                return d;
+            *wait_first = false;
+            return best;
         }
         return d;
     }
