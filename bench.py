@@ -890,7 +890,7 @@ def run_gpu(args):
         # of the dirty ones the write flush leaves behind
         flush32 = flush.view(torch.int32)
         for a, b in evs:
-            flush32.sum()
+            torch.amax(flush32)          # int32 max: reads the buffer, no cast, one tiny write
             a.record(stream)
             step()
             b.record(stream)
