@@ -23,6 +23,7 @@ SHAPES = {
     "qwen14b": dict(N=8, Hq=40, Hkv=8, D=128, P=32),      # shared pass R = 40 (tcgen05)
     "qwen8b": dict(N=4, Hq=32, Hkv=8, D=128, P=16),       # R = 16: tcgen05 with 16-token pages (two producers)
     "d64": dict(N=3, Hq=8, Hkv=2, D=64, P=16),            # head dim 64
+    "r8_p32": dict(N=2, Hq=32, Hkv=8, D=128, P=32),       # R = 8 (mma.sync) with one 32-token page a stage
 }
 
 
@@ -57,7 +58,7 @@ def test_tails_match_oracle(shape):
     compare(out, ref, lse, lref, what=f"tails {shape}")
 
 
-@pytest.mark.parametrize("shape", ["llama8b", "qwen14b"])
+@pytest.mark.parametrize("shape", ["llama8b", "qwen14b", "r8_p32"])
 def test_empty_tails_give_the_plain_decode_bits(shape):
     """Every tail empty: the merge has one live split with weight exactly 1,
     so the result is the shared decode's own bits."""
