@@ -50,6 +50,7 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.shkv_splitkv_merge(1, 1, 1, 6, 16, 16, 16, None, None) == N.SHKV_ERR_INVALID_ARG  # D % 4
     assert lib.shkv_pool_set_decode_consumer(None, 0) == N.SHKV_ERR_INVALID_ARG
     assert lib.shkv_decode_attention_noalloc(None, 1, 1, 1, None, 1.0, None, None, None) == N.SHKV_ERR_INVALID_ARG
+    assert lib.shkv_selftest_bounded_wait(None, None) == N.SHKV_ERR_INVALID_ARG
 
 
 def plan_costs(consumer, P, rows):
